@@ -1,0 +1,262 @@
+// api.cu -- the extern "C" entry points declared in include/vsa.h: argument checks, workspace
+// carving and the stream-ordered launch sequence of each operation.  Follows the host surface of
+// FastVideo's backward (compare main...vsa_bwd_fix, block_sparse_bwd_launch_sm100a.cuh:
+// block_sparse_bwd_supported returns an error for bad configurations; the launch chains
+// preprocess -> order -> main -> postprocess on one stream without a host sync) and the caller-
+// workspace contract of cudnn-frontend PR #926's follow-up (no allocation on the hot path).
+#include <climits>
+#include <cmath>
+
+#include "vsa_internal.cuh"
+
+namespace vsa {
+
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  int sms = 1;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = 1;
+  if (dev >= 0 && dev < 64) cached[dev] = sms;
+  return sms;
+}
+
+}  // namespace vsa
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+vsa_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return VSA_ERR_CUDA;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Shape rules: B, H >= 1; head_dim 128; S a positive multiple of 64; B*H*S rows addressable with
+// 32-bit TMA coordinates.
+vsa_status check_shape(const vsa_shape& s, int* nb) {
+  if (s.batch < 1 || s.heads < 1 || s.seqlen < 1) return VSA_ERR_INVALID_ARG;
+  if (s.head_dim != vsa::HEAD_DIM) return VSA_ERR_UNSUPPORTED;
+  if (s.seqlen % vsa::BLOCK != 0) return VSA_ERR_UNSUPPORTED;
+  const long long rows = static_cast<long long>(s.batch) * s.heads * s.seqlen;
+  if (rows > INT_MAX / 2) return VSA_ERR_UNSUPPORTED;
+  *nb = s.seqlen / vsa::BLOCK;
+  return VSA_OK;
+}
+
+// The kernels are built for sm_103a only.
+vsa_status check_device() {
+  int dev = 0, major = 0, minor = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+    return cuda_fail(e);
+  if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+    return cuda_fail(e);
+  return (major == 10 && minor == 3) ? VSA_OK : VSA_ERR_UNSUPPORTED;
+}
+
+template <typename T>
+T* ws_at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* vsa_status_string(vsa_status status) {
+  switch (status) {
+    case VSA_OK:
+      return "VSA_OK";
+    case VSA_ERR_INVALID_ARG:
+      return "VSA_ERR_INVALID_ARG";
+    case VSA_ERR_UNSUPPORTED:
+      return "VSA_ERR_UNSUPPORTED";
+    case VSA_ERR_WORKSPACE:
+      return "VSA_ERR_WORKSPACE";
+    case VSA_ERR_CUDA:
+      return "VSA_ERR_CUDA";
+  }
+  return "VSA_ERR_UNKNOWN";
+}
+
+int vsa_last_cuda_error(void) { return g_last_cuda_error; }
+
+vsa_status vsa_invert_indices(const int32_t* q2k_idx, const int32_t* q2k_num, int32_t topk,
+                              vsa_shape shape, int32_t* k2q_idx, int32_t* k2q_num,
+                              uint32_t* dev_err, void* stream) {
+  int nb = 0;
+  vsa_status st = check_shape(shape, &nb);
+  if (st != VSA_OK) return st;
+  if (topk < 1 || !q2k_idx || !q2k_num || !k2q_idx || !k2q_num) return VSA_ERR_INVALID_ARG;
+  if (!aligned(q2k_idx, 4) || !aligned(q2k_num, 4) || !aligned(k2q_idx, 4) || !aligned(k2q_num, 4) ||
+      !aligned(dev_err, 4))
+    return VSA_ERR_INVALID_ARG;
+  if ((st = check_device()) != VSA_OK) return st;
+  const cudaError_t e =
+      vsa::launch_invert(q2k_idx, q2k_num, topk, shape.batch * shape.heads, nb, k2q_idx, k2q_num,
+                         dev_err, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? VSA_OK : cuda_fail(e);
+}
+
+size_t vsa_fwd_workspace_bytes(vsa_shape shape) {
+  int nb = 0;
+  if (check_shape(shape, &nb) != VSA_OK) return 0;
+  return vsa::fwd_layout(shape.batch, shape.heads, shape.seqlen).total;
+}
+
+size_t vsa_bwd_workspace_bytes(vsa_shape shape) {
+  int nb = 0;
+  if (check_shape(shape, &nb) != VSA_OK) return 0;
+  return vsa::bwd_layout(shape.batch, shape.heads, shape.seqlen).total;
+}
+
+vsa_status vsa_fwd(const void* q, const void* k, const void* v, const int32_t* q2k_idx,
+                   const int32_t* q2k_num, int32_t topk, const int32_t* vbs, float sm_scale,
+                   vsa_shape shape, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+  int nb = 0;
+  vsa_status st = check_shape(shape, &nb);
+  if (st != VSA_OK) return st;
+  if (!q || !k || !v || !q2k_idx || !q2k_num || !vbs || !o || !lse) return VSA_ERR_INVALID_ARG;
+  if (topk < 1 || !std::isfinite(sm_scale)) return VSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4) || !aligned(q2k_idx, 4) || !aligned(q2k_num, 4) || !aligned(vbs, 4))
+    return VSA_ERR_INVALID_ARG;
+  const vsa::FwdLayout L = vsa::fwd_layout(shape.batch, shape.heads, shape.seqlen);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return VSA_ERR_WORKSPACE;
+  if ((st = check_device()) != VSA_OK) return st;
+
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int BH = shape.batch * shape.heads, S = shape.seqlen;
+  uint32_t* err = ws_at<uint32_t>(workspace, L.err);
+  uint32_t* absmax = ws_at<uint32_t>(workspace, L.absmax);
+  uint32_t* bitmap = ws_at<uint32_t>(workspace, L.bitmap);
+  __half* q16 = ws_at<__half>(workspace, L.q16);
+  __half* k16 = ws_at<__half>(workspace, L.k16);
+  __half* v16 = ws_at<__half>(workspace, L.v16);
+  const auto* qb = static_cast<const __nv_bfloat16*>(q);
+  const auto* kb = static_cast<const __nv_bfloat16*>(k);
+  const auto* vb = static_cast<const __nv_bfloat16*>(v);
+
+  cudaError_t e = cudaMemsetAsync(workspace, 0, L.q16, s);  // header, maxima, bitmap
+  if (e != cudaSuccess) return cuda_fail(e);
+  if ((e = vsa::launch_absmax_delta(qb, kb, vb, nullptr, nullptr, BH, S, absmax, nullptr, nullptr,
+                                    s)) != cudaSuccess)
+    return cuda_fail(e);
+  const __nv_bfloat16* src[3] = {qb, kb, vb};
+  __half* dst[3] = {q16, k16, v16};
+  if ((e = vsa::launch_convert(src, dst, 3, BH, S, absmax, s)) != cudaSuccess) return cuda_fail(e);
+  if ((e = vsa::launch_fwd_bitmap(q2k_idx, q2k_num, topk, BH, nb, bitmap, err, s)) != cudaSuccess)
+    return cuda_fail(e);
+  vsa::FwdMainArgs a{};
+  a.q16 = q16;
+  a.k16 = k16;
+  a.v16 = v16;
+  a.bitmap = bitmap;
+  a.vbs = vbs;
+  a.absmax = absmax;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.err = err;
+  a.B = shape.batch;
+  a.H = shape.heads;
+  a.S = S;
+  a.nb = nb;
+  a.sm_scale = sm_scale;
+  if ((e = vsa::launch_fwd_main(a, s)) != cudaSuccess) return cuda_fail(e);
+  return VSA_OK;
+}
+
+vsa_status vsa_bwd(const void* dout, const void* q, const void* k, const void* v, const void* o,
+                   const float* lse, const int32_t* k2q_idx, const int32_t* k2q_num,
+                   int32_t max_q_blocks, const int32_t* vbs, float sm_scale, vsa_shape shape,
+                   void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+  int nb = 0;
+  vsa_status st = check_shape(shape, &nb);
+  if (st != VSA_OK) return st;
+  if (!dout || !q || !k || !v || !o || !lse || !k2q_idx || !k2q_num || !vbs || !dq || !dk || !dv)
+    return VSA_ERR_INVALID_ARG;
+  if (max_q_blocks < 1 || !std::isfinite(sm_scale)) return VSA_ERR_INVALID_ARG;
+  if (!aligned(dout, 16) || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) ||
+      !aligned(o, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+      !aligned(lse, 4) || !aligned(k2q_idx, 4) || !aligned(k2q_num, 4) || !aligned(vbs, 4))
+    return VSA_ERR_INVALID_ARG;
+  const vsa::BwdLayout L = vsa::bwd_layout(shape.batch, shape.heads, shape.seqlen);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return VSA_ERR_WORKSPACE;
+  if ((st = check_device()) != VSA_OK) return st;
+
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int BH = shape.batch * shape.heads, S = shape.seqlen;
+  uint32_t* err = ws_at<uint32_t>(workspace, L.err);
+  uint32_t* absmax = ws_at<uint32_t>(workspace, L.absmax);
+  float* delta = ws_at<float>(workspace, L.delta);
+  int32_t* order = ws_at<int32_t>(workspace, L.order);
+  float* dqacc = ws_at<float>(workspace, L.dqacc);
+  __half* q16 = ws_at<__half>(workspace, L.q16);
+  __half* k16 = ws_at<__half>(workspace, L.k16);
+  __half* v16 = ws_at<__half>(workspace, L.v16);
+  __half* do16 = ws_at<__half>(workspace, L.do16);
+  const auto* qb = static_cast<const __nv_bfloat16*>(q);
+  const auto* kb = static_cast<const __nv_bfloat16*>(k);
+  const auto* vb = static_cast<const __nv_bfloat16*>(v);
+  const auto* dob = static_cast<const __nv_bfloat16*>(dout);
+  const auto* ob = static_cast<const __nv_bfloat16*>(o);
+
+  cudaError_t e = cudaMemsetAsync(workspace, 0, L.delta, s);  // header and maxima
+  if (e != cudaSuccess) return cuda_fail(e);
+  if ((e = vsa::launch_absmax_delta(qb, kb, vb, dob, ob, BH, S, absmax, delta, dqacc, s)) !=
+      cudaSuccess)
+    return cuda_fail(e);
+  const __nv_bfloat16* src[4] = {qb, kb, vb, dob};
+  __half* dst[4] = {q16, k16, v16, do16};
+  if ((e = vsa::launch_convert(src, dst, 4, BH, S, absmax, s)) != cudaSuccess) return cuda_fail(e);
+  const int32_t* work_order = nullptr;
+  if (nb >= vsa::ORDER_MIN_KV_BLOCKS) {
+    if ((e = vsa::launch_order(k2q_num, BH, nb, max_q_blocks, order, s)) != cudaSuccess)
+      return cuda_fail(e);
+    work_order = order;
+  }
+  vsa::BwdMainArgs a{};
+  a.q16 = q16;
+  a.k16 = k16;
+  a.v16 = v16;
+  a.do16 = do16;
+  a.k2q_idx = k2q_idx;
+  a.k2q_num = k2q_num;
+  a.order = work_order;
+  a.vbs = vbs;
+  a.lse = lse;
+  a.delta = delta;
+  a.absmax = absmax;
+  a.dqacc = dqacc;
+  a.dk = static_cast<__nv_bfloat16*>(dk);
+  a.dv = static_cast<__nv_bfloat16*>(dv);
+  a.err = err;
+  a.B = shape.batch;
+  a.H = shape.heads;
+  a.S = S;
+  a.nb = nb;
+  a.max_q = max_q_blocks;
+  a.sm_scale = sm_scale;
+  if ((e = vsa::launch_bwd_main(a, s)) != cudaSuccess) return cuda_fail(e);
+  if ((e = vsa::launch_postprocess(dqacc, absmax, BH, S, sm_scale,
+                                   static_cast<__nv_bfloat16*>(dq), s)) != cudaSuccess)
+    return cuda_fail(e);
+  return VSA_OK;
+}
+
+vsa_status vsa_read_device_error(const void* workspace, uint32_t* bits, void* stream) {
+  if (!workspace || !bits || !aligned(workspace, 256)) return VSA_ERR_INVALID_ARG;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = cudaMemcpy(bits, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  return e == cudaSuccess ? VSA_OK : cuda_fail(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,600 @@
+// bwd_main.cu -- the main kernel of the block-sparse attention backward on sm_103a.
+//
+// Work unit: one (b, h, kv block j) item, as in FastVideo's sm_100a backward (commit message:
+// "one warp-specialized tcgen05 kernel per (batch, head, kv64 block) computing dK, dV and the dQ
+// partials").  The item's k2q list of q blocks is walked two q blocks at a time, so every UMMA
+// has M = 128 (the q pair, or the 128 head-dim rows) and the fp32 accumulator maps row m to TMEM
+// lane m.  Per q pair (p = the pair's 128 query rows, all operands fp16 with per-head power-of-
+// two scales, fp32 accumulation):
+//   S   [128 q  x  64 kv] = Q_p  K_j^T      A = Q_p  (K-major), B = K_j (K-major)
+//   dP  [128 q  x  64 kv] = dO_p V_j^T      A = dO_p (K-major), B = V_j (K-major)
+//   P   = exp2(S * c - lse), masked (kv row >= vbs[j], or missing second q block) -> fp16 smem
+//   dS  = P * (dP - Delta)                                                          -> fp16 smem
+//   dV^T [128 hd x 64 kv] += dO_p^T P         A = dO_p (MN-major), B = P  (MN-major)
+//   dK^T [128 hd x 64 kv] += Q_p^T  dS        A = Q_p  (MN-major), B = dS (MN-major)
+//   dQ^T [128 hd x 128 q] =  K_j^T  dS^T      A = K_j  (MN-major), B = dS (K-major)
+// The same shared-memory tiles serve as K-major and MN-major operands (128-byte swizzle, 8-row
+// groups 1024 B apart), so no transposed copies of Q or dO are needed.  dQ^T leaves TMEM with
+// head-dim on the lanes, so each warp's fp32 reduction into the dQ accumulator covers 128
+// contiguous bytes of one query row.
+//
+// Roles (320 threads):
+//   warps 0-3  softmax: thread r owns query row r of the pair; reads S and dP rows from TMEM,
+//              writes P and dS (fp16, swizzled) to shared memory.
+//   warps 4-7  dQ drain + epilogue: thread d owns head-dim row d; reduces dQ^T into the fp32
+//              accumulator, and at the end of an item writes dK, dV (bf16, zeros for padded
+//              rows; whole zero blocks for items no q block selects).
+//   warp 8     TMA producer (K_j, V_j once per item; Q and dO of each pair into a 2-stage ring);
+//              also allocates TMEM.
+//   warp 9     UMMA issuer (one thread).
+// TMEM (512 columns): S x2 [0,128), dP x2 [128,256), dV^T [256,320), dK^T [320,384),
+// dQ^T [384,512).
+#include <cudaTypedefs.h>
+
+#include "ptx.cuh"
+#include "vsa_internal.cuh"
+
+namespace vsa {
+
+namespace {
+
+constexpr int NUM_THREADS = 320;
+
+// Shared memory map (offsets from a 1024-byte aligned base).
+constexpr uint32_t SM_K = 0;                    // K_j: 2 chunks x [64 kv x 128 B]
+constexpr uint32_t SM_V = 16384;                // V_j
+constexpr uint32_t SM_Q = 32768;                // 2 stages x 2 chunks x [128 q x 128 B]
+constexpr uint32_t SM_DO = SM_Q + 2 * 32768;    // 2 stages, same layout
+constexpr uint32_t SM_P = SM_DO + 2 * 32768;    // 2 buffers x [128 q x 128 B]
+constexpr uint32_t SM_DS = SM_P + 2 * 16384;    // 2 buffers
+constexpr uint32_t SM_BAR = SM_DS + 2 * 16384;  // mbarriers
+
+enum Bar : uint32_t {
+  KV_FULL = 0,
+  KV_EMPTY,
+  QDO_FULL0,
+  QDO_FULL1,
+  QDO_EMPTY0,
+  QDO_EMPTY1,
+  SDP_FULL0,
+  SDP_FULL1,
+  P_READY0,
+  P_READY1,
+  PDS_FREE0,
+  PDS_FREE1,
+  DQ_FULL,
+  DQ_FREE,
+  ACC_FULL,
+  ACC_EMPTY,
+  DRAIN,
+  NUM_BARS
+};
+constexpr uint32_t SM_TMEM_SLOT = SM_BAR + NUM_BARS * 8;
+constexpr uint32_t SM_ABORT = SM_TMEM_SLOT + 4;
+constexpr uint32_t SM_USED = SM_ABORT + 4;
+constexpr uint32_t SMEM_BYTES = SM_USED + 1024;  // + alignment slack
+
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DVT = 256, TM_DKT = 320, TM_DQT = 384;
+
+constexpr uint32_t IDESC_SDP = idesc_f16_f32acc(128, 64, false, false);
+constexpr uint32_t IDESC_DVK = idesc_f16_f32acc(128, 64, true, true);
+constexpr uint32_t IDESC_DQ = idesc_f16_f32acc(128, 128, true, false);
+
+struct Params {
+  const int32_t* k2q_idx;
+  const int32_t* k2q_num;
+  const int32_t* order;
+  const int32_t* vbs;
+  const float* lse;
+  const float* delta;
+  const uint32_t* absmax;
+  float* dqacc;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  uint32_t* err;
+  int S, nb, max_q, total;
+  float sm_scale;
+};
+
+struct Item {
+  int bh, j, n;
+  const int32_t* list;
+};
+
+__device__ __forceinline__ Item decode_item(const Params& p, int w) {
+  const int item = p.order ? p.order[w] : w;
+  Item it;
+  it.bh = item / p.nb;
+  it.j = item - it.bh * p.nb;
+  const int n = p.k2q_num[item];
+  it.n = n < 0 ? 0 : (n > p.max_q ? p.max_q : n);
+  it.list = p.k2q_idx + static_cast<size_t>(item) * p.max_q;
+  return it;
+}
+
+__device__ __forceinline__ int q_block(const Item& it, int x, int nq) {
+  const int i = it.list[x];
+  return (i < 0 || i >= nq) ? 0 : i;
+}
+
+__device__ __forceinline__ int clamp_vbs(int v) { return v < 0 ? 0 : (v > BLOCK ? BLOCK : v); }
+
+// One elected lane waits; the result is broadcast so the warp stays converged.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          int lane) {
+  int ok = 1;
+  if (lane == 0) ok = mbar_wait_bounded(bar, parity, abort, WAIT_LIMIT_NS) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__device__ __forceinline__ void raise_abort(volatile int* abort, uint32_t* err) {
+  *abort = 1;
+  atomicOr(err, VSA_DEVERR_TIMEOUT);
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_do, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  volatile int* abort = reinterpret_cast<volatile int*>(gbase + SM_ABORT);
+  const uint32_t* tmem_slot = reinterpret_cast<const uint32_t*>(gbase + SM_TMEM_SLOT);
+  auto bar = [&](uint32_t b) { return base + SM_BAR + 8u * b; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = p.S, nq = p.nb;
+
+  if (threadIdx.x == 0) {
+    *abort = 0;
+    mbar_init(bar(KV_FULL), 1);
+    mbar_init(bar(KV_EMPTY), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(QDO_FULL0 + s), 1);
+      mbar_init(bar(QDO_EMPTY0 + s), 1);
+      mbar_init(bar(SDP_FULL0 + s), 1);
+      mbar_init(bar(P_READY0 + s), 4);
+      mbar_init(bar(PDS_FREE0 + s), 1);
+    }
+    mbar_init(bar(DQ_FULL), 1);
+    mbar_init(bar(DQ_FREE), 4);
+    mbar_init(bar(ACC_FULL), 1);
+    mbar_init(bar(ACC_EMPTY), 4);
+    mbar_init(bar(DRAIN), 1);
+    fence_barrier_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(base + SM_TMEM_SLOT, 512);
+    tmem_relinquish();
+  }
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t g = 0;      // global pair-step counter
+      uint32_t itc = 0;    // items with a non-empty list
+      uint32_t kv_loads = 0;
+      int64_t last_g[2] = {-1, -1};
+      bool ok = true;
+      for (int w = blockIdx.x; w < p.total && ok; w += gridDim.x) {
+        const Item it = decode_item(p, w);
+        const int raw_n = p.k2q_num[p.order ? p.order[w] : w];
+        uint32_t bad = 0;
+        if (raw_n != it.n) bad |= VSA_DEVERR_K2Q_COUNT;
+        const int vb = p.vbs[it.j];
+        if (vb != clamp_vbs(vb)) bad |= VSA_DEVERR_VBS;
+        for (int x = 0; x < it.n; ++x) {
+          const int i = it.list[x];
+          if (i < 0 || i >= nq) bad |= VSA_DEVERR_K2Q_ID;
+        }
+        if (bad) atomicOr(p.err, bad);
+        if (it.n == 0) continue;
+        if (!mbar_wait_bounded(bar(KV_EMPTY), (itc & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) {
+          ok = false;
+          break;
+        }
+        const int row_kv = it.bh * S + it.j * BLOCK;
+        mbar_arrive_expect_tx(bar(KV_FULL), 32768);
+        tma_load_2d(base + SM_K, &tm_k, bar(KV_FULL), 0, row_kv);
+        tma_load_2d(base + SM_K + 8192, &tm_k, bar(KV_FULL), 64, row_kv);
+        tma_load_2d(base + SM_V, &tm_v, bar(KV_FULL), 0, row_kv);
+        tma_load_2d(base + SM_V + 8192, &tm_v, bar(KV_FULL), 64, row_kv);
+        ++kv_loads;
+        const int np = (it.n + 1) >> 1;
+        for (int pp = 0; pp < np; ++pp, ++g) {
+          const uint32_t s = g & 1u;
+          if (!mbar_wait_bounded(bar(QDO_EMPTY0 + s), ((g >> 1) & 1u) ^ 1u, abort,
+                                 WAIT_LIMIT_NS)) {
+            ok = false;
+            break;
+          }
+          const int i0 = q_block(it, 2 * pp, nq);
+          const int i1 = (2 * pp + 1 < it.n) ? q_block(it, 2 * pp + 1, nq) : i0;
+          const int r0 = it.bh * S + i0 * BLOCK, r1 = it.bh * S + i1 * BLOCK;
+          const uint32_t qs = base + SM_Q + s * 32768u, ds = base + SM_DO + s * 32768u;
+          mbar_arrive_expect_tx(bar(QDO_FULL0 + s), 65536);
+          tma_load_2d(qs, &tm_q, bar(QDO_FULL0 + s), 0, r0);
+          tma_load_2d(qs + 8192, &tm_q, bar(QDO_FULL0 + s), 0, r1);
+          tma_load_2d(qs + 16384, &tm_q, bar(QDO_FULL0 + s), 64, r0);
+          tma_load_2d(qs + 24576, &tm_q, bar(QDO_FULL0 + s), 64, r1);
+          tma_load_2d(ds, &tm_do, bar(QDO_FULL0 + s), 0, r0);
+          tma_load_2d(ds + 8192, &tm_do, bar(QDO_FULL0 + s), 0, r1);
+          tma_load_2d(ds + 16384, &tm_do, bar(QDO_FULL0 + s), 64, r0);
+          tma_load_2d(ds + 24576, &tm_do, bar(QDO_FULL0 + s), 64, r1);
+          last_g[s] = g;
+        }
+        ++itc;
+      }
+      if (!ok) {
+        raise_abort(abort, p.err);
+        // Let the copies already issued land before the CTA's shared memory goes away.
+        volatile int never = 0;
+        if (kv_loads > 0)
+          mbar_wait_bounded(bar(KV_FULL), (kv_loads - 1) & 1u, &never, DRAIN_LIMIT_NS);
+        for (int s = 0; s < 2; ++s)
+          if (last_g[s] >= 0)
+            mbar_wait_bounded(bar(QDO_FULL0 + s), (static_cast<uint32_t>(last_g[s]) >> 1) & 1u,
+                              &never, DRAIN_LIMIT_NS);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------------ UMMA issuer
+    if (lane == 0) {
+      uint32_t g = 0, itc = 0;
+      bool ok = true, issued = false;
+      auto issue_sdp = [&](uint32_t gs) {
+        const uint32_t s = gs & 1u;
+        const uint32_t qa = base + SM_Q + s * 32768u, da = base + SM_DO + s * 32768u;
+        const uint32_t ts = tmem + TM_S + s * 64u, tdp = tmem + TM_DP + s * 64u;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t c = kk >> 2, off = (kk & 3) * 32;
+          umma_f16(ts, sdesc_sw128(qa + c * 16384u + off, 16, 1024),
+                   sdesc_sw128(base + SM_K + c * 8192u + off, 16, 1024), IDESC_SDP, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t c = kk >> 2, off = (kk & 3) * 32;
+          umma_f16(tdp, sdesc_sw128(da + c * 16384u + off, 16, 1024),
+                   sdesc_sw128(base + SM_V + c * 8192u + off, 16, 1024), IDESC_SDP, kk > 0);
+        }
+        umma_commit(bar(SDP_FULL0 + s));
+      };
+      for (int w = blockIdx.x; w < p.total && ok; w += gridDim.x) {
+        const Item it = decode_item(p, w);
+        if (it.n == 0) continue;
+        const int np = (it.n + 1) >> 1;
+        if (!mbar_wait_bounded(bar(KV_FULL), itc & 1u, abort, WAIT_LIMIT_NS)) {
+          ok = false;
+          break;
+        }
+        if (!mbar_wait_bounded(bar(QDO_FULL0 + (g & 1u)), (g >> 1) & 1u, abort, WAIT_LIMIT_NS)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        issue_sdp(g);
+        issued = true;
+        for (int pp = 0; pp < np; ++pp, ++g) {
+          const uint32_t s = g & 1u;
+          if (pp + 1 < np) {
+            const uint32_t gn = g + 1;
+            if (!mbar_wait_bounded(bar(QDO_FULL0 + (gn & 1u)), (gn >> 1) & 1u, abort,
+                                   WAIT_LIMIT_NS)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            issue_sdp(gn);
+          }
+          if (!mbar_wait_bounded(bar(P_READY0 + s), (g >> 1) & 1u, abort, WAIT_LIMIT_NS)) {
+            ok = false;
+            break;
+          }
+          if (pp == 0 &&
+              !mbar_wait_bounded(bar(ACC_EMPTY), (itc & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t qa = base + SM_Q + s * 32768u, da = base + SM_DO + s * 32768u;
+          const uint32_t pa = base + SM_P + s * 16384u, dsa = base + SM_DS + s * 16384u;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_f16(tmem + TM_DVT, sdesc_sw128(da + kk * 2048u, 16384, 1024),
+                     sdesc_sw128(pa + kk * 2048u, 16384, 1024), IDESC_DVK, (pp > 0 || kk > 0));
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_f16(tmem + TM_DKT, sdesc_sw128(qa + kk * 2048u, 16384, 1024),
+                     sdesc_sw128(dsa + kk * 2048u, 16384, 1024), IDESC_DVK, (pp > 0 || kk > 0));
+          if (!mbar_wait_bounded(bar(DQ_FREE), (g & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_f16(tmem + TM_DQT, sdesc_sw128(base + SM_K + kk * 2048u, 8192, 1024),
+                     sdesc_sw128(dsa + kk * 32u, 16, 1024), IDESC_DQ, kk > 0);
+          umma_commit(bar(DQ_FULL));
+          umma_commit(bar(QDO_EMPTY0 + s));
+          umma_commit(bar(PDS_FREE0 + s));
+        }
+        if (!ok) break;
+        umma_commit(bar(ACC_FULL));
+        umma_commit(bar(KV_EMPTY));
+        ++itc;
+      }
+      if (!ok) raise_abort(abort, p.err);
+      if (issued) {
+        // Every UMMA has completed before TMEM is released.
+        umma_commit(bar(DRAIN));
+        volatile int never = 0;
+        mbar_wait_bounded(bar(DRAIN), 0, &never, DRAIN_LIMIT_NS);
+      }
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ------------------------------------------------------------------ softmax / dS
+    const int r = warp * 32 + lane;  // query row of the pair == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    uint32_t g = 0;
+    const uint32_t sw = static_cast<uint32_t>(r & 7);
+    for (int w = blockIdx.x; w < p.total; w += gridDim.x) {
+      const Item it = decode_item(p, w);
+      if (it.n == 0) continue;
+      const int vb = clamp_vbs(p.vbs[it.j]);
+      const uint32_t* am = p.absmax + it.bh * 4;
+      const int eq = operand_exponent(am[0]), ek = operand_exponent(am[1]);
+      const int ev = operand_exponent(am[2]), eo = operand_exponent(am[3]);
+      const float c1 = p.sm_scale * LOG2E_F * exp2i(eq + ek);
+      const float dscale = exp2i(-(eo + ev));
+      const int np = (it.n + 1) >> 1;
+      bool ok = true;
+      for (int pp = 0; pp < np; ++pp, ++g) {
+        const uint32_t s = g & 1u;
+        const bool has2 = (2 * pp + 1 < it.n);
+        const bool valid = (r < 64) || has2;
+        const int qb = q_block(it, 2 * pp + ((r >= 64 && has2) ? 1 : 0), nq);
+        const size_t grow = static_cast<size_t>(it.bh) * S + static_cast<size_t>(qb) * BLOCK + (r & 63);
+        const float nlse = static_cast<float>(KP) - p.lse[grow];
+        const float dl = p.delta[grow] * dscale;  // Delta in the units of dP' = dO'.V'
+        if (!warp_wait(bar(SDP_FULL0 + s), (g >> 1) & 1u, abort, lane)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        if (!warp_wait(bar(PDS_FREE0 + s), ((g >> 1) & 1u) ^ 1u, abort, lane)) {
+          ok = false;
+          break;
+        }
+        const uint32_t prow = base + SM_P + s * 16384u + static_cast<uint32_t>(r) * 128u;
+        const uint32_t dsrow = base + SM_DS + s * 16384u + static_cast<uint32_t>(r) * 128u;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t sv[32], dpv[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + TM_S + s * 64u + h * 32u, sv);
+          tmem_ld_32x32b_x32(tmem + lane_off + TM_DP + s * 64u + h * 32u, dpv);
+          tmem_wait_ld();
+          uint32_t pk[16], dk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const int u = h * 32 + c;
+            const bool v0 = valid && (u < vb), v1 = valid && (u + 1 < vb);
+            const float p0 = v0 ? ex2(fmaf(__uint_as_float(sv[c]), c1, nlse)) : 0.f;
+            const float p1 = v1 ? ex2(fmaf(__uint_as_float(sv[c + 1]), c1, nlse)) : 0.f;
+            const float d0 = p0 * (__uint_as_float(dpv[c]) - dl);
+            const float d1 = p1 * (__uint_as_float(dpv[c + 1]) - dl);
+            pk[c >> 1] = pack_half2(p0, p1);
+            dk[c >> 1] = pack_half2(v0 ? d0 : 0.f, v1 ? d1 : 0.f);
+          }
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            const uint32_t phys = ((static_cast<uint32_t>(h * 4 + ch)) ^ sw) * 16u;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + phys),
+                         "r"(pk[4 * ch]), "r"(pk[4 * ch + 1]), "r"(pk[4 * ch + 2]),
+                         "r"(pk[4 * ch + 3])
+                         : "memory");
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dsrow + phys),
+                         "r"(dk[4 * ch]), "r"(dk[4 * ch + 1]), "r"(dk[4 * ch + 2]),
+                         "r"(dk[4 * ch + 3])
+                         : "memory");
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(P_READY0 + s));
+      }
+      if (!ok) {
+        if (lane == 0) raise_abort(abort, p.err);
+        break;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ dQ drain + epilogue
+    const int wq = warp - 4;
+    const int d = wq * 32 + lane;  // head-dim row == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    uint32_t g = 0, itc = 0;
+    for (int w = blockIdx.x; w < p.total; w += gridDim.x) {
+      const Item it = decode_item(p, w);
+      const size_t row_kv = static_cast<size_t>(it.bh) * S + static_cast<size_t>(it.j) * BLOCK;
+      __nv_bfloat16* dk_out = p.dk + row_kv * HEAD_DIM + d;
+      __nv_bfloat16* dv_out = p.dv + row_kv * HEAD_DIM + d;
+      if (it.n == 0) {
+        // No q block selects this kv block: exact-zero dK/dV rows.
+        const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
+        for (int t = 0; t < BLOCK; ++t) {
+          dk_out[t * HEAD_DIM] = z;
+          dv_out[t * HEAD_DIM] = z;
+        }
+        continue;
+      }
+      const uint32_t* am = p.absmax + it.bh * 4;
+      const int eq = operand_exponent(am[0]);
+      const int ev = operand_exponent(am[2]), eo = operand_exponent(am[3]);
+      const float sv_scale = exp2i(eo - KP);
+      const float sk_scale = p.sm_scale * exp2i(eq + eo + ev - KP);
+      const int vb = clamp_vbs(p.vbs[it.j]);
+      const int np = (it.n + 1) >> 1;
+      bool ok = true;
+      for (int pp = 0; pp < np; ++pp, ++g) {
+        const bool has2 = (2 * pp + 1 < it.n);
+        const int i0 = q_block(it, 2 * pp, nq);
+        const int i1 = has2 ? q_block(it, 2 * pp + 1, nq) : i0;
+        if (!warp_wait(bar(DQ_FULL), g & 1u, abort, lane)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          uint32_t v[64];
+          tmem_ld_32x32b_x32(tmem + lane_off + TM_DQT + c2 * 64u, v);
+          tmem_ld_32x32b_x32(tmem + lane_off + TM_DQT + c2 * 64u + 32u, v + 32);
+          tmem_wait_ld();
+          if (c2 == 1) {
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(DQ_FREE));
+          }
+          if (c2 == 0 || has2) {
+            const int qb = c2 ? i1 : i0;
+            float* dst = p.dqacc +
+                         (static_cast<size_t>(it.bh) * S + static_cast<size_t>(qb) * BLOCK) *
+                             HEAD_DIM +
+                         d;
+#pragma unroll
+            for (int n = 0; n < 64; ++n) atomicAdd(dst + n * HEAD_DIM, __uint_as_float(v[n]));
+          }
+        }
+      }
+      if (!ok) {
+        if (lane == 0) raise_abort(abort, p.err);
+        break;
+      }
+      if (!warp_wait(bar(ACC_FULL), itc & 1u, abort, lane)) {
+        if (lane == 0) raise_abort(abort, p.err);
+        break;
+      }
+      tc_fence_after_sync();
+      {
+        uint32_t v[64];
+        tmem_ld_32x32b_x32(tmem + lane_off + TM_DVT, v);
+        tmem_ld_32x32b_x32(tmem + lane_off + TM_DVT + 32u, v + 32);
+        tmem_wait_ld();
+#pragma unroll
+        for (int t = 0; t < BLOCK; ++t)
+          dv_out[t * HEAD_DIM] = __float2bfloat16_rn(t < vb ? __uint_as_float(v[t]) * sv_scale : 0.f);
+      }
+      {
+        uint32_t v[64];
+        tmem_ld_32x32b_x32(tmem + lane_off + TM_DKT, v);
+        tmem_ld_32x32b_x32(tmem + lane_off + TM_DKT + 32u, v + 32);
+        tmem_wait_ld();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(ACC_EMPTY));
+#pragma unroll
+        for (int t = 0; t < BLOCK; ++t)
+          dk_out[t * HEAD_DIM] = __float2bfloat16_rn(t < vb ? __uint_as_float(v[t]) * sk_scale : 0.f);
+      }
+      ++itc;
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 8) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+cudaError_t make_tmap_rows128_f16(CUtensorMap* map, const void* ptr, long rows) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(HEAD_DIM), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(HEAD_DIM) * sizeof(__half)};
+  const cuuint32_t box[2] = {64u, 64u};
+  const cuuint32_t estride[2] = {1u, 1u};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), gdim,
+                      gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bwd_main(const BwdMainArgs& a, cudaStream_t stream) {
+  const long rows = static_cast<long>(a.B) * a.H * a.S;
+  CUtensorMap tq, tk, tv, tdo;
+  cudaError_t e;
+  if ((e = make_tmap_rows128_f16(&tq, a.q16, rows)) != cudaSuccess) return e;
+  if ((e = make_tmap_rows128_f16(&tk, a.k16, rows)) != cudaSuccess) return e;
+  if ((e = make_tmap_rows128_f16(&tv, a.v16, rows)) != cudaSuccess) return e;
+  if ((e = make_tmap_rows128_f16(&tdo, a.do16, rows)) != cudaSuccess) return e;
+  static bool attr_set = false;
+  if (!attr_set) {
+    e = cudaFuncSetAttribute(bwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(SMEM_BYTES));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  Params p{};
+  p.k2q_idx = a.k2q_idx;
+  p.k2q_num = a.k2q_num;
+  p.order = a.order;
+  p.vbs = a.vbs;
+  p.lse = a.lse;
+  p.delta = a.delta;
+  p.absmax = a.absmax;
+  p.dqacc = a.dqacc;
+  p.dk = a.dk;
+  p.dv = a.dv;
+  p.err = a.err;
+  p.S = a.S;
+  p.nb = a.nb;
+  p.max_q = a.max_q;
+  p.total = a.B * a.H * a.nb;
+  p.sm_scale = a.sm_scale;
+  const int sms = device_sm_count();
+  const int grid = p.total < sms ? p.total : sms;
+  bwd_main_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tq, tk, tv, tdo, p);
+  return cudaGetLastError();
+}
+
+}  // namespace vsa

@@ -1,0 +1,260 @@
+// prepost.cu -- the memory-bound kernels around the tensor-core kernels:
+//   absmax_delta  per-head max|X| of the operands; Delta = rowsum(bf16(O) * dO) (FastVideo compare
+//                 main...vsa_bwd_fix, block_sparse_bwd_launch_sm100a.cuh, BlockSparseVsaBwdArgs:
+//                 "fp32 rowsum(bf16(o) * dout), written by the preprocess"); zeroing of the fp32
+//                 dQ accumulator ("preprocess zeroes, main reduce-adds, postprocess reads").
+//   convert       scaled fp16 copies of the bf16 operands for the tensor cores.
+//   order         work order: (b, h) segments, items sorted by descending k2q list length,
+//                 stable (the commit message's "a device kernel sorts by list length from 1024 kv
+//                 blocks per sequence on").
+//   postprocess   dQ = bf16(dqacc * sm_scale * 2^scale) ("postprocess (dQ ... + sm_scale)").
+//   fwd_bitmap    per-q-block selection bitmaps for the forward.
+// All are HBM-bound; each thread moves 16-byte vectors, grids cover the data once.
+#include "vsa_internal.cuh"
+
+namespace vsa {
+
+namespace {
+
+__device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t absmax_bits8(uint4 x) {
+  uint32_t m = 0;
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    m = max(m, (w[i] << 16) & 0x7FFFFFFFu);
+    m = max(m, w[i] & 0x7FFF0000u);
+  }
+  return m;
+}
+
+__device__ __forceinline__ uint32_t warp_max(uint32_t v) {
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, d));
+  return v;
+}
+
+// Grid (S / 64, BH), 256 threads: 16 lanes per 128-element row (8 bf16 = 16 B per lane), two
+// rows per warp per iteration, 64 rows per CTA.
+constexpr int PRE_THREADS = 256;
+
+__global__ void __launch_bounds__(PRE_THREADS) absmax_delta_kernel(
+    const uint4* __restrict__ q, const uint4* __restrict__ k, const uint4* __restrict__ v,
+    const uint4* __restrict__ dout, const uint4* __restrict__ o, int S, uint32_t* absmax,
+    float* __restrict__ delta, float4* __restrict__ dqacc) {
+  const int bh = blockIdx.y;
+  const int half = threadIdx.x >> 4;  // which of the 16 rows-in-flight
+  const int sub = threadIdx.x & 15;   // 16-byte chunk of the row
+  const bool bwd = (dout != nullptr);
+  uint32_t mq = 0, mk = 0, mv = 0, mdo = 0;
+  for (int rr = half; rr < BLOCK; rr += PRE_THREADS / 16) {
+    const size_t row = static_cast<size_t>(bh) * S + static_cast<size_t>(blockIdx.x) * BLOCK + rr;
+    const size_t at = row * 16 + sub;
+    mq = max(mq, absmax_bits8(q[at]));
+    mk = max(mk, absmax_bits8(k[at]));
+    mv = max(mv, absmax_bits8(v[at]));
+    if (bwd) {
+      const uint4 a = dout[at], b = o[at];
+      mdo = max(mdo, absmax_bits8(a));
+      float s = bf16lo(a.x) * bf16lo(b.x) + bf16hi(a.x) * bf16hi(b.x);
+      s += bf16lo(a.y) * bf16lo(b.y) + bf16hi(a.y) * bf16hi(b.y);
+      s += bf16lo(a.z) * bf16lo(b.z) + bf16hi(a.z) * bf16hi(b.z);
+      s += bf16lo(a.w) * bf16lo(b.w) + bf16hi(a.w) * bf16hi(b.w);
+#pragma unroll
+      for (int d = 8; d > 0; d >>= 1) s += __shfl_xor_sync(0xffffffffu, s, d);
+      if (sub == 0) delta[row] = s;
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      float4* dst = dqacc + row * 32 + sub * 2;
+      dst[0] = z;
+      dst[1] = z;
+    }
+  }
+  __shared__ uint32_t red[4][PRE_THREADS / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  mq = warp_max(mq);
+  mk = warp_max(mk);
+  mv = warp_max(mv);
+  mdo = warp_max(mdo);
+  if (lane == 0) {
+    red[0][warp] = mq;
+    red[1][warp] = mk;
+    red[2][warp] = mv;
+    red[3][warp] = mdo;
+  }
+  __syncthreads();
+  if (threadIdx.x < 4) {
+    uint32_t m = 0;
+    for (int w = 0; w < PRE_THREADS / 32; ++w) m = max(m, red[threadIdx.x][w]);
+    if (m) atomicMax(absmax + bh * 4 + threadIdx.x, m);
+  }
+}
+
+// One thread per 8 elements; up to four tensors in one launch (blockIdx.y).
+struct ConvertPack {
+  const uint4* src[4];
+  uint4* dst[4];
+};
+
+__global__ void __launch_bounds__(256) convert_kernel(ConvertPack pk, size_t chunks_per_head,
+                                                      size_t total_chunks,
+                                                      const uint32_t* __restrict__ absmax) {
+  const int t = blockIdx.y;
+  const uint4* __restrict__ src = t == 0 ? pk.src[0] : t == 1 ? pk.src[1] : t == 2 ? pk.src[2] : pk.src[3];
+  uint4* __restrict__ dst = t == 0 ? pk.dst[0] : t == 1 ? pk.dst[1] : t == 2 ? pk.dst[2] : pk.dst[3];
+  if (src == nullptr) return;
+  for (size_t c = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; c < total_chunks;
+       c += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int bh = static_cast<int>(c / chunks_per_head);
+    const float s = exp2i(-operand_exponent(absmax[bh * 4 + t]));
+    const uint4 x = src[c];
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 h = __floats2half2_rn(bf16lo(w[i]) * s, bf16hi(w[i]) * s);
+      out[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    dst[c] = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+}
+
+// Grid (BH, ceil(nb / 256)): item x of head bh goes to position
+// #{y : c_y > c_x} + #{y < x : c_y == c_x}, i.e. a stable sort by descending count.
+__global__ void __launch_bounds__(256) order_kernel(const int32_t* __restrict__ k2q_num, int nb,
+                                                    int max_q, int32_t* __restrict__ order) {
+  extern __shared__ int32_t cnt[];
+  const int bh = blockIdx.x;
+  const int32_t* num = k2q_num + static_cast<size_t>(bh) * nb;
+  for (int y = threadIdx.x; y < nb; y += blockDim.x) {
+    const int c = num[y];
+    cnt[y] = c < 0 ? 0 : (c > max_q ? max_q : c);
+  }
+  __syncthreads();
+  const int x = blockIdx.y * blockDim.x + threadIdx.x;
+  if (x >= nb) return;
+  const int cx = cnt[x];
+  int pos = 0;
+  for (int y = 0; y < nb; ++y) {
+    const int cy = cnt[y];
+    pos += (cy > cx) || (cy == cx && y < x);
+  }
+  order[static_cast<size_t>(bh) * nb + pos] = bh * nb + x;
+}
+
+__global__ void __launch_bounds__(256) postprocess_kernel(const float4* __restrict__ dqacc,
+                                                          const uint32_t* __restrict__ absmax,
+                                                          size_t chunks_per_head,
+                                                          size_t total_chunks, float sm_scale,
+                                                          uint4* __restrict__ dq) {
+  for (size_t c = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; c < total_chunks;
+       c += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int bh = static_cast<int>(c / chunks_per_head);
+    const uint32_t* am = absmax + bh * 4;
+    const int e = operand_exponent(am[1]) + operand_exponent(am[2]) + operand_exponent(am[3]) - KP;
+    const float s = sm_scale * exp2i(e);
+    const float4 a = dqacc[2 * c], b = dqacc[2 * c + 1];
+    const __nv_bfloat162 r0 = __floats2bfloat162_rn(a.x * s, a.y * s);
+    const __nv_bfloat162 r1 = __floats2bfloat162_rn(a.z * s, a.w * s);
+    const __nv_bfloat162 r2 = __floats2bfloat162_rn(b.x * s, b.y * s);
+    const __nv_bfloat162 r3 = __floats2bfloat162_rn(b.z * s, b.w * s);
+    dq[c] = make_uint4(*reinterpret_cast<const uint32_t*>(&r0),
+                       *reinterpret_cast<const uint32_t*>(&r1),
+                       *reinterpret_cast<const uint32_t*>(&r2),
+                       *reinterpret_cast<const uint32_t*>(&r3));
+  }
+}
+
+// One thread per q2k entry: set bit j of q block i's row of the selection bitmap.
+__global__ void __launch_bounds__(256) fwd_bitmap_kernel(const int32_t* __restrict__ q2k_idx,
+                                                         const int32_t* __restrict__ q2k_num,
+                                                         int topk, int nb, size_t entries,
+                                                         uint32_t* __restrict__ bitmap,
+                                                         uint32_t* err) {
+  const int words = (nb + 31) >> 5;
+  uint32_t bad = 0;
+  for (size_t e = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; e < entries;
+       e += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t r = e / topk;
+    const int s = static_cast<int>(e - r * topk);
+    const int c = q2k_num[r];
+    const int cnt = c < 0 ? 0 : (c > topk ? topk : c);
+    if (s == 0 && cnt != c) bad |= VSA_DEVERR_Q2K_COUNT;
+    if (s >= cnt) continue;
+    const int j = q2k_idx[e];
+    if (j < 0 || j >= nb) {
+      bad |= VSA_DEVERR_Q2K_ID;
+      continue;
+    }
+    atomicOr(bitmap + r * words + (j >> 5), 1u << (j & 31));
+  }
+  if (bad && err) atomicOr(err, bad);
+}
+
+int grid_for(size_t work, int threads, int per_sm) {
+  const size_t want = (work + threads - 1) / threads;
+  const size_t cap = static_cast<size_t>(device_sm_count()) * per_sm;
+  return static_cast<int>(want < cap ? (want < 1 ? 1 : want) : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_absmax_delta(const __nv_bfloat16* q, const __nv_bfloat16* k,
+                                const __nv_bfloat16* v, const __nv_bfloat16* dout,
+                                const __nv_bfloat16* o, int BH, int S, uint32_t* absmax,
+                                float* delta, float* dqacc, cudaStream_t stream) {
+  dim3 grid(static_cast<unsigned>(S / BLOCK), static_cast<unsigned>(BH));
+  absmax_delta_kernel<<<grid, PRE_THREADS, 0, stream>>>(
+      reinterpret_cast<const uint4*>(q), reinterpret_cast<const uint4*>(k),
+      reinterpret_cast<const uint4*>(v), reinterpret_cast<const uint4*>(dout),
+      reinterpret_cast<const uint4*>(o), S, absmax, delta, reinterpret_cast<float4*>(dqacc));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_convert(const __nv_bfloat16* const* src, __half* const* dst, int count, int BH,
+                           int S, const uint32_t* absmax, cudaStream_t stream) {
+  ConvertPack pk{};
+  for (int t = 0; t < 4; ++t) {
+    pk.src[t] = (t < count && src[t]) ? reinterpret_cast<const uint4*>(src[t]) : nullptr;
+    pk.dst[t] = (t < count && src[t]) ? reinterpret_cast<uint4*>(dst[t]) : nullptr;
+  }
+  const size_t per_head = static_cast<size_t>(S) * HEAD_DIM / 8;
+  const size_t total = per_head * BH;
+  dim3 grid(static_cast<unsigned>(grid_for(total, 256, 8)), static_cast<unsigned>(count));
+  convert_kernel<<<grid, 256, 0, stream>>>(pk, per_head, total, absmax);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_order(const int32_t* k2q_num, int BH, int nb, int max_q, int32_t* order,
+                         cudaStream_t stream) {
+  const size_t smem = static_cast<size_t>(nb) * sizeof(int32_t);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>((nb + 255) / 256));
+  order_kernel<<<grid, 256, smem, stream>>>(k2q_num, nb, max_q, order);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_postprocess(const float* dqacc, const uint32_t* absmax, int BH, int S,
+                               float sm_scale, __nv_bfloat16* dq, cudaStream_t stream) {
+  const size_t per_head = static_cast<size_t>(S) * HEAD_DIM / 8;
+  const size_t total = per_head * BH;
+  postprocess_kernel<<<grid_for(total, 256, 8), 256, 0, stream>>>(
+      reinterpret_cast<const float4*>(dqacc), absmax, per_head, total, sm_scale,
+      reinterpret_cast<uint4*>(dq));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_bitmap(const int32_t* q2k_idx, const int32_t* q2k_num, int topk, int BH,
+                              int nb, uint32_t* bitmap, uint32_t* err, cudaStream_t stream) {
+  const size_t entries = static_cast<size_t>(BH) * nb * topk;
+  fwd_bitmap_kernel<<<grid_for(entries, 256, 4), 256, 0, stream>>>(q2k_idx, q2k_num, topk, nb,
+                                                                    entries, bitmap, err);
+  return cudaGetLastError();
+}
+
+}  // namespace vsa

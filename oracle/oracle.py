@@ -39,7 +39,10 @@ def build_variant(source_text, tag):
     with open(src, "w") as f:
         f.write(source_text)
     subprocess.check_call(["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-o", lib, src, "-lm"])
-    return _declare(ctypes.CDLL(lib))
+    handle = _declare(ctypes.CDLL(lib))
+    os.remove(lib)  # the loaded image stays mapped
+    os.remove(src)
+    return handle
 
 
 _P = ctypes.c_void_p

@@ -1,0 +1,85 @@
+"""The C ABI without a GPU: libvsa.so builds, loads, exports every function include/vsa.h
+declares, and rejects bad arguments on the host before touching the device."""
+import ctypes
+import math
+import os
+import re
+import shutil
+
+import pytest
+
+from block_sparse_video_tok_gb300 import build as vsa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "vsa.h")
+
+pytestmark = pytest.mark.skipif(shutil.which("nvcc") is None and not os.path.exists(
+    "/usr/local/cuda/bin/nvcc"), reason="nvcc is needed to build libvsa.so")
+
+
+@pytest.fixture(scope="module")
+def vsa():
+    vsa_build.build()
+    from block_sparse_video_tok_gb300 import vsa as binding
+    return binding
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(vsa_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(vsa):
+    names = declared_functions()
+    assert len(names) == 8, names
+    lib = vsa.lib()
+    for name in names:
+        assert hasattr(lib, name), name
+        assert name in vsa.SIGNATURES, name
+
+
+def test_status_strings(vsa):
+    assert vsa.status_string(0) == "VSA_OK"
+    assert vsa.status_string(3) == "VSA_ERR_WORKSPACE"
+    assert vsa.status_string(99) == "VSA_ERR_UNKNOWN"
+
+
+def test_workspace_sizes(vsa):
+    B, H, S = 2, 3, 640
+    rows = B * H * S
+    bwd = vsa.vsa_bwd_workspace_bytes(B, H, S)
+    fwd = vsa.vsa_fwd_workspace_bytes(B, H, S)
+    # dQ accumulator (fp32) + four fp16 operand copies dominate the backward workspace.
+    assert bwd >= rows * 128 * 4 + 4 * rows * 128 * 2 + rows * 4
+    assert fwd >= 3 * rows * 128 * 2
+    assert vsa.vsa_bwd_workspace_bytes(B, H, 100) == 0      # S not a multiple of 64
+    assert vsa.vsa_bwd_workspace_bytes(B, H, S, 64) == 0    # head_dim 64
+    assert vsa.vsa_fwd_workspace_bytes(0, H, S) == 0
+
+
+def _bwd_args(vsa, shape, ptr=0x100000, ws_bytes=1 << 40, scale=0.088):
+    p = ctypes.c_void_p(ptr)
+    return [p, p, p, p, p, p, p, p, 8, p, scale, shape, p, p, p, p, ws_bytes, None]
+
+
+def test_host_side_rejections(vsa):
+    lib = vsa.lib()
+    good = vsa.make_shape(1, 2, 512)
+    # Null pointers.
+    null = [None] * 8 + [8, None, 0.1, good] + [None] * 4 + [1 << 40, None]
+    assert lib.vsa_bwd(*null) == 1
+    # Unsupported head_dim / sequence length.
+    assert lib.vsa_bwd(*_bwd_args(vsa, vsa.make_shape(1, 2, 512, 64))) == 2
+    assert lib.vsa_bwd(*_bwd_args(vsa, vsa.make_shape(1, 2, 500))) == 2
+    # Non-finite softmax scale, bad row stride, misaligned pointer.
+    assert lib.vsa_bwd(*_bwd_args(vsa, good, scale=math.inf)) == 1
+    bad = _bwd_args(vsa, good)
+    bad[8] = 0
+    assert lib.vsa_bwd(*bad) == 1
+    assert lib.vsa_bwd(*_bwd_args(vsa, good, ptr=0x100008)) == 1
+    # Workspace too small.
+    assert lib.vsa_bwd(*_bwd_args(vsa, good, ws_bytes=1024)) == 3
+    p = ctypes.c_void_p(0x100000)
+    assert lib.vsa_invert_indices(p, p, 0, good, p, p, None, None) == 1
+    assert lib.vsa_fwd(p, p, p, p, p, 4, p, 0.1, good, p, p, p, 16, None) == 3
