@@ -59,6 +59,10 @@ vsa_status check_device() {
   return (major == 10 && minor == 3) ? VSA_OK : VSA_ERR_UNSUPPORTED;
 }
 
+cudaError_t record(void* event, cudaStream_t s) {
+  return event ? cudaEventRecord(static_cast<cudaEvent_t>(event), s) : cudaSuccess;
+}
+
 template <typename T>
 T* ws_at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
@@ -177,6 +181,16 @@ vsa_status vsa_bwd(const void* dout, const void* q, const void* k, const void* v
                    int32_t max_q_blocks, const int32_t* vbs, float sm_scale, vsa_shape shape,
                    void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                    void* stream) {
+  return vsa_bwd_timed(dout, q, k, v, o, lse, k2q_idx, k2q_num, max_q_blocks, vbs, sm_scale, shape,
+                       dq, dk, dv, workspace, workspace_bytes, nullptr, stream);
+}
+
+vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const void* v,
+                         const void* o, const float* lse, const int32_t* k2q_idx,
+                         const int32_t* k2q_num, int32_t max_q_blocks, const int32_t* vbs,
+                         float sm_scale, vsa_shape shape, void* dq, void* dk, void* dv,
+                         void* workspace, size_t workspace_bytes, const vsa_bwd_events* events,
+                         void* stream) {
   int nb = 0;
   vsa_status st = check_shape(shape, &nb);
   if (st != VSA_OK) return st;
@@ -208,8 +222,10 @@ vsa_status vsa_bwd(const void* dout, const void* q, const void* k, const void* v
   const auto* dob = static_cast<const __nv_bfloat16*>(dout);
   const auto* ob = static_cast<const __nv_bfloat16*>(o);
 
-  cudaError_t e = cudaMemsetAsync(workspace, 0, L.delta, s);  // header and maxima
+  cudaError_t e = record(events ? events->start : nullptr, s);
   if (e != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaMemsetAsync(workspace, 0, L.delta, s)) != cudaSuccess)  // header and maxima
+    return cuda_fail(e);
   if ((e = vsa::launch_absmax_delta(qb, kb, vb, dob, ob, BH, S, absmax, delta, dqacc, s)) !=
       cudaSuccess)
     return cuda_fail(e);
@@ -244,10 +260,13 @@ vsa_status vsa_bwd(const void* dout, const void* q, const void* k, const void* v
   a.nb = nb;
   a.max_q = max_q_blocks;
   a.sm_scale = sm_scale;
+  if ((e = record(events ? events->before_main : nullptr, s)) != cudaSuccess) return cuda_fail(e);
   if ((e = vsa::launch_bwd_main(a, s)) != cudaSuccess) return cuda_fail(e);
+  if ((e = record(events ? events->after_main : nullptr, s)) != cudaSuccess) return cuda_fail(e);
   if ((e = vsa::launch_postprocess(dqacc, absmax, BH, S, sm_scale,
                                    static_cast<__nv_bfloat16*>(dq), s)) != cudaSuccess)
     return cuda_fail(e);
+  if ((e = record(events ? events->end : nullptr, s)) != cudaSuccess) return cuda_fail(e);
   return VSA_OK;
 }
 

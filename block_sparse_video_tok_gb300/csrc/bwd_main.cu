@@ -21,14 +21,21 @@
 // Roles (320 threads):
 //   warps 0-3  softmax: thread r owns query row r of the pair; reads S and dP rows from TMEM,
 //              writes P and dS (fp16, swizzled) to shared memory.
-//   warps 4-7  dQ drain + epilogue: thread d owns head-dim row d; reduces dQ^T into the fp32
-//              accumulator, and at the end of an item writes dK, dV (bf16, zeros for padded
-//              rows; whole zero blocks for items no q block selects).
+//   warps 4-7  dQ drain + epilogue: thread d owns head-dim row d; moves dQ^T through a 4 KB
+//              per-warp staging box ([32 query rows x 32 head dims] fp32) and adds it into the fp32
+//              accumulator with TMA bulk tensor reductions; at the end of an item writes dK, dV
+//              (bf16, zeros for padded rows; whole zero blocks for items no q block selects).
 //   warp 8     TMA producer (K_j, V_j once per item; Q and dO of each pair into a 2-stage ring);
 //              also allocates TMEM.
-//   warp 9     UMMA issuer (one thread).
-// TMEM (512 columns): S x2 [0,128), dP x2 [128,256), dV^T [256,320), dK^T [320,384),
-// dQ^T [384,512).
+//   warp 9     UMMA issuer (one thread).  Per step g: S/dP(g), then dQ^T(g-1), then (once the
+//              softmax has written P/dS(g)) dV^T/dK^T(g), after which the Q/dO stage of step g is
+//              released -- so a stage's reload has almost a whole step to land, the tensor pipe
+//              works on dQ^T(g-1) while the softmax of step g runs, and the dQ^T drain lags one
+//              step behind in a second TMEM buffer.
+// TMEM (512 columns): S [0,64), dP [64,128), dV^T [128,192), dK^T [192,256),
+// dQ^T x2 [256,512).  Shared memory: K_j, V_j; a 2-stage Q/dO ring; P (one buffer: when the
+// softmax sees S/dP(g) complete, dV^T(g-1), the only reader of P(g-1), has completed too); dS
+// (two buffers: dQ^T(g-1) still reads dS(g-1) while the softmax of step g runs); dQ staging.
 #include <cudaTypedefs.h>
 
 #include "ptx.cuh"
@@ -45,9 +52,10 @@ constexpr uint32_t SM_K = 0;                    // K_j: 2 chunks x [64 kv x 128 
 constexpr uint32_t SM_V = 16384;                // V_j
 constexpr uint32_t SM_Q = 32768;                // 2 stages x 2 chunks x [128 q x 128 B]
 constexpr uint32_t SM_DO = SM_Q + 2 * 32768;    // 2 stages, same layout
-constexpr uint32_t SM_P = SM_DO + 2 * 32768;    // 2 buffers x [128 q x 128 B]
-constexpr uint32_t SM_DS = SM_P + 2 * 16384;    // 2 buffers
-constexpr uint32_t SM_BAR = SM_DS + 2 * 16384;  // mbarriers
+constexpr uint32_t SM_P = SM_DO + 2 * 32768;    // [128 q x 128 B]
+constexpr uint32_t SM_DS = SM_P + 16384;        // 2 buffers x [128 q x 128 B]
+constexpr uint32_t SM_STG = SM_DS + 2 * 16384;  // dQ staging: 4 warps x [32 q x 32 fp32]
+constexpr uint32_t SM_BAR = SM_STG + 4 * 4096;  // mbarriers
 
 enum Bar : uint32_t {
   KV_FULL = 0,
@@ -56,14 +64,14 @@ enum Bar : uint32_t {
   QDO_FULL1,
   QDO_EMPTY0,
   QDO_EMPTY1,
-  SDP_FULL0,
-  SDP_FULL1,
-  P_READY0,
-  P_READY1,
+  SDP_FULL,
+  P_READY,
   PDS_FREE0,
   PDS_FREE1,
-  DQ_FULL,
-  DQ_FREE,
+  DQ_FULL0,
+  DQ_FULL1,
+  DQ_FREE0,
+  DQ_FREE1,
   ACC_FULL,
   ACC_EMPTY,
   DRAIN,
@@ -76,7 +84,7 @@ constexpr uint32_t SMEM_BYTES = SM_USED + 1024;  // + alignment slack
 
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DVT = 256, TM_DKT = 320, TM_DQT = 384;
+constexpr uint32_t TM_S = 0, TM_DP = 64, TM_DVT = 128, TM_DKT = 192, TM_DQT = 256;  // dQ^T x2
 
 constexpr uint32_t IDESC_SDP = idesc_f16_f32acc(128, 64, false, false);
 constexpr uint32_t IDESC_DVK = idesc_f16_f32acc(128, 64, true, true);
@@ -148,7 +156,8 @@ __device__ __forceinline__ float ex2(float x) {
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
-                    const __grid_constant__ CUtensorMap tm_do, const Params p) {
+                    const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_dq, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -167,12 +176,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(QDO_FULL0 + s), 1);
       mbar_init(bar(QDO_EMPTY0 + s), 1);
-      mbar_init(bar(SDP_FULL0 + s), 1);
-      mbar_init(bar(P_READY0 + s), 4);
       mbar_init(bar(PDS_FREE0 + s), 1);
+      mbar_init(bar(DQ_FULL0 + s), 1);
+      mbar_init(bar(DQ_FREE0 + s), 4);
     }
-    mbar_init(bar(DQ_FULL), 1);
-    mbar_init(bar(DQ_FREE), 4);
+    mbar_init(bar(SDP_FULL), 1);
+    mbar_init(bar(P_READY), 4);
     mbar_init(bar(ACC_FULL), 1);
     mbar_init(bar(ACC_EMPTY), 4);
     mbar_init(bar(DRAIN), 1);
@@ -187,6 +196,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_dq);
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -268,23 +278,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       uint32_t g = 0, itc = 0;
       bool ok = true, issued = false;
+      // S = Q_p K_j^T and dP = dO_p V_j^T of step gs (stage gs & 1).
       auto issue_sdp = [&](uint32_t gs) {
         const uint32_t s = gs & 1u;
         const uint32_t qa = base + SM_Q + s * 32768u, da = base + SM_DO + s * 32768u;
-        const uint32_t ts = tmem + TM_S + s * 64u, tdp = tmem + TM_DP + s * 64u;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t c = kk >> 2, off = (kk & 3) * 32;
-          umma_f16(ts, sdesc_sw128(qa + c * 16384u + off, 16, 1024),
+          umma_f16(tmem + TM_S, sdesc_sw128(qa + c * 16384u + off, 16, 1024),
                    sdesc_sw128(base + SM_K + c * 8192u + off, 16, 1024), IDESC_SDP, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t c = kk >> 2, off = (kk & 3) * 32;
-          umma_f16(tdp, sdesc_sw128(da + c * 16384u + off, 16, 1024),
+          umma_f16(tmem + TM_DP, sdesc_sw128(da + c * 16384u + off, 16, 1024),
                    sdesc_sw128(base + SM_V + c * 8192u + off, 16, 1024), IDESC_SDP, kk > 0);
         }
-        umma_commit(bar(SDP_FULL0 + s));
+        umma_commit(bar(SDP_FULL));
+      };
+      // dQ^T = K_j^T dS^T of step gs into TMEM buffer gs & 1; then its P/dS buffer is free.
+      auto issue_dq = [&](uint32_t gs) -> bool {
+        const uint32_t b = gs & 1u;
+        if (!mbar_wait_bounded(bar(DQ_FREE0 + b), ((gs >> 1) & 1u) ^ 1u, abort, WAIT_LIMIT_NS))
+          return false;
+        tc_fence_after_sync();
+        const uint32_t dsa = base + SM_DS + b * 16384u;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_f16(tmem + TM_DQT + b * 128u, sdesc_sw128(base + SM_K + kk * 2048u, 8192, 1024),
+                   sdesc_sw128(dsa + kk * 32u, 16, 1024), IDESC_DQ, kk > 0);
+        umma_commit(bar(DQ_FULL0 + b));
+        umma_commit(bar(PDS_FREE0 + b));
+        return true;
       };
       for (int w = blockIdx.x; w < p.total && ok; w += gridDim.x) {
         const Item it = decode_item(p, w);
@@ -294,26 +319,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ok = false;
           break;
         }
-        if (!mbar_wait_bounded(bar(QDO_FULL0 + (g & 1u)), (g >> 1) & 1u, abort, WAIT_LIMIT_NS)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        issue_sdp(g);
-        issued = true;
         for (int pp = 0; pp < np; ++pp, ++g) {
           const uint32_t s = g & 1u;
-          if (pp + 1 < np) {
-            const uint32_t gn = g + 1;
-            if (!mbar_wait_bounded(bar(QDO_FULL0 + (gn & 1u)), (gn >> 1) & 1u, abort,
-                                   WAIT_LIMIT_NS)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after_sync();
-            issue_sdp(gn);
+          if (!mbar_wait_bounded(bar(QDO_FULL0 + s), (g >> 1) & 1u, abort, WAIT_LIMIT_NS)) {
+            ok = false;
+            break;
           }
-          if (!mbar_wait_bounded(bar(P_READY0 + s), (g >> 1) & 1u, abort, WAIT_LIMIT_NS)) {
+          tc_fence_after_sync();
+          // The softmax finished reading S/dP(g-1) before it arrived on P_READY(g-1).
+          issue_sdp(g);
+          issued = true;
+          if (pp > 0 && !issue_dq(g - 1)) {
+            ok = false;
+            break;
+          }
+          if (!mbar_wait_bounded(bar(P_READY), g & 1u, abort, WAIT_LIMIT_NS)) {
             ok = false;
             break;
           }
@@ -324,7 +344,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           tc_fence_after_sync();
           const uint32_t qa = base + SM_Q + s * 32768u, da = base + SM_DO + s * 32768u;
-          const uint32_t pa = base + SM_P + s * 16384u, dsa = base + SM_DS + s * 16384u;
+          const uint32_t pa = base + SM_P, dsa = base + SM_DS + s * 16384u;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             umma_f16(tmem + TM_DVT, sdesc_sw128(da + kk * 2048u, 16384, 1024),
@@ -333,20 +353,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int kk = 0; kk < 8; ++kk)
             umma_f16(tmem + TM_DKT, sdesc_sw128(qa + kk * 2048u, 16384, 1024),
                      sdesc_sw128(dsa + kk * 2048u, 16384, 1024), IDESC_DVK, (pp > 0 || kk > 0));
-          if (!mbar_wait_bounded(bar(DQ_FREE), (g & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_f16(tmem + TM_DQT, sdesc_sw128(base + SM_K + kk * 2048u, 8192, 1024),
-                     sdesc_sw128(dsa + kk * 32u, 16, 1024), IDESC_DQ, kk > 0);
-          umma_commit(bar(DQ_FULL));
-          umma_commit(bar(QDO_EMPTY0 + s));
-          umma_commit(bar(PDS_FREE0 + s));
+          umma_commit(bar(QDO_EMPTY0 + s));  // Q_p and dO_p of step g are no longer read
         }
         if (!ok) break;
+        if (!issue_dq(g - 1)) {
+          ok = false;
+          break;
+        }
         umma_commit(bar(ACC_FULL));
         umma_commit(bar(KV_EMPTY));
         ++itc;
@@ -385,34 +398,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const size_t grow = static_cast<size_t>(it.bh) * S + static_cast<size_t>(qb) * BLOCK + (r & 63);
         const float nlse = static_cast<float>(KP) - p.lse[grow];
         const float dl = p.delta[grow] * dscale;  // Delta in the units of dP' = dO'.V'
-        if (!warp_wait(bar(SDP_FULL0 + s), (g >> 1) & 1u, abort, lane)) {
+        const bool full = valid && (vb == BLOCK);
+        if (!warp_wait(bar(SDP_FULL), g & 1u, abort, lane)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        if (!warp_wait(bar(PDS_FREE0 + s), ((g >> 1) & 1u) ^ 1u, abort, lane)) {
-          ok = false;
-          break;
-        }
-        const uint32_t prow = base + SM_P + s * 16384u + static_cast<uint32_t>(r) * 128u;
+        const uint32_t prow = base + SM_P + static_cast<uint32_t>(r) * 128u;
         const uint32_t dsrow = base + SM_DS + s * 16384u + static_cast<uint32_t>(r) * 128u;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t sv[32], dpv[32];
-          tmem_ld_32x32b_x32(tmem + lane_off + TM_S + s * 64u + h * 32u, sv);
-          tmem_ld_32x32b_x32(tmem + lane_off + TM_DP + s * 64u + h * 32u, dpv);
+          tmem_ld_32x32b_x32(tmem + lane_off + TM_S + h * 32u, sv);
+          tmem_ld_32x32b_x32(tmem + lane_off + TM_DP + h * 32u, dpv);
           tmem_wait_ld();
-          uint32_t pk[16], dk[16];
+          uint32_t pk[16], dk[16];  // P and dS of 32 columns, fp16 pairs
+          if (full) {  // every column visible: no masking
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const int u = h * 32 + c;
-            const bool v0 = valid && (u < vb), v1 = valid && (u + 1 < vb);
-            const float p0 = v0 ? ex2(fmaf(__uint_as_float(sv[c]), c1, nlse)) : 0.f;
-            const float p1 = v1 ? ex2(fmaf(__uint_as_float(sv[c + 1]), c1, nlse)) : 0.f;
-            const float d0 = p0 * (__uint_as_float(dpv[c]) - dl);
-            const float d1 = p1 * (__uint_as_float(dpv[c + 1]) - dl);
-            pk[c >> 1] = pack_half2(p0, p1);
-            dk[c >> 1] = pack_half2(v0 ? d0 : 0.f, v1 ? d1 : 0.f);
+            for (int c = 0; c < 32; c += 2) {
+              const float p0 = ex2(fmaf(__uint_as_float(sv[c]), c1, nlse));
+              const float p1 = ex2(fmaf(__uint_as_float(sv[c + 1]), c1, nlse));
+              pk[c >> 1] = pack_half2(p0, p1);
+              dk[c >> 1] = pack_half2(p0 * (__uint_as_float(dpv[c]) - dl),
+                                      p1 * (__uint_as_float(dpv[c + 1]) - dl));
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              const int u = h * 32 + c;
+              const bool v0 = valid && (u < vb), v1 = valid && (u + 1 < vb);
+              const float p0 = v0 ? ex2(fmaf(__uint_as_float(sv[c]), c1, nlse)) : 0.f;
+              const float p1 = v1 ? ex2(fmaf(__uint_as_float(sv[c + 1]), c1, nlse)) : 0.f;
+              const float d0 = p0 * (__uint_as_float(dpv[c]) - dl);
+              const float d1 = p1 * (__uint_as_float(dpv[c + 1]) - dl);
+              pk[c >> 1] = pack_half2(p0, p1);
+              dk[c >> 1] = pack_half2(v0 ? d0 : 0.f, v1 ? d1 : 0.f);
+            }
+          }
+          // The buffer's previous contents (step g-2) must have been consumed by dQ^T(g-2).
+          if (h == 0 && !warp_wait(bar(PDS_FREE0 + s), ((g >> 1) & 1u) ^ 1u, abort, lane)) {
+            ok = false;
+            break;
           }
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
@@ -427,10 +453,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                          : "memory");
           }
         }
+        if (!ok) break;
         fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(P_READY0 + s));
+        if (lane == 0) mbar_arrive(bar(P_READY));
       }
       if (!ok) {
         if (lane == 0) raise_abort(abort, p.err);
@@ -440,7 +467,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else {
     // ------------------------------------------------------------------ dQ drain + epilogue
     const int wq = warp - 4;
-    const int d = wq * 32 + lane;  // head-dim row == TMEM lane
+    const int d = wq * 32 + lane;  // head-dim row == TMEM lane (dK/dV epilogue column)
+    const uint32_t stg = base + SM_STG + static_cast<uint32_t>(wq) * 4096u;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     uint32_t g = 0, itc = 0;
     for (int w = blockIdx.x; w < p.total; w += gridDim.x) {
@@ -469,30 +497,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const bool has2 = (2 * pp + 1 < it.n);
         const int i0 = q_block(it, 2 * pp, nq);
         const int i1 = has2 ? q_block(it, 2 * pp + 1, nq) : i0;
-        if (!warp_wait(bar(DQ_FULL), g & 1u, abort, lane)) {
+        const uint32_t buf = g & 1u;
+        if (!warp_wait(bar(DQ_FULL0 + buf), (g >> 1) & 1u, abort, lane)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-#pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          uint32_t v[64];
-          tmem_ld_32x32b_x32(tmem + lane_off + TM_DQT + c2 * 64u, v);
-          tmem_ld_32x32b_x32(tmem + lane_off + TM_DQT + c2 * 64u + 32u, v + 32);
+        // Four 32-column chunks of dQ^T: chunks 0, 1 are rows 0-31, 32-63 of q block i0,
+        // chunks 2, 3 those of i1.  Each goes TMEM -> registers -> this warp's staging box
+        // (row q: 32 fp32 of head dims 32*wq .. 32*wq+31, so the 32 lanes' stores of one row
+        // are 128 contiguous bytes) -> one TMA reduce-add into the accumulator.
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + TM_DQT + buf * 128u + c * 32u, v);
           tmem_wait_ld();
-          if (c2 == 1) {
+          if (c == 3) {  // the TMEM buffer is free once all four chunks are in registers
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(DQ_FREE));
+            if (lane == 0) mbar_arrive(bar(DQ_FREE0 + buf));
           }
-          if (c2 == 0 || has2) {
-            const int qb = c2 ? i1 : i0;
-            float* dst = p.dqacc +
-                         (static_cast<size_t>(it.bh) * S + static_cast<size_t>(qb) * BLOCK) *
-                             HEAD_DIM +
-                         d;
+          if (c >= 2 && !has2) continue;
+          if (lane == 0) bulk_wait_read_all();  // the previous box has left the staging area
+          __syncwarp();
 #pragma unroll
-            for (int n = 0; n < 64; ++n) atomicAdd(dst + n * HEAD_DIM, __uint_as_float(v[n]));
+          for (int q = 0; q < 32; ++q)
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(stg + static_cast<uint32_t>(q) * 128u +
+                                                          static_cast<uint32_t>(lane) * 4u),
+                         "r"(v[q])
+                         : "memory");
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int qb = (c < 2) ? i0 : i1;
+            tma_reduce_add_2d(&tm_dq, stg, wq * 32,
+                              it.bh * S + qb * BLOCK + (c & 1) * 32);
+            bulk_commit_group();
           }
         }
       }
@@ -528,6 +568,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       ++itc;
     }
+    // Every reduction this warp issued has landed before the CTA retires.
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before_sync();
@@ -538,16 +581,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 }  // namespace
 
-cudaError_t make_tmap_rows128_f16(CUtensorMap* map, const void* ptr, long rows) {
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
                                                      cudaEnableDefault, &q);
-    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return nullptr;
     encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
+  return encode;
+}
+
+// [rows, 128] fp32 (the dQ accumulator), box 32 columns x 32 rows, no swizzle.
+cudaError_t make_tmap_rows128_f32(CUtensorMap* map, const void* ptr, long rows) {
+  auto encode = tensor_map_encoder();
+  if (!encode) return cudaErrorNotSupported;
+  const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(HEAD_DIM), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(HEAD_DIM) * sizeof(float)};
+  const cuuint32_t box[2] = {32u, 32u};
+  const cuuint32_t estride[2] = {1u, 1u};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), gdim,
+                      gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t make_tmap_rows128_f16(CUtensorMap* map, const void* ptr, long rows) {
+  auto encode = tensor_map_encoder();
+  if (!encode) return cudaErrorNotSupported;
   const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(HEAD_DIM), static_cast<cuuint64_t>(rows)};
   const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(HEAD_DIM) * sizeof(__half)};
   const cuuint32_t box[2] = {64u, 64u};
@@ -561,8 +629,9 @@ cudaError_t make_tmap_rows128_f16(CUtensorMap* map, const void* ptr, long rows) 
 
 cudaError_t launch_bwd_main(const BwdMainArgs& a, cudaStream_t stream) {
   const long rows = static_cast<long>(a.B) * a.H * a.S;
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   cudaError_t e;
+  if ((e = make_tmap_rows128_f32(&tdq, a.dqacc, rows)) != cudaSuccess) return e;
   if ((e = make_tmap_rows128_f16(&tq, a.q16, rows)) != cudaSuccess) return e;
   if ((e = make_tmap_rows128_f16(&tk, a.k16, rows)) != cudaSuccess) return e;
   if ((e = make_tmap_rows128_f16(&tv, a.v16, rows)) != cudaSuccess) return e;
@@ -593,7 +662,7 @@ cudaError_t launch_bwd_main(const BwdMainArgs& a, cudaStream_t stream) {
   p.sm_scale = a.sm_scale;
   const int sms = device_sm_count();
   const int grid = p.total < sms ? p.total : sms;
-  bwd_main_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tq, tk, tv, tdo, p);
+  bwd_main_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tq, tk, tv, tdo, tdq, p);
   return cudaGetLastError();
 }
 

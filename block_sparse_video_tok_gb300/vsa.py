@@ -30,6 +30,11 @@ class VsaShape(ctypes.Structure):
                 ("seqlen", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
 
 
+class VsaBwdEvents(ctypes.Structure):
+    _fields_ = [("start", ctypes.c_void_p), ("before_main", ctypes.c_void_p),
+                ("after_main", ctypes.c_void_p), ("end", ctypes.c_void_p)]
+
+
 class VsaError(RuntimeError):
     """A libvsa call returned a non-OK status."""
 
@@ -50,6 +55,8 @@ SIGNATURES = {
     "vsa_bwd_workspace_bytes": (_SZ, [VsaShape]),
     "vsa_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _P, _F, VsaShape, _P, _P,
                                _P, _P, _SZ, _P]),
+    "vsa_bwd_timed": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _P, _F, VsaShape, _P,
+                                     _P, _P, _P, _SZ, ctypes.POINTER(VsaBwdEvents), _P]),
     "vsa_read_device_error": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
 }
 
@@ -173,9 +180,19 @@ def vsa_fwd(q, k, v, q2k_idx, q2k_num, vbs, sm_scale, o=None, lse=None, workspac
     return o, lse
 
 
+def _event_handle(ev):
+    if ev is None:
+        return None
+    if ev.cuda_event == 0:      # torch creates the CUDA event lazily, on first record
+        ev.record()
+    return ctypes.c_void_p(ev.cuda_event)
+
+
 def vsa_bwd(dout, q, k, v, o, lse, k2q_idx, k2q_num, vbs, sm_scale, dq=None, dk=None, dv=None,
-            workspace=None, stream=None):
-    """Block-sparse backward.  Returns (dq, dk, dv) bf16 [B,H,S,128]."""
+            workspace=None, stream=None, events=None):
+    """Block-sparse backward.  Returns (dq, dk, dv) bf16 [B,H,S,128].  ``events``: optional
+    dict of torch.cuda.Event (enable_timing) under keys start / before_main / after_main / end,
+    recorded around the backward's stages (vsa_bwd_timed)."""
     B, H, S, D = _activation_shape(q)
     for name, t in (("dout", dout), ("k", k), ("v", v), ("o", o)):
         _need(t, name, torch.bfloat16, 4)
@@ -195,10 +212,15 @@ def vsa_bwd(dout, q, k, v, o, lse, k2q_idx, k2q_num, vbs, sm_scale, dq=None, dk=
     need = int(lib().vsa_bwd_workspace_bytes(shape))
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-    _check(lib().vsa_bwd(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(k2q_idx),
-                         _ptr(k2q_num), max_q, _ptr(vbs), float(sm_scale), shape, _ptr(dq),
-                         _ptr(dk), _ptr(dv), _ptr(workspace),
-                         workspace.numel() * workspace.element_size(), _stream(stream)), "vsa_bwd")
+    args = (_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(k2q_idx),
+            _ptr(k2q_num), max_q, _ptr(vbs), float(sm_scale), shape, _ptr(dq), _ptr(dk), _ptr(dv),
+            _ptr(workspace), workspace.numel() * workspace.element_size())
+    if events is None:
+        _check(lib().vsa_bwd(*args, _stream(stream)), "vsa_bwd")
+    else:
+        ev = VsaBwdEvents(*(_event_handle(events.get(n)) for n in
+                            ("start", "before_main", "after_main", "end")))
+        _check(lib().vsa_bwd_timed(*args, ctypes.byref(ev), _stream(stream)), "vsa_bwd_timed")
     return dq, dk, dv
 
 

@@ -157,6 +157,28 @@ vsa_status vsa_bwd(const void* dout, const void* q, const void* k, const void* v
                    void* stream);
 
 /*
+ * vsa_bwd_timed -- vsa_bwd, plus CUDA events recorded on `stream` around its stages, for callers
+ * that time the kernels (a benchmark's roofline).  `events` may be NULL (then it is vsa_bwd);
+ * any NULL member is skipped.  Members are cudaEvent_t handles created by the caller:
+ *   start        before the preprocess,        before_main  before the main kernel,
+ *   after_main   after the main kernel,         end          after the dQ postprocess.
+ * The events do not change what is computed.
+ */
+typedef struct vsa_bwd_events {
+  void* start;
+  void* before_main;
+  void* after_main;
+  void* end;
+} vsa_bwd_events;
+
+vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const void* v,
+                         const void* o, const float* lse, const int32_t* k2q_idx,
+                         const int32_t* k2q_num, int32_t max_q_blocks, const int32_t* vbs,
+                         float sm_scale, vsa_shape shape, void* dq, void* dk, void* dv,
+                         void* workspace, size_t workspace_bytes, const vsa_bwd_events* events,
+                         void* stream);
+
+/*
  * vsa_read_device_error -- synchronise `stream`, then copy the device error word of a
  * vsa_fwd / vsa_bwd workspace (the bits raised by the last call that used it) to *bits.
  */
