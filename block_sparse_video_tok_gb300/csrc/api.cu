@@ -70,6 +70,12 @@ T* ws_at(void* ws, size_t off) {
 
 }  // namespace
 
+namespace vsa {
+
+vsa_status record_cuda_failure(cudaError_t e) { return cuda_fail(e); }
+
+}  // namespace vsa
+
 extern "C" {
 
 const char* vsa_status_string(vsa_status status) {

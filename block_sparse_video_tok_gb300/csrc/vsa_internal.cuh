@@ -174,4 +174,7 @@ cudaError_t make_tmap_rows128_f16(CUtensorMap* map, const void* base, long rows)
 
 int device_sm_count();
 
+// Records `e` as this thread's last CUDA error (vsa_last_cuda_error) and returns VSA_ERR_CUDA.
+vsa_status record_cuda_failure(cudaError_t e);
+
 }  // namespace vsa

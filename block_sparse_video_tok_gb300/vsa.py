@@ -57,6 +57,8 @@ SIGNATURES = {
                                _P, _P, _SZ, _P]),
     "vsa_bwd_timed": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _P, _F, VsaShape, _P,
                                      _P, _P, _P, _SZ, ctypes.POINTER(VsaBwdEvents), _P]),
+    "vsa_bwd_no_alloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _P, _F, VsaShape,
+                                        _P, _P, _P, _P]),
     "vsa_read_device_error": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
 }
 
@@ -221,6 +223,32 @@ def vsa_bwd(dout, q, k, v, o, lse, k2q_idx, k2q_num, vbs, sm_scale, dq=None, dk=
         ev = VsaBwdEvents(*(_event_handle(events.get(n)) for n in
                             ("start", "before_main", "after_main", "end")))
         _check(lib().vsa_bwd_timed(*args, ctypes.byref(ev), _stream(stream)), "vsa_bwd_timed")
+    return dq, dk, dv
+
+
+def vsa_bwd_no_alloc(dout, q, k, v, o, lse, k2q_idx, k2q_num, vbs, sm_scale, dq=None, dk=None,
+                     dv=None, stream=None):
+    """vsa_bwd without a workspace argument: the library uses its static scratch array (for
+    callers that cannot allocate device memory; see include/vsa.h).  Returns (dq, dk, dv)."""
+    B, H, S, D = _activation_shape(q)
+    for name, t in (("dout", dout), ("k", k), ("v", v), ("o", o)):
+        _need(t, name, torch.bfloat16, 4)
+        if t.shape != q.shape:
+            raise ValueError("%s must have q's shape" % name)
+    _need(lse, "lse", torch.float32, 3)
+    _need(k2q_num, "k2q_num", torch.int32, 3)
+    _need(vbs, "vbs", torch.int32, 1)
+    _need(k2q_idx, "k2q_idx", torch.int32)
+    max_q = k2q_idx.shape[-1]
+    if k2q_idx.numel() != B * H * (S // BLOCK) * max_q:
+        raise ValueError("k2q_idx must hold [B, H, nb, max_q_blocks] entries")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check(lib().vsa_bwd_no_alloc(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                  _ptr(k2q_idx), _ptr(k2q_num), max_q, _ptr(vbs), float(sm_scale),
+                                  make_shape(B, H, S, D), _ptr(dq), _ptr(dk), _ptr(dv),
+                                  _stream(stream)), "vsa_bwd_no_alloc")
     return dq, dk, dv
 
 

@@ -178,6 +178,42 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
                          void* workspace, size_t workspace_bytes, const vsa_bwd_events* events,
                          void* stream);
 
+/* Largest workspace vsa_bwd_no_alloc can serve (32 MiB): the size of the static scratch array
+ * that every GPU loading this library holds until the process exits.  A shape needs
+ * vsa_bwd_workspace_bytes(shape) of it, about 1540 bytes per (batch, head, token) row plus a
+ * small header: for example B = 1, H = 4, S = 4096 fits, H = 8 at S = 4096 does not. */
+#define VSA_BWD_NO_ALLOC_MAX_WORKSPACE_BYTES (32u * 1024u * 1024u)
+
+/*
+ * vsa_bwd_no_alloc -- the backward (same arguments, same results as vsa_bwd) without a workspace
+ * argument, for callers that cannot allocate device memory.  The pages have no counterpart of
+ * this entry point; it exists for this library's users.
+ *
+ * Who needs it: code that runs inside a host framework which owns all device memory and does not
+ * let a plugin allocate (cudaMalloc synchronises the device, can fail under fragmentation and
+ * escapes the framework's accounting), or a service with a fixed device-memory budget that has
+ * no room to hand over a workspace per call.  Such callers still pass every input and output
+ * buffer; only the scratch moves into the library.
+ *
+ * How: the scratch is a static device array of VSA_BWD_NO_ALLOC_MAX_WORKSPACE_BYTES inside
+ * libvsa.so.  The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that first call before
+ * any stream capture.  No call allocates anything.
+ *
+ * Limits and sharing: a shape needing more than VSA_BWD_NO_ALLOC_MAX_WORKSPACE_BYTES of scratch
+ * is rejected with VSA_ERR_WORKSPACE before anything is enqueued.  Every call uses the same
+ * array, which keeps the previous call's contents (each call clears what must start at zero).
+ * Calls whose GPU work overlaps -- on different streams, or from host threads that are not
+ * ordered -- race on the array; order them (one stream, or events).  The device error word of
+ * the last call sits at the start of the array and is not reachable through
+ * vsa_read_device_error.
+ */
+vsa_status vsa_bwd_no_alloc(const void* dout, const void* q, const void* k, const void* v,
+                            const void* o, const float* lse, const int32_t* k2q_idx,
+                            const int32_t* k2q_num, int32_t max_q_blocks, const int32_t* vbs,
+                            float sm_scale, vsa_shape shape, void* dq, void* dk, void* dv,
+                            void* stream);
+
 /*
  * vsa_read_device_error -- synchronise `stream`, then copy the device error word of a
  * vsa_fwd / vsa_bwd workspace (the bits raised by the last call that used it) to *bits.

@@ -32,7 +32,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(vsa):
     names = declared_functions()
-    assert len(names) == 9, names
+    assert len(names) == 10, names
     lib = vsa.lib()
     for name in names:
         assert hasattr(lib, name), name
