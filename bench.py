@@ -51,6 +51,25 @@ def parse():
     return ap.parse_args()
 
 
+def main_kernel_traffic(config):
+    """DRAM bytes per main-kernel launch from the committed ncu summary of this workload, or None
+    when there is none or the kernel source changed since it was captured."""
+    import hashlib
+    import re
+    prof = os.path.join(ROOT, "profiles", "bwd_main_%s.md" % config.split("_")[0])
+    src = os.path.join(ROOT, "block_sparse_video_tok_gb300", "csrc", "bwd_main.cu")
+    if not os.path.exists(prof):
+        return None
+    text = open(prof).read()
+    m_sha = re.search(r"sha256 at capture: `([0-9a-f]{64})`", text)
+    m_tr = re.search(r"traffic_bytes_per_launch \| (\d+)", text)
+    if not (m_sha and m_tr):
+        return None
+    if hashlib.sha256(open(src, "rb").read()).hexdigest() != m_sha.group(1):
+        return None
+    return int(m_tr.group(1))
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -174,15 +193,11 @@ class OracleSampler:
         self.idx = case["q2k_idx"][b:b + 1, h:h + 1]
         self.num = case["q2k_num"][b:b + 1, h:h + 1]
         self.nb, self.vbs, self.sc = case["nb"], case["vbs"], case["sm_scale"]
-        k2q_idx, k2q_num, _ = orc.invert(self.idx, self.num, self.nb)
-        self.kv = [0, 1] if self.nb > 1 else [0]
-        self.pairs_kv = int(sum(k2q_num[0, 0, j] for j in self.kv))
-        sel = set(int(i) for j in self.kv for i in k2q_idx[0, 0, j, :k2q_num[0, 0, j]])
+        self.k2q_idx, self.k2q_num, _ = orc.invert(self.idx, self.num, self.nb)
         S, D = self.sub["q"].shape[2:]
         self.o = np.zeros((1, 1, S, D))
         self.lse = np.zeros((1, 1, S))
         self.have = set()
-        self._forward(sorted(sel | {0}))
 
     def _forward(self, blocks):
         blocks = [i for i in blocks if i not in self.have]
@@ -200,32 +215,39 @@ class OracleSampler:
     def pairs_q(self, m):
         return int(sum(len(set(self.idx[0, 0, i, :self.num[0, 0, i]].tolist())) for i in range(m)))
 
+    def pairs_kv(self, m):
+        return int(self.k2q_num[0, 0, :m].sum())
+
     def run(self, m):
-        """Time one sample with dQ rows of m q blocks.  Returns (TFLOPS, seconds)."""
+        """Time one sample: dQ rows of q blocks 0..m-1 and dK/dV rows of kv blocks 0..m-1.
+        Returns (TFLOPS, seconds)."""
         m = max(1, min(m, self.nb))
-        self._forward(range(m))
+        need = set(range(m))
+        for j in range(m):
+            need.update(int(i) for i in self.k2q_idx[0, 0, j, :self.k2q_num[0, 0, j]])
+        self._forward(sorted(need))
         s = self.sub
         t0 = time.perf_counter()
         self.orc.bwd(s["q"], s["k"], s["v"], self.o, s["do"], self.lse, self.idx, self.num,
-                     self.vbs, self.sc, qblocks=list(range(m)), kvblocks=self.kv)
+                     self.vbs, self.sc, qblocks=list(range(m)), kvblocks=list(range(m)))
         t = time.perf_counter() - t0
         # The oracle's dQ loop recomputes S, dP and forms dQ (3 GEMM-sized products per pair);
         # its dK/dV loop recomputes S, dP and forms dV, dK (4 per pair): a pair completed = 7.
-        done = (3 * self.pairs_q(m) + 4 * self.pairs_kv) / 7.0
+        done = (3 * self.pairs_q(m) + 4 * self.pairs_kv(m)) / 7.0
         return done * FLOP_PER_PAIR / t / 1e12, t
 
     def size_for(self, target_s):
         """m whose sample takes about target_s seconds (from a small calibration run)."""
-        m0 = min(4, self.nb)
+        m0 = min(max(4, 2 * self.orc.num_threads()), self.nb)  # enough blocks for every thread
         _, t = self.run(m0)
         return int(max(1, min(self.nb, m0 * target_s / max(t, 1e-3))))
 
     def describe(self, m):
         b, h = self.head
         return ("oracle backward (fp64, OpenMP) on head (b=%d,h=%d): dQ rows of q blocks 0..%d "
-                "(%d pairs) and dK/dV rows of kv blocks %s (%d pairs); TFLOPS counted as "
-                "completed pairs x 5 GEMMs" % (b, h, m - 1, self.pairs_q(m), self.kv,
-                                               self.pairs_kv))
+                "(%d pairs) and dK/dV rows of kv blocks 0..%d (%d pairs); TFLOPS counted as "
+                "completed pairs x 5 GEMMs" % (b, h, m - 1, self.pairs_q(m), m - 1,
+                                               self.pairs_kv(m)))
 
 
 def run_reference(args, rank, world):
@@ -432,7 +454,7 @@ def main():
         "breakdown_ms": {"invert": float(np.mean(inv_ms)), "preprocess": float(np.mean(pre_ms)),
                          "main": main_avg, "postprocess": float(np.mean(post_ms))},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": main_kernel_traffic(args.config),
                      "peak_source": "%s bf16_tflops (burst); fp16 dense rate = bf16" % peak_src,
                      "frac_of_sustained": achieved / peak_sus},
         "fwd": {"ms": fwd_ms, "note": "operand producer, timed alone; not in the step"},
