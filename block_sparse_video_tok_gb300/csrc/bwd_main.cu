@@ -18,16 +18,17 @@
 // head-dim on the lanes, so each warp's fp32 reduction into the dQ accumulator covers 128
 // contiguous bytes of one query row.
 //
-// Roles (320 threads):
-//   warps 0-3  softmax: thread r owns query row r of the pair; reads S and dP rows from TMEM,
-//              writes P and dS (fp16, swizzled) to shared memory.
-//   warps 4-7  dQ drain + epilogue: thread d owns head-dim row d; moves dQ^T through a 4 KB
+// Roles (448 threads):
+//   warps 0-7  softmax: warps w and w+4 share TMEM lane quarter w (query rows 32w..32w+31 of the
+//              pair) and split the 64 kv columns in halves; each thread turns 32 columns of its
+//              S and dP row into P and dS (fp16, swizzled) in shared memory.
+//   warps 8-11 dQ drain + epilogue: thread d owns head-dim row d; moves dQ^T through a 4 KB
 //              per-warp staging box ([32 query rows x 32 head dims] fp32) and adds it into the fp32
 //              accumulator with TMA bulk tensor reductions; at the end of an item writes dK, dV
 //              (bf16, zeros for padded rows; whole zero blocks for items no q block selects).
-//   warp 8     TMA producer (K_j, V_j once per item; Q and dO of each pair into a 2-stage ring);
+//   warp 12    TMA producer (K_j, V_j once per item; Q and dO of each pair into a 2-stage ring);
 //              also allocates TMEM.
-//   warp 9     UMMA issuer (one thread).  Per step g: S/dP(g), then dQ^T(g-1), then (once the
+//   warp 13    UMMA issuer (one thread).  Per step g: S/dP(g), then dQ^T(g-1), then (once the
 //              softmax has written P/dS(g)) dV^T/dK^T(g), after which the Q/dO stage of step g is
 //              released -- so a stage's reload has almost a whole step to land, the tensor pipe
 //              works on dQ^T(g-1) while the softmax of step g runs, and the dQ^T drain lags one
@@ -45,7 +46,11 @@ namespace vsa {
 
 namespace {
 
-constexpr int NUM_THREADS = 320;
+constexpr int NUM_THREADS = 448;
+constexpr int SOFTMAX_WARPS = 8;  // warps 0-7: lane quarter w % 4, column half w / 4
+constexpr int DRAIN_WARP0 = 8;    // warps 8-11: dQ drain + epilogue
+constexpr int TMA_WARP = 12;
+constexpr int MMA_WARP = 13;
 
 // Shared memory map (offsets from a 1024-byte aligned base).
 constexpr uint32_t SM_K = 0;                    // K_j: 2 chunks x [64 kv x 128 B]
@@ -181,17 +186,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(bar(DQ_FREE0 + s), 4);
     }
     mbar_init(bar(SDP_FULL), 1);
-    mbar_init(bar(P_READY), 4);
+    mbar_init(bar(P_READY), SOFTMAX_WARPS);
     mbar_init(bar(ACC_FULL), 1);
     mbar_init(bar(ACC_EMPTY), 4);
     mbar_init(bar(DRAIN), 1);
     fence_barrier_init();
   }
-  if (warp == 8) {
+  if (warp == TMA_WARP) {
     tmem_alloc(base + SM_TMEM_SLOT, 512);
     tmem_relinquish();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == TMA_WARP && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -203,7 +208,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp == TMA_WARP) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t g = 0;      // global pair-step counter
@@ -273,26 +278,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 9) {
+  } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------------ UMMA issuer
     if (lane == 0) {
       uint32_t g = 0, itc = 0;
       bool ok = true, issued = false;
+      // Operand descriptors, built once; each UMMA only adds a constant byte offset to them.
+      //   K-major (S, dP; dQ^T's B): 32 B per k-step inside a 128-B row, 64-element chunks apart.
+      //   MN-major (dV^T, dK^T, dQ^T's A): 2048 B (16 rows) per k-step.
+      const uint64_t k_kmaj = sdesc_sw128(base + SM_K, 16, 1024);
+      const uint64_t v_kmaj = sdesc_sw128(base + SM_V, 16, 1024);
+      const uint64_t k_mn = sdesc_sw128(base + SM_K, 8192, 1024);
+      const uint64_t p_mn = sdesc_sw128(base + SM_P, 16384, 1024);
+      const uint64_t q_kmaj = sdesc_sw128(base + SM_Q, 16, 1024);
+      const uint64_t do_kmaj = sdesc_sw128(base + SM_DO, 16, 1024);
+      const uint64_t q_mn = sdesc_sw128(base + SM_Q, 16384, 1024);
+      const uint64_t do_mn = sdesc_sw128(base + SM_DO, 16384, 1024);
+      const uint64_t ds_mn = sdesc_sw128(base + SM_DS, 16384, 1024);
+      const uint64_t ds_kmaj = sdesc_sw128(base + SM_DS, 16, 1024);
+      const uint32_t t_s = tmem + TM_S, t_dp = tmem + TM_DP, t_dv = tmem + TM_DVT,
+                     t_dk = tmem + TM_DKT;
       // S = Q_p K_j^T and dP = dO_p V_j^T of step gs (stage gs & 1).
       auto issue_sdp = [&](uint32_t gs) {
-        const uint32_t s = gs & 1u;
-        const uint32_t qa = base + SM_Q + s * 32768u, da = base + SM_DO + s * 32768u;
+        const uint32_t so = (gs & 1u) * 32768u;
+        const uint64_t qa = sdesc_advance(q_kmaj, so), da = sdesc_advance(do_kmaj, so);
+        umma_f16_c<false>(t_s, qa, k_kmaj, IDESC_SDP);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t c = kk >> 2, off = (kk & 3) * 32;
-          umma_f16(tmem + TM_S, sdesc_sw128(qa + c * 16384u + off, 16, 1024),
-                   sdesc_sw128(base + SM_K + c * 8192u + off, 16, 1024), IDESC_SDP, kk > 0);
+        for (int kk = 1; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384u + (kk & 3) * 32u;
+          umma_f16_c<true>(t_s, sdesc_advance(qa, off),
+                           sdesc_advance(k_kmaj, (kk >> 2) * 8192u + (kk & 3) * 32u), IDESC_SDP);
         }
+        umma_f16_c<false>(t_dp, da, v_kmaj, IDESC_SDP);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t c = kk >> 2, off = (kk & 3) * 32;
-          umma_f16(tmem + TM_DP, sdesc_sw128(da + c * 16384u + off, 16, 1024),
-                   sdesc_sw128(base + SM_V + c * 8192u + off, 16, 1024), IDESC_SDP, kk > 0);
+        for (int kk = 1; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384u + (kk & 3) * 32u;
+          umma_f16_c<true>(t_dp, sdesc_advance(da, off),
+                           sdesc_advance(v_kmaj, (kk >> 2) * 8192u + (kk & 3) * 32u), IDESC_SDP);
         }
         umma_commit(bar(SDP_FULL));
       };
@@ -302,14 +324,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!mbar_wait_bounded(bar(DQ_FREE0 + b), ((gs >> 1) & 1u) ^ 1u, abort, WAIT_LIMIT_NS))
           return false;
         tc_fence_after_sync();
-        const uint32_t dsa = base + SM_DS + b * 16384u;
+        const uint64_t dsb = sdesc_advance(ds_kmaj, b * 16384u);
+        const uint32_t t_dq = tmem + TM_DQT + b * 128u;
+        umma_f16_c<false>(t_dq, k_mn, dsb, IDESC_DQ);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_f16(tmem + TM_DQT + b * 128u, sdesc_sw128(base + SM_K + kk * 2048u, 8192, 1024),
-                   sdesc_sw128(dsa + kk * 32u, 16, 1024), IDESC_DQ, kk > 0);
+        for (int kk = 1; kk < 4; ++kk)
+          umma_f16_c<true>(t_dq, sdesc_advance(k_mn, kk * 2048u), sdesc_advance(dsb, kk * 32u),
+                           IDESC_DQ);
         umma_commit(bar(DQ_FULL0 + b));
         umma_commit(bar(PDS_FREE0 + b));
         return true;
+      };
+      // dV^T += dO_p^T P and dK^T += Q_p^T dS of step gs; the first step of an item overwrites.
+      auto issue_dvdk = [&](uint32_t gs, bool first) {
+        const uint32_t so = (gs & 1u) * 32768u;
+        const uint64_t da = sdesc_advance(do_mn, so), qa = sdesc_advance(q_mn, so);
+        const uint64_t dsb = sdesc_advance(ds_mn, (gs & 1u) * 16384u);
+        if (first)
+          umma_f16_c<false>(t_dv, da, p_mn, IDESC_DVK);
+        else
+          umma_f16_c<true>(t_dv, da, p_mn, IDESC_DVK);
+#pragma unroll
+        for (int kk = 1; kk < 8; ++kk)
+          umma_f16_c<true>(t_dv, sdesc_advance(da, kk * 2048u), sdesc_advance(p_mn, kk * 2048u),
+                           IDESC_DVK);
+        if (first)
+          umma_f16_c<false>(t_dk, qa, dsb, IDESC_DVK);
+        else
+          umma_f16_c<true>(t_dk, qa, dsb, IDESC_DVK);
+#pragma unroll
+        for (int kk = 1; kk < 8; ++kk)
+          umma_f16_c<true>(t_dk, sdesc_advance(qa, kk * 2048u), sdesc_advance(dsb, kk * 2048u),
+                           IDESC_DVK);
       };
       for (int w = blockIdx.x; w < p.total && ok; w += gridDim.x) {
         const Item it = decode_item(p, w);
@@ -343,16 +389,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           tc_fence_after_sync();
-          const uint32_t qa = base + SM_Q + s * 32768u, da = base + SM_DO + s * 32768u;
-          const uint32_t pa = base + SM_P, dsa = base + SM_DS + s * 16384u;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_f16(tmem + TM_DVT, sdesc_sw128(da + kk * 2048u, 16384, 1024),
-                     sdesc_sw128(pa + kk * 2048u, 16384, 1024), IDESC_DVK, (pp > 0 || kk > 0));
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_f16(tmem + TM_DKT, sdesc_sw128(qa + kk * 2048u, 16384, 1024),
-                     sdesc_sw128(dsa + kk * 2048u, 16384, 1024), IDESC_DVK, (pp > 0 || kk > 0));
+          issue_dvdk(g, pp == 0);
           umma_commit(bar(QDO_EMPTY0 + s));  // Q_p and dO_p of step g are no longer read
         }
         if (!ok) break;
@@ -373,10 +410,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < SOFTMAX_WARPS) {
     // ------------------------------------------------------------------ softmax / dS
-    const int r = warp * 32 + lane;  // query row of the pair == TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int quarter = warp & 3, h = warp >> 2;  // TMEM lane quarter; S/dP column half
+    const int r = quarter * 32 + lane;            // query row of the pair == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     uint32_t g = 0;
     const uint32_t sw = static_cast<uint32_t>(r & 7);
     for (int w = blockIdx.x; w < p.total; w += gridDim.x) {
@@ -406,13 +444,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after_sync();
         const uint32_t prow = base + SM_P + static_cast<uint32_t>(r) * 128u;
         const uint32_t dsrow = base + SM_DS + s * 16384u + static_cast<uint32_t>(r) * 128u;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        {
           uint32_t sv[32], dpv[32];
           tmem_ld_32x32b_x32(tmem + lane_off + TM_S + h * 32u, sv);
           tmem_ld_32x32b_x32(tmem + lane_off + TM_DP + h * 32u, dpv);
           tmem_wait_ld();
-          uint32_t pk[16], dk[16];  // P and dS of 32 columns, fp16 pairs
+          uint32_t pk[16], dk[16];  // P and dS of this warp's 32 columns, fp16 pairs
           if (full) {  // every column visible: no masking
 #pragma unroll
             for (int c = 0; c < 32; c += 2) {
@@ -436,7 +473,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
           // The buffer's previous contents (step g-2) must have been consumed by dQ^T(g-2).
-          if (h == 0 && !warp_wait(bar(PDS_FREE0 + s), ((g >> 1) & 1u) ^ 1u, abort, lane)) {
+          if (!warp_wait(bar(PDS_FREE0 + s), ((g >> 1) & 1u) ^ 1u, abort, lane)) {
             ok = false;
             break;
           }
@@ -466,7 +503,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------------ dQ drain + epilogue
-    const int wq = warp - 4;
+    const int wq = warp - DRAIN_WARP0;  // lane quarter (DRAIN_WARP0 % 4 == 0)
     const int d = wq * 32 + lane;  // head-dim row == TMEM lane (dK/dV epilogue column)
     const uint32_t stg = base + SM_STG + static_cast<uint32_t>(wq) * 4096u;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
@@ -545,26 +582,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         break;
       }
       tc_fence_after_sync();
-      {
-        uint32_t v[64];
-        tmem_ld_32x32b_x32(tmem + lane_off + TM_DVT, v);
-        tmem_ld_32x32b_x32(tmem + lane_off + TM_DVT + 32u, v + 32);
+      // dV^T and dK^T rows (head dim d, kv rows 0..63) in 32-column chunks; masked kv rows get
+      // an explicit +0.0.
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        const bool is_dk = c >= 2;
+        const uint32_t col = (is_dk ? TM_DKT : TM_DVT) + (c & 1) * 32u;
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem + lane_off + col, v);
         tmem_wait_ld();
+        if (c == 3) {
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(ACC_EMPTY));
+        }
+        __nv_bfloat16* out = (is_dk ? dk_out : dv_out) + (c & 1) * 32 * HEAD_DIM;
+        const float sc = is_dk ? sk_scale : sv_scale;
 #pragma unroll
-        for (int t = 0; t < BLOCK; ++t)
-          dv_out[t * HEAD_DIM] = __float2bfloat16_rn(t < vb ? __uint_as_float(v[t]) * sv_scale : 0.f);
-      }
-      {
-        uint32_t v[64];
-        tmem_ld_32x32b_x32(tmem + lane_off + TM_DKT, v);
-        tmem_ld_32x32b_x32(tmem + lane_off + TM_DKT + 32u, v + 32);
-        tmem_wait_ld();
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(ACC_EMPTY));
-#pragma unroll
-        for (int t = 0; t < BLOCK; ++t)
-          dk_out[t * HEAD_DIM] = __float2bfloat16_rn(t < vb ? __uint_as_float(v[t]) * sk_scale : 0.f);
+        for (int t = 0; t < 32; ++t)
+          out[t * HEAD_DIM] =
+              __float2bfloat16_rn((c & 1) * 32 + t < vb ? __uint_as_float(v[t]) * sc : 0.f);
       }
       ++itc;
     }
@@ -576,7 +613,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  if (warp == 8) tmem_dealloc(tmem, 512);
+  if (warp == TMA_WARP) tmem_dealloc(tmem, 512);
 }
 
 }  // namespace

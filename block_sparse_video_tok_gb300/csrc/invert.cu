@@ -38,19 +38,35 @@ __global__ void __launch_bounds__(INV_THREADS) invert_kernel(const int32_t* __re
   const int32_t* idx = q2k_idx + static_cast<size_t>(bh) * nq * topk;
   const int32_t* num = q2k_num + static_cast<size_t>(bh) * nq;
   const int entries = nq * topk;
-  for (int e = threadIdx.x; e < entries; e += blockDim.x) {
-    const int i = e / topk, s = e - i * topk;
-    const int c = num[i];
-    const int cnt = c < 0 ? 0 : (c > topk ? topk : c);
-    if (s == 0 && cnt != c) bad |= VSA_DEVERR_Q2K_COUNT;
-    if (s >= cnt) continue;
-    const int j = idx[e];
-    if (j < 0 || j >= nb) {
-      bad |= VSA_DEVERR_Q2K_ID;
-      continue;
+  // Sixteen independent loads per thread before any is used, so the scan is not bound by one
+  // L2 round trip per entry.
+  constexpr int U = 16;
+  for (int e0 = 0; e0 < entries; e0 += U * INV_THREADS) {
+    int jv[U], cv[U], sv[U], iv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int e = e0 + u * INV_THREADS + static_cast<int>(threadIdx.x);
+      const bool in = e < entries;
+      const int i = in ? e / topk : 0;
+      iv[u] = i;
+      sv[u] = in ? e - i * topk : topk;  // topk: never an active slot
+      jv[u] = in ? idx[e] : 0;
+      cv[u] = in ? num[i] : 0;
     }
-    const int jj = j - j0;
-    if (jj >= 0 && jj < ncols) atomicOr(&bm[jj * words + (i >> 5)], 1u << (i & 31));
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int c = cv[u];
+      const int cnt = c < 0 ? 0 : (c > topk ? topk : c);
+      if (sv[u] == 0 && cnt != c) bad |= VSA_DEVERR_Q2K_COUNT;
+      if (sv[u] >= cnt) continue;
+      const int j = jv[u];
+      if (j < 0 || j >= nb) {
+        bad |= VSA_DEVERR_Q2K_ID;
+        continue;
+      }
+      const int jj = j - j0;
+      if (jj >= 0 && jj < ncols) atomicOr(&bm[jj * words + (iv[u] >> 5)], 1u << (iv[u] & 31));
+    }
   }
   // Report invalid entries once per head (the first slice sees all of them).
   if (bad && blockIdx.y == 0 && err) atomicOr(err, bad);

@@ -148,6 +148,33 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// The same with the accumulate flag fixed at compile time (no runtime predicate set-up).
+template <bool ACCUMULATE>
+__device__ __forceinline__ void umma_f16_c(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc) {
+  if constexpr (ACCUMULATE) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.eq.u32 p, 1, 1;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, 1, 1;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc)
+        : "memory");
+  }
+}
+
+// Advance a shared-memory descriptor's start address by `bytes` (a multiple of 16).  The start
+// field is the low 14 bits (address >> 4); shared addresses stay below 2^18, so no carry leaves it.
+__device__ __forceinline__ uint64_t sdesc_advance(uint64_t desc, uint32_t bytes) {
+  return desc + static_cast<uint64_t>(bytes >> 4);
+}
+
 // Arrive once on `bar` when every UMMA this thread issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
