@@ -12,8 +12,12 @@
 //           O += P V_j   (A = P K-major, B = V_j MN-major; fp32 accumulator in TMEM).
 // No rescaling of O is needed, at the price of recomputing S once.
 //
-// Roles (192 threads): warps 0-3 softmax (thread r owns query row r), warp 4 TMA producer and
-// TMEM owner, warp 5 UMMA issuer.  TMEM (256 columns): S x2 [0,128), O [128,256).
+// Roles (320 threads): warps 0-7 softmax -- warps w and w+4 share TMEM lane quarter w (query
+// rows 32w..32w+31) and split the 64 kv columns of S (and the 128 columns of O) in halves, merging
+// their pass-1 row statistics through shared memory; warp 8 TMA producer and TMEM owner; warp 9
+// UMMA issuer, which in pass 2 issues S of the next kv block before waiting for P of the current
+// one, so the softmax and the tensor pipe overlap.  TMEM (256 columns): S x2 [0,128),
+// O [128,256).
 #include "ptx.cuh"
 #include "vsa_internal.cuh"
 
@@ -21,13 +25,17 @@ namespace vsa {
 
 namespace {
 
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 320;
+constexpr int SOFTMAX_WARPS = 8;
+constexpr int TMA_WARP = 8;
+constexpr int MMA_WARP = 9;
 constexpr int KV_STAGES = 4;
 
 constexpr uint32_t SM_Q = 0;                                // 2 chunks x [128 q x 128 B]
 constexpr uint32_t SM_KV = 32768;                           // stages x (K 16 KB, V 16 KB)
 constexpr uint32_t SM_P = SM_KV + KV_STAGES * 32768;        // 2 x [128 q x 128 B]
-constexpr uint32_t SM_BAR = SM_P + 2 * 16384;
+constexpr uint32_t SM_STAT = SM_P + 2 * 16384;              // [2 halves][128 rows] (max, sum)
+constexpr uint32_t SM_BAR = SM_STAT + 2 * 128 * 8;
 
 enum Bar : uint32_t {
   Q_FULL = 0,
@@ -41,7 +49,8 @@ enum Bar : uint32_t {
   O_FULL = P_FREE0 + 2,
   O_EMPTY,
   DRAIN,
-  NUM_BARS
+  STAT0,  // one per lane quarter: the two column-half warps have published their statistics
+  NUM_BARS = STAT0 + 4
 };
 constexpr uint32_t SM_TMEM_SLOT = SM_BAR + NUM_BARS * 8;
 constexpr uint32_t SM_ABORT = SM_TMEM_SLOT + 4;
@@ -157,16 +166,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(S_FULL0 + s), 1);
-      mbar_init(bar(S_FREE0 + s), 4);
-      mbar_init(bar(P_READY0 + s), 4);
+      mbar_init(bar(S_FREE0 + s), SOFTMAX_WARPS);
+      mbar_init(bar(P_READY0 + s), SOFTMAX_WARPS);
       mbar_init(bar(P_FREE0 + s), 1);
     }
     mbar_init(bar(O_FULL), 1);
-    mbar_init(bar(O_EMPTY), 4);
+    mbar_init(bar(O_EMPTY), SOFTMAX_WARPS);
     mbar_init(bar(DRAIN), 1);
+    for (int qq = 0; qq < 4; ++qq) mbar_init(bar(STAT0 + qq), 2);
     fence_barrier_init();
   }
-  if (warp == 4) {
+  if (warp == TMA_WARP) {
     tmem_alloc(base + SM_TMEM_SLOT, 256);
     tmem_relinquish();
   }
@@ -175,7 +185,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == TMA_WARP) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t lg = 0, itc = 0, q_loads = 0;
@@ -231,63 +241,100 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------------ UMMA issuer
     if (lane == 0) {
       uint32_t lg = 0, sg = 0, pg = 0, itc = 0;
       bool ok = true, issued = false;
+      const uint64_t q_kmaj = sdesc_sw128(base + SM_Q, 16, 1024);
+      const uint64_t kv_kmaj = sdesc_sw128(base + SM_KV, 16, 1024);    // K of stage 0
+      const uint64_t kv_mn = sdesc_sw128(base + SM_KV + 16384u, 8192, 1024);  // V of stage 0
+      const uint64_t p_kmaj = sdesc_sw128(base + SM_P, 16, 1024);
+      // S = Q_p K_j^T into S buffer sg & 1, K from KV stage lg % KV_STAGES.
+      auto issue_s = [&]() -> bool {
+        const uint32_t st = lg % KV_STAGES, sb = sg & 1u;
+        if (!mbar_wait_bounded(bar(KV_FULL0 + st), (lg / KV_STAGES) & 1u, abort, WAIT_LIMIT_NS))
+          return false;
+        if (!mbar_wait_bounded(bar(S_FREE0 + sb), ((sg >> 1) & 1u) ^ 1u, abort, WAIT_LIMIT_NS))
+          return false;
+        tc_fence_after_sync();
+        const uint64_t kd = sdesc_advance(kv_kmaj, st * 32768u);
+        const uint32_t ts = tmem + TM_S + sb * 64u;
+        umma_f16_c<false>(ts, q_kmaj, kd, IDESC_S);
+#pragma unroll
+        for (int kk = 1; kk < 8; ++kk) {
+          const uint32_t off = (kk & 3) * 32u;
+          umma_f16_c<true>(ts, sdesc_advance(q_kmaj, (kk >> 2) * 16384u + off),
+                           sdesc_advance(kd, (kk >> 2) * 8192u + off), IDESC_S);
+        }
+        umma_commit(bar(S_FULL0 + sb));
+        issued = true;
+        ++sg;
+        return true;
+      };
+      // O += P V_j with P buffer pg & 1 and V of KV stage `st`.
+      auto issue_pv = [&](uint32_t st, bool first) -> bool {
+        const uint32_t pb = pg & 1u;
+        if (!mbar_wait_bounded(bar(P_READY0 + pb), (pg >> 1) & 1u, abort, WAIT_LIMIT_NS))
+          return false;
+        if (first && !mbar_wait_bounded(bar(O_EMPTY), (itc & 1u) ^ 1u, abort, WAIT_LIMIT_NS))
+          return false;
+        tc_fence_after_sync();
+        const uint64_t pa = sdesc_advance(p_kmaj, pb * 16384u);
+        const uint64_t vb = sdesc_advance(kv_mn, st * 32768u);
+        if (first)
+          umma_f16_c<false>(tmem + TM_O, pa, vb, IDESC_PV);
+        else
+          umma_f16_c<true>(tmem + TM_O, pa, vb, IDESC_PV);
+#pragma unroll
+        for (int kk = 1; kk < 4; ++kk)
+          umma_f16_c<true>(tmem + TM_O, sdesc_advance(pa, kk * 32u), sdesc_advance(vb, kk * 2048u),
+                           IDESC_PV);
+        umma_commit(bar(P_FREE0 + pb));
+        umma_commit(bar(KV_EMPTY0 + st));
+        ++pg;
+        return true;
+      };
       for (int w = blockIdx.x; w < p.total && ok; w += gridDim.x) {
         const Pair q = decode_pair(p, w);
-        if (union_size(p, q) == 0) continue;
+        const int nu = union_size(p, q);
+        if (nu == 0) continue;
         if (!mbar_wait_bounded(bar(Q_FULL), itc & 1u, abort, WAIT_LIMIT_NS)) {
           ok = false;
           break;
         }
-        for (int pass = 0; pass < 2 && ok; ++pass) {
-          int e = 0;
-          ok = for_union(p, q, [&](int /*j*/) {
-            const uint32_t st = lg % KV_STAGES, sb = sg & 1u;
-            if (!mbar_wait_bounded(bar(KV_FULL0 + st), (lg / KV_STAGES) & 1u, abort,
-                                   WAIT_LIMIT_NS))
-              return false;
-            if (!mbar_wait_bounded(bar(S_FREE0 + sb), ((sg >> 1) & 1u) ^ 1u, abort,
-                                   WAIT_LIMIT_NS))
-              return false;
-            tc_fence_after_sync();
-            const uint32_t kd = base + SM_KV + st * 32768u;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t c = kk >> 2, off = (kk & 3) * 32;
-              umma_f16(tmem + TM_S + sb * 64u, sdesc_sw128(base + SM_Q + c * 16384u + off, 16, 1024),
-                       sdesc_sw128(kd + c * 8192u + off, 16, 1024), IDESC_S, kk > 0);
-            }
-            issued = true;
-            umma_commit(bar(S_FULL0 + sb));
-            if (pass == 1) {
-              const uint32_t pb = pg & 1u;
-              if (!mbar_wait_bounded(bar(P_READY0 + pb), (pg >> 1) & 1u, abort, WAIT_LIMIT_NS))
-                return false;
-              if (e == 0 &&
-                  !mbar_wait_bounded(bar(O_EMPTY), (itc & 1u) ^ 1u, abort, WAIT_LIMIT_NS))
-                return false;
-              tc_fence_after_sync();
-              const uint32_t pa = base + SM_P + pb * 16384u;
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                umma_f16(tmem + TM_O, sdesc_sw128(pa + kk * 32u, 16, 1024),
-                         sdesc_sw128(kd + 16384u + kk * 2048u, 8192, 1024), IDESC_PV,
-                         (e > 0 || kk > 0));
-              umma_commit(bar(P_FREE0 + pb));
-              ++pg;
-            }
-            umma_commit(bar(KV_EMPTY0 + st));
-            ++lg;
-            ++sg;
-            ++e;
-            return true;
-          });
+        // Pass 1: S of every union block; K stages are released as soon as S is done.
+        for (int e = 0; e < nu && ok; ++e) {
+          const uint32_t st = lg % KV_STAGES;
+          if (!issue_s()) {
+            ok = false;
+            break;
+          }
+          umma_commit(bar(KV_EMPTY0 + st));
+          ++lg;
         }
         if (!ok) break;
+        // Pass 2: S(e+1) is issued before P.V(e) waits for the softmax of block e.
+        const uint32_t lg0 = lg;
+        if (!issue_s()) {
+          ok = false;
+          break;
+        }
+        for (int e = 0; e < nu && ok; ++e) {
+          if (e + 1 < nu) {
+            lg = lg0 + e + 1;
+            if (!issue_s()) {
+              ok = false;
+              break;
+            }
+          }
+          if (!issue_pv((lg0 + e) % KV_STAGES, e == 0)) {
+            ok = false;
+            break;
+          }
+        }
+        if (!ok) break;
+        lg = lg0 + nu;
         umma_commit(bar(O_FULL));
         umma_commit(bar(Q_EMPTY));
         ++itc;
@@ -301,10 +348,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------------ softmax (warps 0-3)
-    const int r = warp * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    // ------------------------------------------------------------------ softmax (warps 0-7)
+    const int quarter = warp & 3, h = warp >> 2;  // TMEM lane quarter; column half
+    const int r = quarter * 32 + lane;            // query row of the pair == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t sw = static_cast<uint32_t>(r & 7);
+    float2* stat = reinterpret_cast<float2*>(gbase + SM_STAT);  // [half][row] (max, sum)
     uint32_t sg = 0, pg = 0, itc = 0;
     for (int w = blockIdx.x; w < p.total; w += gridDim.x) {
       const Pair q = decode_pair(p, w);
@@ -313,11 +362,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const size_t grow = static_cast<size_t>(q.bh) * S +
                           static_cast<size_t>(r < 64 ? q.i0 : (q.i1 >= 0 ? q.i1 : q.i0)) * BLOCK +
                           (r & 63);
-      uint4* orow = reinterpret_cast<uint4*>(p.o + grow * HEAD_DIM);
+      uint4* orow = reinterpret_cast<uint4*>(p.o + grow * HEAD_DIM) + h * 8;
       if (union_size(p, q) == 0) {
         if (valid) {
-          for (int c = 0; c < 16; ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
-          p.lse[grow] = -INFINITY;
+          for (int c = 0; c < 8; ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
+          if (h == 0) p.lse[grow] = -INFINITY;
         }
         continue;
       }
@@ -333,25 +382,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!warp_wait(bar(S_FULL0 + sb), (sg >> 1) & 1u, abort, lane)) return false;
           tc_fence_after_sync();
           const bool mine = valid && ((own[j >> 5] >> (j & 31)) & 1u);
-          const int vb = mine ? clamp_vbs(p.vbs[j]) : 0;
-          uint32_t sv[64];
-          tmem_ld_32x32b_x32(tmem + lane_off + TM_S + sb * 64u, sv);
-          tmem_ld_32x32b_x32(tmem + lane_off + TM_S + sb * 64u + 32u, sv + 32);
+          const int vb = mine ? clamp_vbs(p.vbs[j]) - h * 32 : 0;  // visible columns in my half
+          uint32_t sv[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + TM_S + sb * 64u + h * 32u, sv);
           tmem_wait_ld();
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(S_FREE0 + sb));
           ++sg;
           if (pass == 0) {
-            float mloc = -INFINITY;
-#pragma unroll
-            for (int u = 0; u < 64; ++u)
-              if (u < vb) mloc = fmaxf(mloc, __uint_as_float(sv[u]) * c1);
             if (vb > 0) {
+              float mloc = -INFINITY;
+#pragma unroll
+              for (int u = 0; u < 32; ++u)
+                if (u < vb) mloc = fmaxf(mloc, __uint_as_float(sv[u]) * c1);
               const float mn = fmaxf(m, mloc);
               float acc = 0.f;
 #pragma unroll
-              for (int u = 0; u < 64; ++u)
+              for (int u = 0; u < 32; ++u)
                 if (u < vb) acc += ex2(__uint_as_float(sv[u]) * c1 - mn);
               l = l * ex2(m - mn) + acc;
               m = mn;
@@ -359,9 +407,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             return true;
           }
           const float off = static_cast<float>(KP) - lse;
-          uint32_t pk[32];
+          uint32_t pk[16];
 #pragma unroll
-          for (int u = 0; u < 64; u += 2) {
+          for (int u = 0; u < 32; u += 2) {
             const float p0 = (u < vb) ? ex2(fmaf(__uint_as_float(sv[u]), c1, off)) : 0.f;
             const float p1 = (u + 1 < vb) ? ex2(fmaf(__uint_as_float(sv[u + 1]), c1, off)) : 0.f;
             pk[u >> 1] = pack_half2(p0, p1);
@@ -370,8 +418,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!warp_wait(bar(P_FREE0 + pb), ((pg >> 1) & 1u) ^ 1u, abort, lane)) return false;
           const uint32_t prow = base + SM_P + pb * 16384u + static_cast<uint32_t>(r) * 128u;
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            const uint32_t phys = (static_cast<uint32_t>(ch) ^ sw) * 16u;
+          for (int ch = 0; ch < 4; ++ch) {
+            const uint32_t phys = ((static_cast<uint32_t>(h * 4 + ch)) ^ sw) * 16u;
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + phys),
                          "r"(pk[4 * ch]), "r"(pk[4 * ch + 1]), "r"(pk[4 * ch + 2]),
                          "r"(pk[4 * ch + 3])
@@ -383,7 +431,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ++pg;
           return true;
         });
-        if (pass == 0) lse = (l > 0.f) ? m + log2f(l) : -INFINITY;
+        if (pass == 0 && ok) {
+          // Merge the two column halves' statistics of each row.  The slot is rewritten only in
+          // the next item's pass 1, which cannot start before both warps finished this item.
+          stat[h * 128 + r] = make_float2(m, l);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(STAT0 + quarter));
+          if (!warp_wait(bar(STAT0 + quarter), itc & 1u, abort, lane)) {
+            ok = false;
+            break;
+          }
+          const float2 o2 = stat[(1 - h) * 128 + r];
+          const float mm = fmaxf(m, o2.x);
+          const float ll = (mm == -INFINITY) ? 0.f : l * ex2(m - mm) + o2.y * ex2(o2.x - mm);
+          lse = (ll > 0.f) ? mm + log2f(ll) : -INFINITY;
+        }
       }
       if (!ok) {
         if (lane == 0) raise_abort(abort, p.err);
@@ -395,30 +457,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       tc_fence_after_sync();
       const float os = exp2i(ev - KP);
+      uint32_t v[64];  // O columns h*64 .. h*64+63 of row r
+      tmem_ld_32x32b_x32(tmem + lane_off + TM_O + h * 64u, v);
+      tmem_ld_32x32b_x32(tmem + lane_off + TM_O + h * 64u + 32u, v + 32);
+      tmem_wait_ld();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(O_EMPTY));
+      if (valid) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t v[64];
-        tmem_ld_32x32b_x32(tmem + lane_off + TM_O + h * 64u, v);
-        tmem_ld_32x32b_x32(tmem + lane_off + TM_O + h * 64u + 32u, v + 32);
-        tmem_wait_ld();
-        if (h == 1) {
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(O_EMPTY));
+        for (int c = 0; c < 8; ++c) {
+          const int u = 8 * c;
+          orow[c] = make_uint4(
+              pack_bf162(__uint_as_float(v[u]) * os, __uint_as_float(v[u + 1]) * os),
+              pack_bf162(__uint_as_float(v[u + 2]) * os, __uint_as_float(v[u + 3]) * os),
+              pack_bf162(__uint_as_float(v[u + 4]) * os, __uint_as_float(v[u + 5]) * os),
+              pack_bf162(__uint_as_float(v[u + 6]) * os, __uint_as_float(v[u + 7]) * os));
         }
-        if (valid) {
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const int u = 8 * c;
-            orow[h * 8 + c] = make_uint4(
-                pack_bf162(__uint_as_float(v[u]) * os, __uint_as_float(v[u + 1]) * os),
-                pack_bf162(__uint_as_float(v[u + 2]) * os, __uint_as_float(v[u + 3]) * os),
-                pack_bf162(__uint_as_float(v[u + 4]) * os, __uint_as_float(v[u + 5]) * os),
-                pack_bf162(__uint_as_float(v[u + 6]) * os, __uint_as_float(v[u + 7]) * os));
-          }
-        }
+        if (h == 0) p.lse[grow] = lse;
       }
-      if (valid) p.lse[grow] = lse;
       ++itc;
     }
   }
@@ -426,7 +483,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  if (warp == 4) tmem_dealloc(tmem, 256);
+  if (warp == TMA_WARP) tmem_dealloc(tmem, 256);
 }
 
 }  // namespace
