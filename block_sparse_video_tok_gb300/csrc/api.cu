@@ -230,7 +230,7 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
 
   cudaError_t e = record(events ? events->start : nullptr, s);
   if (e != cudaSuccess) return cuda_fail(e);
-  if ((e = cudaMemsetAsync(workspace, 0, L.delta, s)) != cudaSuccess)  // header and maxima
+  if ((e = cudaMemsetAsync(workspace, 0, L.delta, s)) != cudaSuccess)  // header, counter, maxima
     return cuda_fail(e);
   if ((e = vsa::launch_absmax_delta(qb, kb, vb, dob, ob, BH, S, absmax, delta, dqacc, s)) !=
       cudaSuccess)
@@ -260,6 +260,7 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
   a.dk = static_cast<__nv_bfloat16*>(dk);
   a.dv = static_cast<__nv_bfloat16*>(dv);
   a.err = err;
+  a.sched = ws_at<int32_t>(workspace, L.sched);
   a.B = shape.batch;
   a.H = shape.heads;
   a.S = S;

@@ -80,11 +80,17 @@ enum Bar : uint32_t {
   ACC_FULL,
   ACC_EMPTY,
   DRAIN,
-  NUM_BARS
+  ITEM_FULL0,                  // 4 slots of the work-item queue
+  ITEM_EMPTY0 = ITEM_FULL0 + 4,
+  NUM_BARS = ITEM_EMPTY0 + 4
 };
+constexpr int ITEM_SLOTS = 4;
+// Every role takes every item from the queue: the UMMA thread, 8 softmax warps, 4 drain warps.
+constexpr uint32_t ITEM_CONSUMERS = 1 + SOFTMAX_WARPS + 4;
 constexpr uint32_t SM_TMEM_SLOT = SM_BAR + NUM_BARS * 8;
 constexpr uint32_t SM_ABORT = SM_TMEM_SLOT + 4;
-constexpr uint32_t SM_USED = SM_ABORT + 4;
+constexpr uint32_t SM_QUEUE = SM_ABORT + 4;  // int[ITEM_SLOTS]: work-item ids
+constexpr uint32_t SM_USED = SM_QUEUE + 4 * ITEM_SLOTS;
 constexpr uint32_t SMEM_BYTES = SM_USED + 1024;  // + alignment slack
 
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -107,6 +113,7 @@ struct Params {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   uint32_t* err;
+  int32_t* sched;  // work counter, zero at launch
   int S, nb, max_q, total;
   float sm_scale;
 };
@@ -147,6 +154,28 @@ __device__ __forceinline__ void raise_abort(volatile int* abort, uint32_t* err) 
   atomicOr(err, VSA_DEVERR_TIMEOUT);
 }
 
+// The k-th work item of this CTA, as the producer published it in queue slot k % ITEM_SLOTS;
+// the slot is handed back at once.  One thread calls this; false on abort or timeout.
+__device__ __forceinline__ bool take_item(uint32_t bar_base, volatile int* queue, uint32_t k,
+                                          volatile int* abort, int* w) {
+  const uint32_t slot = k % ITEM_SLOTS;
+  if (!mbar_wait_bounded(bar_base + 8u * (ITEM_FULL0 + slot), (k / ITEM_SLOTS) & 1u, abort,
+                         WAIT_LIMIT_NS))
+    return false;
+  *w = queue[slot];
+  mbar_arrive(bar_base + 8u * (ITEM_EMPTY0 + slot));
+  return true;
+}
+
+// take_item for a whole warp: lane 0 takes the item and broadcasts it.
+__device__ __forceinline__ bool warp_take_item(uint32_t bar_base, volatile int* queue, uint32_t k,
+                                               volatile int* abort, int lane, int* w) {
+  int ok = 1, v = 0;
+  if (lane == 0) ok = take_item(bar_base, queue, k, abort, &v) ? 1 : 0;
+  *w = __shfl_sync(0xffffffffu, v, 0);
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -168,6 +197,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   volatile int* abort = reinterpret_cast<volatile int*>(gbase + SM_ABORT);
+  volatile int* queue = reinterpret_cast<volatile int*>(gbase + SM_QUEUE);
   const uint32_t* tmem_slot = reinterpret_cast<const uint32_t*>(gbase + SM_TMEM_SLOT);
   auto bar = [&](uint32_t b) { return base + SM_BAR + 8u * b; };
 
@@ -190,6 +220,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(bar(ACC_FULL), 1);
     mbar_init(bar(ACC_EMPTY), 4);
     mbar_init(bar(DRAIN), 1);
+    for (int s = 0; s < ITEM_SLOTS; ++s) {
+      mbar_init(bar(ITEM_FULL0 + s), 1);
+      mbar_init(bar(ITEM_EMPTY0 + s), ITEM_CONSUMERS);
+    }
     fence_barrier_init();
   }
   if (warp == TMA_WARP) {
@@ -216,7 +250,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t kv_loads = 0;
       int64_t last_g[2] = {-1, -1};
       bool ok = true;
-      for (int w = blockIdx.x; w < p.total && ok; w += gridDim.x) {
+      // Items are handed out dynamically: the next one is claimed from the global counter once
+      // the loads of the current one are issued, so the CTAs that finish early take more.
+      for (uint32_t k = 0;; ++k) {
+        const uint32_t slot = k % ITEM_SLOTS;
+        if (!mbar_wait_bounded(bar(ITEM_EMPTY0 + slot), ((k / ITEM_SLOTS) & 1u) ^ 1u, abort,
+                               WAIT_LIMIT_NS)) {
+          ok = false;
+          break;
+        }
+        const int w = atomicAdd(p.sched, 1);
+        queue[slot] = w;
+        mbar_arrive(bar(ITEM_FULL0 + slot));  // w >= total is the end marker
+        if (w >= p.total) break;
         const Item it = decode_item(p, w);
         const int raw_n = p.k2q_num[p.order ? p.order[w] : w];
         uint32_t bad = 0;
@@ -263,6 +309,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tma_load_2d(ds + 24576, &tm_do, bar(QDO_FULL0 + s), 64, r1);
           last_g[s] = g;
         }
+        if (!ok) break;
         ++itc;
       }
       if (!ok) {
@@ -357,7 +404,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           umma_f16_c<true>(t_dk, sdesc_advance(qa, kk * 2048u), sdesc_advance(dsb, kk * 2048u),
                            IDESC_DVK);
       };
-      for (int w = blockIdx.x; w < p.total && ok; w += gridDim.x) {
+      for (uint32_t k = 0;; ++k) {
+        int w;
+        if (!take_item(bar(0), queue, k, abort, &w)) {
+          ok = false;
+          break;
+        }
+        if (w >= p.total) break;
         const Item it = decode_item(p, w);
         if (it.n == 0) continue;
         const int np = (it.n + 1) >> 1;
@@ -417,7 +470,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     uint32_t g = 0;
     const uint32_t sw = static_cast<uint32_t>(r & 7);
-    for (int w = blockIdx.x; w < p.total; w += gridDim.x) {
+    for (uint32_t k = 0;; ++k) {
+      int w;
+      if (!warp_take_item(bar(0), queue, k, abort, lane, &w)) {
+        if (lane == 0) raise_abort(abort, p.err);
+        break;
+      }
+      if (w >= p.total) break;
       const Item it = decode_item(p, w);
       if (it.n == 0) continue;
       const int vb = clamp_vbs(p.vbs[it.j]);
@@ -508,7 +567,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t stg = base + SM_STG + static_cast<uint32_t>(wq) * 4096u;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     uint32_t g = 0, itc = 0;
-    for (int w = blockIdx.x; w < p.total; w += gridDim.x) {
+    for (uint32_t k = 0;; ++k) {
+      int w;
+      if (!warp_take_item(bar(0), queue, k, abort, lane, &w)) {
+        if (lane == 0) raise_abort(abort, p.err);
+        break;
+      }
+      if (w >= p.total) break;
       const Item it = decode_item(p, w);
       const size_t row_kv = static_cast<size_t>(it.bh) * S + static_cast<size_t>(it.j) * BLOCK;
       __nv_bfloat16* dk_out = p.dk + row_kv * HEAD_DIM + d;
@@ -692,6 +757,7 @@ cudaError_t launch_bwd_main(const BwdMainArgs& a, cudaStream_t stream) {
   p.dk = a.dk;
   p.dv = a.dv;
   p.err = a.err;
+  p.sched = a.sched;
   p.S = a.S;
   p.nb = a.nb;
   p.max_q = a.max_q;

@@ -29,7 +29,7 @@ constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;   // in-flight copies after an
 // dO), then 1024-byte aligned arrays.
 
 struct BwdLayout {
-  size_t err, absmax, delta, order, dqacc, q16, k16, v16, do16, total;
+  size_t err, sched, absmax, delta, order, dqacc, q16, k16, v16, do16, total;
 };
 struct FwdLayout {
   size_t err, absmax, bitmap, q16, k16, v16, total;
@@ -42,6 +42,7 @@ inline BwdLayout bwd_layout(long B, long H, long S) {
   const size_t bh = static_cast<size_t>(B) * H, rows = bh * S, nb = S / BLOCK;
   size_t off = 0;
   L.err = off;
+  L.sched = 128;  // work counter of the main kernel's dynamic scheduler (inside the header)
   off += 256;
   L.absmax = off;
   off = align_up(off + bh * 4 * sizeof(uint32_t), 1024);
@@ -148,6 +149,7 @@ struct BwdMainArgs {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   uint32_t* err;
+  int32_t* sched;  // zeroed work counter
   int B, H, S, nb, max_q;
   float sm_scale;
 };
