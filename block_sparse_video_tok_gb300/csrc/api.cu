@@ -173,6 +173,7 @@ vsa_status vsa_fwd(const void* q, const void* k, const void* v, const int32_t* q
   a.o = static_cast<__nv_bfloat16*>(o);
   a.lse = lse;
   a.err = err;
+  a.sched = ws_at<int32_t>(workspace, L.sched);
   a.B = shape.batch;
   a.H = shape.heads;
   a.S = S;

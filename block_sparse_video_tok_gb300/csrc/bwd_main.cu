@@ -40,6 +40,7 @@
 #include <cudaTypedefs.h>
 
 #include "ptx.cuh"
+#include "queue.cuh"
 #include "vsa_internal.cuh"
 
 namespace vsa {
@@ -80,11 +81,10 @@ enum Bar : uint32_t {
   ACC_FULL,
   ACC_EMPTY,
   DRAIN,
-  ITEM_FULL0,                  // 4 slots of the work-item queue
-  ITEM_EMPTY0 = ITEM_FULL0 + 4,
-  NUM_BARS = ITEM_EMPTY0 + 4
+  ITEM_FULL0,  // the work-item queue (queue.cuh)
+  ITEM_EMPTY0 = ITEM_FULL0 + ITEM_SLOTS,
+  NUM_BARS = ITEM_EMPTY0 + ITEM_SLOTS
 };
-constexpr int ITEM_SLOTS = 4;
 // Every role takes every item from the queue: the UMMA thread, 8 softmax warps, 4 drain warps.
 constexpr uint32_t ITEM_CONSUMERS = 1 + SOFTMAX_WARPS + 4;
 constexpr uint32_t SM_TMEM_SLOT = SM_BAR + NUM_BARS * 8;
@@ -152,28 +152,6 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 __device__ __forceinline__ void raise_abort(volatile int* abort, uint32_t* err) {
   *abort = 1;
   atomicOr(err, VSA_DEVERR_TIMEOUT);
-}
-
-// The k-th work item of this CTA, as the producer published it in queue slot k % ITEM_SLOTS;
-// the slot is handed back at once.  One thread calls this; false on abort or timeout.
-__device__ __forceinline__ bool take_item(uint32_t bar_base, volatile int* queue, uint32_t k,
-                                          volatile int* abort, int* w) {
-  const uint32_t slot = k % ITEM_SLOTS;
-  if (!mbar_wait_bounded(bar_base + 8u * (ITEM_FULL0 + slot), (k / ITEM_SLOTS) & 1u, abort,
-                         WAIT_LIMIT_NS))
-    return false;
-  *w = queue[slot];
-  mbar_arrive(bar_base + 8u * (ITEM_EMPTY0 + slot));
-  return true;
-}
-
-// take_item for a whole warp: lane 0 takes the item and broadcasts it.
-__device__ __forceinline__ bool warp_take_item(uint32_t bar_base, volatile int* queue, uint32_t k,
-                                               volatile int* abort, int lane, int* w) {
-  int ok = 1, v = 0;
-  if (lane == 0) ok = take_item(bar_base, queue, k, abort, &v) ? 1 : 0;
-  *w = __shfl_sync(0xffffffffu, v, 0);
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
@@ -253,16 +231,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // Items are handed out dynamically: the next one is claimed from the global counter once
       // the loads of the current one are issued, so the CTAs that finish early take more.
       for (uint32_t k = 0;; ++k) {
-        const uint32_t slot = k % ITEM_SLOTS;
-        if (!mbar_wait_bounded(bar(ITEM_EMPTY0 + slot), ((k / ITEM_SLOTS) & 1u) ^ 1u, abort,
-                               WAIT_LIMIT_NS)) {
+        int w;
+        if (!publish_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, p.sched, abort, &w)) {
           ok = false;
           break;
         }
-        const int w = atomicAdd(p.sched, 1);
-        queue[slot] = w;
-        mbar_arrive(bar(ITEM_FULL0 + slot));  // w >= total is the end marker
-        if (w >= p.total) break;
+        if (w >= p.total) break;  // the end marker
         const Item it = decode_item(p, w);
         const int raw_n = p.k2q_num[p.order ? p.order[w] : w];
         uint32_t bad = 0;
@@ -406,7 +380,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       };
       for (uint32_t k = 0;; ++k) {
         int w;
-        if (!take_item(bar(0), queue, k, abort, &w)) {
+        if (!take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, &w)) {
           ok = false;
           break;
         }
@@ -472,7 +446,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t sw = static_cast<uint32_t>(r & 7);
     for (uint32_t k = 0;; ++k) {
       int w;
-      if (!warp_take_item(bar(0), queue, k, abort, lane, &w)) {
+      if (!warp_take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, lane, &w)) {
         if (lane == 0) raise_abort(abort, p.err);
         break;
       }
@@ -569,7 +543,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t g = 0, itc = 0;
     for (uint32_t k = 0;; ++k) {
       int w;
-      if (!warp_take_item(bar(0), queue, k, abort, lane, &w)) {
+      if (!warp_take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, lane, &w)) {
         if (lane == 0) raise_abort(abort, p.err);
         break;
       }

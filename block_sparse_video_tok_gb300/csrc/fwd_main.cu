@@ -6,19 +6,24 @@
 // Work unit: one (b, h, q pair) item -- q blocks 2x and 2x+1 -- so the UMMA M dimension is 128
 // and row m of every accumulator is TMEM lane m.  The item walks the UNION of the two q blocks'
 // selected kv blocks (ascending); for each row, kv blocks its own q block did not select are
-// masked.  Two passes over the union:
-//   pass 1  S = Q_p K_j^T, per-row running max / sum of exp2 (statistics only),
-//   pass 2  S again, P = exp2(S*c - lse) (exactly normalised, fp16 * 2^KP) -> shared memory,
-//           O += P V_j   (A = P K-major, B = V_j MN-major; fp32 accumulator in TMEM).
-// No rescaling of O is needed, at the price of recomputing S once.
+// masked.  One pass with an online softmax per kv block j:
+//   S = Q_p K_j^T (both operands in shared memory, fp32 accumulator in TMEM);
+//   the row maximum of the block; if it exceeds the row's reference maximum m by more than
+//   RESCALE (log2 units), m moves up to it and the O row and the running sum are scaled by
+//   2^(m_old - m_new) first (otherwise m stays, so P stays below 2^(RESCALE + KPF));
+//   P = 2^(s - m + KPF) in fp16, written to TMEM, where it is the A operand of
+//   O += P V_j (B = V_j from shared memory, MN-major).
+// At the end O / l and lse = m + log2(l).  P never passes through shared memory, so per kv block
+// the tensor pipe reads Q_p, K_j and V_j only.
 //
 // Roles (320 threads): warps 0-7 softmax -- warps w and w+4 share TMEM lane quarter w (query
-// rows 32w..32w+31) and split the 64 kv columns of S (and the 128 columns of O) in halves, merging
-// their pass-1 row statistics through shared memory; warp 8 TMA producer and TMEM owner; warp 9
-// UMMA issuer, which in pass 2 issues S of the next kv block before waiting for P of the current
-// one, so the softmax and the tensor pipe overlap.  TMEM (256 columns): S x2 [0,128),
-// O [128,256).
+// rows 32w..32w+31) and split the 64 kv columns of S (and the 128 columns of O) in halves,
+// exchanging their block maxima through shared memory; warp 8 TMA producer, TMEM owner and work
+// claimer; warp 9 UMMA issuer, which issues S of the next kv block before P.V of the current one
+// so the softmax of one block overlaps the tensor work of its neighbours.
+// TMEM (512 columns allocated): O [0,128), S x2 [128,256), P x2 [256,320).
 #include "ptx.cuh"
+#include "queue.cuh"
 #include "vsa_internal.cuh"
 
 namespace vsa {
@@ -30,34 +35,40 @@ constexpr int SOFTMAX_WARPS = 8;
 constexpr int TMA_WARP = 8;
 constexpr int MMA_WARP = 9;
 constexpr int KV_STAGES = 4;
+constexpr int KPF = 7;               // P is carried as P * 2^KPF: below 2^(RESCALE + KPF) = 2^15
+constexpr float RESCALE = 8.0f;      // log2 units the block maximum may exceed m by before a rescale
 
-constexpr uint32_t SM_Q = 0;                                // 2 chunks x [128 q x 128 B]
-constexpr uint32_t SM_KV = 32768;                           // stages x (K 16 KB, V 16 KB)
-constexpr uint32_t SM_P = SM_KV + KV_STAGES * 32768;        // 2 x [128 q x 128 B]
-constexpr uint32_t SM_STAT = SM_P + 2 * 16384;              // [2 halves][128 rows] (max, sum)
-constexpr uint32_t SM_BAR = SM_STAT + 2 * 128 * 8;
+constexpr uint32_t SM_Q = 0;                          // 2 stages x 2 chunks x [128 q x 128 B]
+constexpr uint32_t SM_KV = 2 * 32768;                 // stages x (K 16 KB, V 16 KB)
+constexpr uint32_t SM_XCH = SM_KV + KV_STAGES * 32768;  // [2 parity][2 halves][128 rows] float
+constexpr uint32_t SM_BAR = SM_XCH + 2 * 2 * 128 * 4;
 
 enum Bar : uint32_t {
-  Q_FULL = 0,
-  Q_EMPTY,
-  KV_FULL0,
+  Q_FULL0 = 0,
+  Q_EMPTY0 = Q_FULL0 + 2,
+  KV_FULL0 = Q_EMPTY0 + 2,
   KV_EMPTY0 = KV_FULL0 + KV_STAGES,
   S_FULL0 = KV_EMPTY0 + KV_STAGES,
   S_FREE0 = S_FULL0 + 2,
   P_READY0 = S_FREE0 + 2,
   P_FREE0 = P_READY0 + 2,
-  O_FULL = P_FREE0 + 2,
+  PV_DONE = P_FREE0 + 2,  // one phase per P.V, for the rescale of O
+  O_FULL,
   O_EMPTY,
   DRAIN,
-  STAT0,  // one per lane quarter: the two column-half warps have published their statistics
-  NUM_BARS = STAT0 + 4
+  XCH0,  // one per lane quarter: both column-half warps have published a value
+  ITEM_FULL0 = XCH0 + 4,
+  ITEM_EMPTY0 = ITEM_FULL0 + ITEM_SLOTS,
+  NUM_BARS = ITEM_EMPTY0 + ITEM_SLOTS
 };
+constexpr uint32_t ITEM_CONSUMERS = 1 + SOFTMAX_WARPS;  // the UMMA thread and the softmax warps
 constexpr uint32_t SM_TMEM_SLOT = SM_BAR + NUM_BARS * 8;
 constexpr uint32_t SM_ABORT = SM_TMEM_SLOT + 4;
-constexpr uint32_t SMEM_BYTES = SM_ABORT + 4 + 1024;
+constexpr uint32_t SM_QUEUE = SM_ABORT + 4;
+constexpr uint32_t SMEM_BYTES = SM_QUEUE + 4 * ITEM_SLOTS + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-constexpr uint32_t TM_S = 0, TM_O = 128;
+constexpr uint32_t TM_O = 0, TM_S = 128, TM_P = 256;
 constexpr uint32_t IDESC_S = idesc_f16_f32acc(128, 64, false, false);
 constexpr uint32_t IDESC_PV = idesc_f16_f32acc(128, 128, false, true);
 
@@ -68,6 +79,7 @@ struct Params {
   __nv_bfloat16* o;
   float* lse;
   uint32_t* err;
+  int32_t* sched;
   int S, nb, words, npairs, total;
   float sm_scale;
 };
@@ -151,6 +163,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   volatile int* abort = reinterpret_cast<volatile int*>(gbase + SM_ABORT);
+  volatile int* queue = reinterpret_cast<volatile int*>(gbase + SM_QUEUE);
   const uint32_t* tmem_slot = reinterpret_cast<const uint32_t*>(gbase + SM_TMEM_SLOT);
   auto bar = [&](uint32_t b) { return base + SM_BAR + 8u * b; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -158,27 +171,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     *abort = 0;
-    mbar_init(bar(Q_FULL), 1);
-    mbar_init(bar(Q_EMPTY), 1);
-    for (int s = 0; s < KV_STAGES; ++s) {
-      mbar_init(bar(KV_FULL0 + s), 1);
-      mbar_init(bar(KV_EMPTY0 + s), 1);
-    }
     for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(Q_FULL0 + s), 1);
+      mbar_init(bar(Q_EMPTY0 + s), 1);
       mbar_init(bar(S_FULL0 + s), 1);
       mbar_init(bar(S_FREE0 + s), SOFTMAX_WARPS);
       mbar_init(bar(P_READY0 + s), SOFTMAX_WARPS);
       mbar_init(bar(P_FREE0 + s), 1);
     }
+    for (int s = 0; s < KV_STAGES; ++s) {
+      mbar_init(bar(KV_FULL0 + s), 1);
+      mbar_init(bar(KV_EMPTY0 + s), 1);
+    }
+    mbar_init(bar(PV_DONE), 1);
     mbar_init(bar(O_FULL), 1);
     mbar_init(bar(O_EMPTY), SOFTMAX_WARPS);
     mbar_init(bar(DRAIN), 1);
-    for (int qq = 0; qq < 4; ++qq) mbar_init(bar(STAT0 + qq), 2);
+    for (int qq = 0; qq < 4; ++qq) mbar_init(bar(XCH0 + qq), 2);
+    for (int s = 0; s < ITEM_SLOTS; ++s) {
+      mbar_init(bar(ITEM_FULL0 + s), 1);
+      mbar_init(bar(ITEM_EMPTY0 + s), ITEM_CONSUMERS);
+    }
     fence_barrier_init();
   }
   if (warp == TMA_WARP) {
-    tmem_alloc(base + SM_TMEM_SLOT, 256);
+    tmem_alloc(base + SM_TMEM_SLOT, 512);
     tmem_relinquish();
+  }
+  if (warp == TMA_WARP && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -188,51 +211,61 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == TMA_WARP) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      uint32_t lg = 0, itc = 0, q_loads = 0;
-      int64_t last_lg[KV_STAGES];
+      uint32_t lg = 0, itc = 0;  // kv blocks loaded; items with a non-empty union
+      int64_t last_lg[KV_STAGES], last_q[2] = {-1, -1};
       for (int s = 0; s < KV_STAGES; ++s) last_lg[s] = -1;
       bool ok = true;
-      for (int w = blockIdx.x; w < p.total && ok; w += gridDim.x) {
+      for (uint32_t k = 0;; ++k) {
+        int w;
+        if (!publish_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, p.sched, abort, &w)) {
+          ok = false;
+          break;
+        }
+        if (w >= p.total) break;  // the end marker
         const Pair q = decode_pair(p, w);
         if (union_size(p, q) == 0) continue;
-        if (!mbar_wait_bounded(bar(Q_EMPTY), (itc & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) {
+        const uint32_t qs = itc & 1u;
+        if (!mbar_wait_bounded(bar(Q_EMPTY0 + qs), ((itc >> 1) & 1u) ^ 1u, abort,
+                               WAIT_LIMIT_NS)) {
           ok = false;
           break;
         }
         const int r0 = q.bh * S + q.i0 * BLOCK;
         const int r1 = q.bh * S + (q.i1 >= 0 ? q.i1 : q.i0) * BLOCK;
-        mbar_arrive_expect_tx(bar(Q_FULL), 32768);
-        tma_load_2d(base + SM_Q, &tm_q, bar(Q_FULL), 0, r0);
-        tma_load_2d(base + SM_Q + 8192, &tm_q, bar(Q_FULL), 0, r1);
-        tma_load_2d(base + SM_Q + 16384, &tm_q, bar(Q_FULL), 64, r0);
-        tma_load_2d(base + SM_Q + 24576, &tm_q, bar(Q_FULL), 64, r1);
-        ++q_loads;
-        for (int pass = 0; pass < 2 && ok; ++pass) {
-          ok = for_union(p, q, [&](int j) {
-            const uint32_t st = lg % KV_STAGES;
-            if (!mbar_wait_bounded(bar(KV_EMPTY0 + st), ((lg / KV_STAGES) & 1u) ^ 1u, abort,
-                                   WAIT_LIMIT_NS))
-              return false;
-            const int rk = q.bh * S + j * BLOCK;
-            const uint32_t kd = base + SM_KV + st * 32768u;
-            mbar_arrive_expect_tx(bar(KV_FULL0 + st), pass ? 32768u : 16384u);
-            tma_load_2d(kd, &tm_k, bar(KV_FULL0 + st), 0, rk);
-            tma_load_2d(kd + 8192, &tm_k, bar(KV_FULL0 + st), 64, rk);
-            if (pass) {
-              tma_load_2d(kd + 16384, &tm_v, bar(KV_FULL0 + st), 0, rk);
-              tma_load_2d(kd + 24576, &tm_v, bar(KV_FULL0 + st), 64, rk);
-            }
-            last_lg[st] = lg;
-            ++lg;
-            return true;
-          });
-        }
+        const uint32_t qd = base + SM_Q + qs * 32768u;
+        mbar_arrive_expect_tx(bar(Q_FULL0 + qs), 32768);
+        tma_load_2d(qd, &tm_q, bar(Q_FULL0 + qs), 0, r0);
+        tma_load_2d(qd + 8192, &tm_q, bar(Q_FULL0 + qs), 0, r1);
+        tma_load_2d(qd + 16384, &tm_q, bar(Q_FULL0 + qs), 64, r0);
+        tma_load_2d(qd + 24576, &tm_q, bar(Q_FULL0 + qs), 64, r1);
+        last_q[qs] = itc;
+        ok = for_union(p, q, [&](int j) {
+          const uint32_t st = lg % KV_STAGES;
+          if (!mbar_wait_bounded(bar(KV_EMPTY0 + st), ((lg / KV_STAGES) & 1u) ^ 1u, abort,
+                                 WAIT_LIMIT_NS))
+            return false;
+          const int rk = q.bh * S + j * BLOCK;
+          const uint32_t kd = base + SM_KV + st * 32768u;
+          mbar_arrive_expect_tx(bar(KV_FULL0 + st), 32768u);
+          tma_load_2d(kd, &tm_k, bar(KV_FULL0 + st), 0, rk);
+          tma_load_2d(kd + 8192, &tm_k, bar(KV_FULL0 + st), 64, rk);
+          tma_load_2d(kd + 16384, &tm_v, bar(KV_FULL0 + st), 0, rk);
+          tma_load_2d(kd + 24576, &tm_v, bar(KV_FULL0 + st), 64, rk);
+          last_lg[st] = lg;
+          ++lg;
+          return true;
+        });
+        if (!ok) break;
         ++itc;
       }
       if (!ok) {
         raise_abort(abort, p.err);
+        // Let the copies already issued land before the CTA's shared memory goes away.
         volatile int never = 0;
-        if (q_loads) mbar_wait_bounded(bar(Q_FULL), (q_loads - 1) & 1u, &never, DRAIN_LIMIT_NS);
+        for (int s = 0; s < 2; ++s)
+          if (last_q[s] >= 0)
+            mbar_wait_bounded(bar(Q_FULL0 + s), (static_cast<uint32_t>(last_q[s]) >> 1) & 1u,
+                              &never, DRAIN_LIMIT_NS);
         for (int s = 0; s < KV_STAGES; ++s)
           if (last_lg[s] >= 0)
             mbar_wait_bounded(bar(KV_FULL0 + s),
@@ -244,103 +277,97 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------------ UMMA issuer
     if (lane == 0) {
-      uint32_t lg = 0, sg = 0, pg = 0, itc = 0;
+      uint32_t t = 0, itc = 0;  // kv blocks issued (one S and one P.V each); items
       bool ok = true, issued = false;
       const uint64_t q_kmaj = sdesc_sw128(base + SM_Q, 16, 1024);
-      const uint64_t kv_kmaj = sdesc_sw128(base + SM_KV, 16, 1024);    // K of stage 0
-      const uint64_t kv_mn = sdesc_sw128(base + SM_KV + 16384u, 8192, 1024);  // V of stage 0
-      const uint64_t p_kmaj = sdesc_sw128(base + SM_P, 16, 1024);
-      // S = Q_p K_j^T into S buffer sg & 1, K from KV stage lg % KV_STAGES.
-      auto issue_s = [&]() -> bool {
-        const uint32_t st = lg % KV_STAGES, sb = sg & 1u;
-        if (!mbar_wait_bounded(bar(KV_FULL0 + st), (lg / KV_STAGES) & 1u, abort, WAIT_LIMIT_NS))
+      const uint64_t k_kmaj = sdesc_sw128(base + SM_KV, 16, 1024);           // K of stage 0
+      const uint64_t v_mn = sdesc_sw128(base + SM_KV + 16384u, 8192, 1024);  // V of stage 0
+      // S = Q_p K_j^T of kv block tb into S buffer tb & 1; Q from stage qs.
+      auto issue_s = [&](uint32_t tb, uint32_t qs) -> bool {
+        const uint32_t st = tb % KV_STAGES, sb = tb & 1u;
+        if (!mbar_wait_bounded(bar(KV_FULL0 + st), (tb / KV_STAGES) & 1u, abort, WAIT_LIMIT_NS))
           return false;
-        if (!mbar_wait_bounded(bar(S_FREE0 + sb), ((sg >> 1) & 1u) ^ 1u, abort, WAIT_LIMIT_NS))
+        if (!mbar_wait_bounded(bar(S_FREE0 + sb), ((tb >> 1) & 1u) ^ 1u, abort, WAIT_LIMIT_NS))
           return false;
         tc_fence_after_sync();
-        const uint64_t kd = sdesc_advance(kv_kmaj, st * 32768u);
+        const uint64_t qa = sdesc_advance(q_kmaj, qs * 32768u);
+        const uint64_t kd = sdesc_advance(k_kmaj, st * 32768u);
         const uint32_t ts = tmem + TM_S + sb * 64u;
-        umma_f16_c<false>(ts, q_kmaj, kd, IDESC_S);
+        umma_f16_c<false>(ts, qa, kd, IDESC_S);
 #pragma unroll
         for (int kk = 1; kk < 8; ++kk) {
           const uint32_t off = (kk & 3) * 32u;
-          umma_f16_c<true>(ts, sdesc_advance(q_kmaj, (kk >> 2) * 16384u + off),
+          umma_f16_c<true>(ts, sdesc_advance(qa, (kk >> 2) * 16384u + off),
                            sdesc_advance(kd, (kk >> 2) * 8192u + off), IDESC_S);
         }
         umma_commit(bar(S_FULL0 + sb));
         issued = true;
-        ++sg;
         return true;
       };
-      // O += P V_j with P buffer pg & 1 and V of KV stage `st`.
-      auto issue_pv = [&](uint32_t st, bool first) -> bool {
-        const uint32_t pb = pg & 1u;
-        if (!mbar_wait_bounded(bar(P_READY0 + pb), (pg >> 1) & 1u, abort, WAIT_LIMIT_NS))
+      // O += P V_j of kv block tb: A = P buffer tb & 1 in TMEM (8 columns per 16 kv), B = V_j.
+      auto issue_pv = [&](uint32_t tb, bool first) -> bool {
+        const uint32_t pb = tb & 1u, st = tb % KV_STAGES;
+        if (!mbar_wait_bounded(bar(P_READY0 + pb), (tb >> 1) & 1u, abort, WAIT_LIMIT_NS))
           return false;
         if (first && !mbar_wait_bounded(bar(O_EMPTY), (itc & 1u) ^ 1u, abort, WAIT_LIMIT_NS))
           return false;
         tc_fence_after_sync();
-        const uint64_t pa = sdesc_advance(p_kmaj, pb * 16384u);
-        const uint64_t vb = sdesc_advance(kv_mn, st * 32768u);
+        const uint32_t pa = tmem + TM_P + pb * 32u;
+        const uint64_t vb = sdesc_advance(v_mn, st * 32768u);
         if (first)
-          umma_f16_c<false>(tmem + TM_O, pa, vb, IDESC_PV);
+          umma_f16_ta<false>(tmem + TM_O, pa, vb, IDESC_PV);
         else
-          umma_f16_c<true>(tmem + TM_O, pa, vb, IDESC_PV);
+          umma_f16_ta<true>(tmem + TM_O, pa, vb, IDESC_PV);
 #pragma unroll
         for (int kk = 1; kk < 4; ++kk)
-          umma_f16_c<true>(tmem + TM_O, sdesc_advance(pa, kk * 32u), sdesc_advance(vb, kk * 2048u),
-                           IDESC_PV);
+          umma_f16_ta<true>(tmem + TM_O, pa + kk * 8u, sdesc_advance(vb, kk * 2048u), IDESC_PV);
         umma_commit(bar(P_FREE0 + pb));
         umma_commit(bar(KV_EMPTY0 + st));
-        ++pg;
+        umma_commit(bar(PV_DONE));
         return true;
       };
-      for (int w = blockIdx.x; w < p.total && ok; w += gridDim.x) {
+      for (uint32_t k = 0;; ++k) {
+        int w;
+        if (!take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, &w)) {
+          ok = false;
+          break;
+        }
+        if (w >= p.total) break;
         const Pair q = decode_pair(p, w);
         const int nu = union_size(p, q);
         if (nu == 0) continue;
-        if (!mbar_wait_bounded(bar(Q_FULL), itc & 1u, abort, WAIT_LIMIT_NS)) {
+        const uint32_t qs = itc & 1u;
+        if (!mbar_wait_bounded(bar(Q_FULL0 + qs), (itc >> 1) & 1u, abort, WAIT_LIMIT_NS)) {
           ok = false;
           break;
         }
-        // Pass 1: S of every union block; K stages are released as soon as S is done.
-        for (int e = 0; e < nu && ok; ++e) {
-          const uint32_t st = lg % KV_STAGES;
-          if (!issue_s()) {
-            ok = false;
-            break;
-          }
-          umma_commit(bar(KV_EMPTY0 + st));
-          ++lg;
-        }
-        if (!ok) break;
-        // Pass 2: S(e+1) is issued before P.V(e) waits for the softmax of block e.
-        const uint32_t lg0 = lg;
-        if (!issue_s()) {
+        const uint32_t t0 = t;
+        if (!issue_s(t0, qs)) {
           ok = false;
           break;
         }
-        for (int e = 0; e < nu && ok; ++e) {
+        for (int e = 0; e < nu; ++e) {
           if (e + 1 < nu) {
-            lg = lg0 + e + 1;
-            if (!issue_s()) {
+            if (!issue_s(t0 + e + 1, qs)) {
               ok = false;
               break;
             }
+          } else {
+            umma_commit(bar(Q_EMPTY0 + qs));  // every S of the item has been issued
           }
-          if (!issue_pv((lg0 + e) % KV_STAGES, e == 0)) {
+          if (!issue_pv(t0 + e, e == 0)) {
             ok = false;
             break;
           }
         }
         if (!ok) break;
-        lg = lg0 + nu;
         umma_commit(bar(O_FULL));
-        umma_commit(bar(Q_EMPTY));
+        t = t0 + nu;
         ++itc;
       }
       if (!ok) raise_abort(abort, p.err);
       if (issued) {
+        // Every UMMA has completed before TMEM is released.
         umma_commit(bar(DRAIN));
         volatile int never = 0;
         mbar_wait_bounded(bar(DRAIN), 0, &never, DRAIN_LIMIT_NS);
@@ -352,10 +379,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int quarter = warp & 3, h = warp >> 2;  // TMEM lane quarter; column half
     const int r = quarter * 32 + lane;            // query row of the pair == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t sw = static_cast<uint32_t>(r & 7);
-    float2* stat = reinterpret_cast<float2*>(gbase + SM_STAT);  // [half][row] (max, sum)
-    uint32_t sg = 0, pg = 0, itc = 0;
-    for (int w = blockIdx.x; w < p.total; w += gridDim.x) {
+    float* xch = reinterpret_cast<float*>(gbase + SM_XCH);
+    uint32_t t = 0, itc = 0, xc = 0;  // kv blocks seen; items with a non-empty union; exchanges
+    // The partner warp's value of this row (the other column half).  Slots alternate with the
+    // exchange count, so a slot is rewritten only after the partner has read it.
+    auto exchange = [&](float x, float* y) -> bool {
+      float* slot = xch + (xc & 1u) * 256u;
+      slot[h * 128 + r] = x;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(XCH0 + quarter));
+      if (!warp_wait(bar(XCH0 + quarter), xc & 1u, abort, lane)) return false;
+      __syncwarp();
+      *y = slot[(1 - h) * 128 + r];
+      ++xc;
+      return true;
+    };
+    for (uint32_t k = 0;; ++k) {
+      int w;
+      if (!warp_take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, lane, &w)) {
+        if (lane == 0) raise_abort(abort, p.err);
+        break;
+      }
+      if (w >= p.total) break;
       const Pair q = decode_pair(p, w);
       const bool valid = (r < 64) || (q.i1 >= 0);
       const uint32_t* own = (r < 64) ? q.bm0 : q.bm1;
@@ -373,90 +418,83 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t* am = p.absmax + q.bh * 4;
       const int eq = operand_exponent(am[0]), ek = operand_exponent(am[1]);
       const int ev = operand_exponent(am[2]);
-      const float c1 = p.sm_scale * LOG2E_F * exp2i(eq + ek);
-      float m = -INFINITY, l = 0.f, lse = -INFINITY;
-      bool ok = true;
-      for (int pass = 0; pass < 2 && ok; ++pass) {
-        ok = for_union(p, q, [&](int j) {
-          const uint32_t sb = sg & 1u;
-          if (!warp_wait(bar(S_FULL0 + sb), (sg >> 1) & 1u, abort, lane)) return false;
-          tc_fence_after_sync();
-          const bool mine = valid && ((own[j >> 5] >> (j & 31)) & 1u);
-          const int vb = mine ? clamp_vbs(p.vbs[j]) - h * 32 : 0;  // visible columns in my half
-          uint32_t sv[32];
-          tmem_ld_32x32b_x32(tmem + lane_off + TM_S + sb * 64u + h * 32u, sv);
-          tmem_wait_ld();
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(S_FREE0 + sb));
-          ++sg;
-          if (pass == 0) {
-            if (vb > 0) {
-              float mloc = -INFINITY;
+      const float c1 = p.sm_scale * LOG2E_F * exp2i(eq + ek);  // S' -> s (log2 units)
+      float m = -INFINITY, l = 0.f;  // reference maximum; this half's sum of P * 2^KPF
+      bool first = true;
+      const bool ok = for_union(p, q, [&](int j) {
+        const uint32_t sb = t & 1u;
+        if (!warp_wait(bar(S_FULL0 + sb), (t >> 1) & 1u, abort, lane)) return false;
+        tc_fence_after_sync();
+        const bool mine = valid && ((own[j >> 5] >> (j & 31)) & 1u);
+        const int vb = mine ? clamp_vbs(p.vbs[j]) - h * 32 : 0;  // visible columns in my half
+        uint32_t sv[32];
+        tmem_ld_32x32b_x32(tmem + lane_off + TM_S + sb * 64u + h * 32u, sv);
+        tmem_wait_ld();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(S_FREE0 + sb));
+        float mloc = -INFINITY;
 #pragma unroll
-              for (int u = 0; u < 32; ++u)
-                if (u < vb) mloc = fmaxf(mloc, __uint_as_float(sv[u]) * c1);
-              const float mn = fmaxf(m, mloc);
-              float acc = 0.f;
+        for (int u = 0; u < 32; ++u)
+          if (u < vb) mloc = fmaxf(mloc, __uint_as_float(sv[u]) * c1);
+        float mo;
+        if (!exchange(mloc, &mo)) return false;
+        const float mb = fmaxf(mloc, mo);  // the row's maximum over this kv block
+        const bool need = mb > m + RESCALE;
+        // P buffer sb is free once P.V of block t-2 has completed; from then on P.V of block
+        // t-1 is the only one that can still be accumulating into O.
+        if (!warp_wait(bar(P_FREE0 + sb), ((t >> 1) & 1u) ^ 1u, abort, lane)) return false;
+        if (__any_sync(0xffffffffu, need)) {
+          const float f = need ? ex2(m - mb) : 1.f;  // m = -inf: f = 0 (nothing accumulated)
+          if (!first) {
+            if (!warp_wait(bar(PV_DONE), (t - 1) & 1u, abort, lane)) return false;
+            tc_fence_after_sync();
+#pragma unroll 1
+            for (int c = 0; c < 2; ++c) {
+              uint32_t ov[32];
+              const uint32_t ta = tmem + lane_off + TM_O + h * 64u + c * 32u;
+              tmem_ld_32x32b_x32(ta, ov);
+              tmem_wait_ld();
 #pragma unroll
-              for (int u = 0; u < 32; ++u)
-                if (u < vb) acc += ex2(__uint_as_float(sv[u]) * c1 - mn);
-              l = l * ex2(m - mn) + acc;
-              m = mn;
+              for (int u = 0; u < 32; ++u) ov[u] = __float_as_uint(__uint_as_float(ov[u]) * f);
+              tmem_st_32x32b_x32(ta, ov);
             }
-            return true;
+            tmem_wait_st();
           }
-          const float off = static_cast<float>(KP) - lse;
-          uint32_t pk[16];
-#pragma unroll
-          for (int u = 0; u < 32; u += 2) {
-            const float p0 = (u < vb) ? ex2(fmaf(__uint_as_float(sv[u]), c1, off)) : 0.f;
-            const float p1 = (u + 1 < vb) ? ex2(fmaf(__uint_as_float(sv[u + 1]), c1, off)) : 0.f;
-            pk[u >> 1] = pack_half2(p0, p1);
-          }
-          const uint32_t pb = pg & 1u;
-          if (!warp_wait(bar(P_FREE0 + pb), ((pg >> 1) & 1u) ^ 1u, abort, lane)) return false;
-          const uint32_t prow = base + SM_P + pb * 16384u + static_cast<uint32_t>(r) * 128u;
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            const uint32_t phys = ((static_cast<uint32_t>(h * 4 + ch)) ^ sw) * 16u;
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + phys),
-                         "r"(pk[4 * ch]), "r"(pk[4 * ch + 1]), "r"(pk[4 * ch + 2]),
-                         "r"(pk[4 * ch + 3])
-                         : "memory");
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(P_READY0 + pb));
-          ++pg;
-          return true;
-        });
-        if (pass == 0 && ok) {
-          // Merge the two column halves' statistics of each row.  The slot is rewritten only in
-          // the next item's pass 1, which cannot start before both warps finished this item.
-          stat[h * 128 + r] = make_float2(m, l);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(STAT0 + quarter));
-          if (!warp_wait(bar(STAT0 + quarter), itc & 1u, abort, lane)) {
-            ok = false;
-            break;
-          }
-          const float2 o2 = stat[(1 - h) * 128 + r];
-          const float mm = fmaxf(m, o2.x);
-          const float ll = (mm == -INFINITY) ? 0.f : l * ex2(m - mm) + o2.y * ex2(o2.x - mm);
-          lse = (ll > 0.f) ? mm + log2f(ll) : -INFINITY;
+          l *= f;
+          if (need) m = mb;
         }
-      }
-      if (!ok) {
+        const float off = static_cast<float>(KPF) - m;
+        uint32_t pk[16];
+        float acc = 0.f;
+#pragma unroll
+        for (int u = 0; u < 32; u += 2) {
+          const float p0 = (u < vb) ? ex2(fmaf(__uint_as_float(sv[u]), c1, off)) : 0.f;
+          const float p1 = (u + 1 < vb) ? ex2(fmaf(__uint_as_float(sv[u + 1]), c1, off)) : 0.f;
+          acc += p0 + p1;
+          pk[u >> 1] = pack_half2(p0, p1);
+        }
+        l += acc;
+        tmem_st_32x32b_x16(tmem + lane_off + TM_P + sb * 32u + h * 16u, pk);
+        tmem_wait_st();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(P_READY0 + sb));
+        ++t;
+        first = false;
+        return true;
+      });
+      float lo = 0.f;
+      if (!ok || !exchange(l, &lo)) {
         if (lane == 0) raise_abort(abort, p.err);
         break;
       }
+      const float lt = l + lo;
       if (!warp_wait(bar(O_FULL), itc & 1u, abort, lane)) {
         if (lane == 0) raise_abort(abort, p.err);
         break;
       }
       tc_fence_after_sync();
-      const float os = exp2i(ev - KP);
       uint32_t v[64];  // O columns h*64 .. h*64+63 of row r
       tmem_ld_32x32b_x32(tmem + lane_off + TM_O + h * 64u, v);
       tmem_ld_32x32b_x32(tmem + lane_off + TM_O + h * 64u + 32u, v + 32);
@@ -465,6 +503,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(O_EMPTY));
       if (valid) {
+        // O = (sum P 2^KPF V') 2^ev / (sum P 2^KPF); an empty row (lt = 0) gives O = 0 and
+        // lse = -inf.
+        const float os = lt > 0.f ? exp2i(ev) / lt : 0.f;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const int u = 8 * c;
@@ -474,7 +515,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               pack_bf162(__uint_as_float(v[u + 4]) * os, __uint_as_float(v[u + 5]) * os),
               pack_bf162(__uint_as_float(v[u + 6]) * os, __uint_as_float(v[u + 7]) * os));
         }
-        if (h == 0) p.lse[grow] = lse;
+        if (h == 0) p.lse[grow] = lt > 0.f ? m + log2f(lt) - static_cast<float>(KPF) : -INFINITY;
       }
       ++itc;
     }
@@ -483,7 +524,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  if (warp == TMA_WARP) tmem_dealloc(tmem, 256);
+  if (warp == TMA_WARP) tmem_dealloc(tmem, 512);
 }
 
 }  // namespace
@@ -509,6 +550,7 @@ cudaError_t launch_fwd_main(const FwdMainArgs& a, cudaStream_t stream) {
   p.o = a.o;
   p.lse = a.lse;
   p.err = a.err;
+  p.sched = a.sched;
   p.S = a.S;
   p.nb = a.nb;
   p.words = (a.nb + 31) / 32;

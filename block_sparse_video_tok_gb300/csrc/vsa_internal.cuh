@@ -32,7 +32,7 @@ struct BwdLayout {
   size_t err, sched, absmax, delta, order, dqacc, q16, k16, v16, do16, total;
 };
 struct FwdLayout {
-  size_t err, absmax, bitmap, q16, k16, v16, total;
+  size_t err, sched, absmax, bitmap, q16, k16, v16, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -70,6 +70,7 @@ inline FwdLayout fwd_layout(long B, long H, long S) {
   const size_t words = (nb + 31) / 32;
   size_t off = 0;
   L.err = off;
+  L.sched = 128;  // work counter of the main kernel's dynamic scheduler (inside the header)
   off += 256;
   L.absmax = off;
   off = align_up(off + bh * 4 * sizeof(uint32_t), 1024);
@@ -166,6 +167,7 @@ struct FwdMainArgs {
   __nv_bfloat16* o;
   float* lse;
   uint32_t* err;
+  int32_t* sched;  // zeroed work counter
   int B, H, S, nb;
   float sm_scale;
 };

@@ -108,6 +108,24 @@ SMALL_CASES["zero_vbs_and_empty_rows"] = lambda: _special(
     "zero_vbs_and_empty_rows", wl.make_case(1, 2, 6, 3, seed=14))
 
 
+def _scaled_kv_blocks(case, factor):
+    """K of kv block j multiplied by factor(j) (then rounded to bf16 again): with growing
+    factors each block's scores exceed the previous maximum by several log2 units, so the online
+    softmax of the forward moves its reference maximum and rescales O many times; with shrinking
+    factors the first block holds the maximum and later P values are tiny."""
+    k = case["k"].float()
+    for j in range(case["nb"]):
+        k[:, :, 64 * j:64 * (j + 1)] *= factor(j)
+    case["k"] = k.to(torch.bfloat16)
+    return case
+
+
+SMALL_CASES["growing_scores"] = lambda: _scaled_kv_blocks(
+    wl.make_case(1, 2, 16, 8, vbs="ragged32", seed=15), lambda j: 1.0 + j)
+SMALL_CASES["shrinking_scores"] = lambda: _scaled_kv_blocks(
+    wl.make_case(1, 2, 16, 8, vbs="ragged32", seed=16), lambda j: 16.0 - j)
+
+
 def _run_small(vsa, case):
     B, H, S, nb = case["B"], case["H"], case["S"], case["nb"]
     o64, lse64 = oracle_forward(case)
