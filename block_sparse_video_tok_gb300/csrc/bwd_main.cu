@@ -301,142 +301,142 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------------ UMMA issuer
-    if (lane == 0) {
-      uint32_t g = 0, itc = 0;
-      bool ok = true, issued = false;
-      // Operand descriptors, built once; each UMMA only adds a constant byte offset to them.
-      //   K-major (S, dP; dQ^T's B): 32 B per k-step inside a 128-B row, 64-element chunks apart.
-      //   MN-major (dV^T, dK^T, dQ^T's A): 2048 B (16 rows) per k-step.
-      const uint64_t k_kmaj = sdesc_sw128(base + SM_K, 16, 1024);
-      const uint64_t v_kmaj = sdesc_sw128(base + SM_V, 16, 1024);
-      const uint64_t k_mn = sdesc_sw128(base + SM_K, 8192, 1024);
-      const uint64_t p_mn = sdesc_sw128(base + SM_P, 16384, 1024);
-      const uint64_t q_kmaj = sdesc_sw128(base + SM_Q, 16, 1024);
-      const uint64_t do_kmaj = sdesc_sw128(base + SM_DO, 16, 1024);
-      const uint64_t q_mn = sdesc_sw128(base + SM_Q, 16384, 1024);
-      const uint64_t do_mn = sdesc_sw128(base + SM_DO, 16384, 1024);
-      const uint64_t ds_mn = sdesc_sw128(base + SM_DS, 16384, 1024);
-      const uint64_t ds_kmaj = sdesc_sw128(base + SM_DS, 16, 1024);
-      const uint32_t t_s = tmem + TM_S, t_dp = tmem + TM_DP, t_dv = tmem + TM_DVT,
-                     t_dk = tmem + TM_DKT;
-      // S = Q_p K_j^T and dP = dO_p V_j^T of step gs (stage gs & 1).
-      auto issue_sdp = [&](uint32_t gs) {
-        const uint32_t so = (gs & 1u) * 32768u;
-        const uint64_t qa = sdesc_advance(q_kmaj, so), da = sdesc_advance(do_kmaj, so);
-        umma_f16_c<false>(t_s, qa, k_kmaj, IDESC_SDP);
+    // The whole warp runs this role in lockstep; every lane polls the barriers and one elected
+    // lane issues each UMMA and commit.
+    uint32_t g = 0, itc = 0;
+    bool ok = true, issued = false;
+    // Operand descriptors, built once; each UMMA only adds a constant byte offset to them.
+    //   K-major (S, dP; dQ^T's B): 32 B per k-step inside a 128-B row, 64-element chunks apart.
+    //   MN-major (dV^T, dK^T, dQ^T's A): 2048 B (16 rows) per k-step.
+    const uint64_t k_kmaj = sdesc_sw128(base + SM_K, 16, 1024);
+    const uint64_t v_kmaj = sdesc_sw128(base + SM_V, 16, 1024);
+    const uint64_t k_mn = sdesc_sw128(base + SM_K, 8192, 1024);
+    const uint64_t p_mn = sdesc_sw128(base + SM_P, 16384, 1024);
+    const uint64_t q_kmaj = sdesc_sw128(base + SM_Q, 16, 1024);
+    const uint64_t do_kmaj = sdesc_sw128(base + SM_DO, 16, 1024);
+    const uint64_t q_mn = sdesc_sw128(base + SM_Q, 16384, 1024);
+    const uint64_t do_mn = sdesc_sw128(base + SM_DO, 16384, 1024);
+    const uint64_t ds_mn = sdesc_sw128(base + SM_DS, 16384, 1024);
+    const uint64_t ds_kmaj = sdesc_sw128(base + SM_DS, 16, 1024);
+    const uint32_t t_s = tmem + TM_S, t_dp = tmem + TM_DP, t_dv = tmem + TM_DVT,
+                   t_dk = tmem + TM_DKT;
+    // S = Q_p K_j^T and dP = dO_p V_j^T of step gs (stage gs & 1).
+    auto issue_sdp = [&](uint32_t gs) {
+      const uint32_t so = (gs & 1u) * 32768u;
+      const uint64_t qa = sdesc_advance(q_kmaj, so), da = sdesc_advance(do_kmaj, so);
+      umma_ss_elect<false>(t_s, qa, k_kmaj, IDESC_SDP);
 #pragma unroll
-        for (int kk = 1; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384u + (kk & 3) * 32u;
-          umma_f16_c<true>(t_s, sdesc_advance(qa, off),
-                           sdesc_advance(k_kmaj, (kk >> 2) * 8192u + (kk & 3) * 32u), IDESC_SDP);
-        }
-        umma_f16_c<false>(t_dp, da, v_kmaj, IDESC_SDP);
+      for (int kk = 1; kk < 8; ++kk) {
+        const uint32_t off = (kk >> 2) * 16384u + (kk & 3) * 32u;
+        umma_ss_elect<true>(t_s, sdesc_advance(qa, off),
+                         sdesc_advance(k_kmaj, (kk >> 2) * 8192u + (kk & 3) * 32u), IDESC_SDP);
+      }
+      umma_ss_elect<false>(t_dp, da, v_kmaj, IDESC_SDP);
 #pragma unroll
-        for (int kk = 1; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384u + (kk & 3) * 32u;
-          umma_f16_c<true>(t_dp, sdesc_advance(da, off),
-                           sdesc_advance(v_kmaj, (kk >> 2) * 8192u + (kk & 3) * 32u), IDESC_SDP);
+      for (int kk = 1; kk < 8; ++kk) {
+        const uint32_t off = (kk >> 2) * 16384u + (kk & 3) * 32u;
+        umma_ss_elect<true>(t_dp, sdesc_advance(da, off),
+                         sdesc_advance(v_kmaj, (kk >> 2) * 8192u + (kk & 3) * 32u), IDESC_SDP);
+      }
+      umma_commit_elect(bar(SDP_FULL));
+    };
+    // dQ^T = K_j^T dS^T of step gs into TMEM buffer gs & 1; then its P/dS buffer is free.
+    auto issue_dq = [&](uint32_t gs) -> bool {
+      const uint32_t b = gs & 1u;
+      if (!mbar_wait_warp(bar(DQ_FREE0 + b), ((gs >> 1) & 1u) ^ 1u, abort, WAIT_LIMIT_NS))
+        return false;
+      tc_fence_after_sync();
+      const uint64_t dsb = sdesc_advance(ds_kmaj, b * 16384u);
+      const uint32_t t_dq = tmem + TM_DQT + b * 128u;
+      umma_ss_elect<false>(t_dq, k_mn, dsb, IDESC_DQ);
+#pragma unroll
+      for (int kk = 1; kk < 4; ++kk)
+        umma_ss_elect<true>(t_dq, sdesc_advance(k_mn, kk * 2048u), sdesc_advance(dsb, kk * 32u),
+                         IDESC_DQ);
+      umma_commit_elect(bar(DQ_FULL0 + b));
+      umma_commit_elect(bar(PDS_FREE0 + b));
+      return true;
+    };
+    // dV^T += dO_p^T P and dK^T += Q_p^T dS of step gs; the first step of an item overwrites.
+    auto issue_dvdk = [&](uint32_t gs, bool first) {
+      const uint32_t so = (gs & 1u) * 32768u;
+      const uint64_t da = sdesc_advance(do_mn, so), qa = sdesc_advance(q_mn, so);
+      const uint64_t dsb = sdesc_advance(ds_mn, (gs & 1u) * 16384u);
+      if (first)
+        umma_ss_elect<false>(t_dv, da, p_mn, IDESC_DVK);
+      else
+        umma_ss_elect<true>(t_dv, da, p_mn, IDESC_DVK);
+#pragma unroll
+      for (int kk = 1; kk < 8; ++kk)
+        umma_ss_elect<true>(t_dv, sdesc_advance(da, kk * 2048u), sdesc_advance(p_mn, kk * 2048u),
+                         IDESC_DVK);
+      if (first)
+        umma_ss_elect<false>(t_dk, qa, dsb, IDESC_DVK);
+      else
+        umma_ss_elect<true>(t_dk, qa, dsb, IDESC_DVK);
+#pragma unroll
+      for (int kk = 1; kk < 8; ++kk)
+        umma_ss_elect<true>(t_dk, sdesc_advance(qa, kk * 2048u), sdesc_advance(dsb, kk * 2048u),
+                         IDESC_DVK);
+    };
+    for (uint32_t k = 0;; ++k) {
+      int w;
+      if (!warp_take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, lane, &w)) {
+        ok = false;
+        break;
+      }
+      if (w >= p.total) break;
+      const Item it = decode_item(p, w);
+      if (it.n == 0) continue;
+      const int np = (it.n + 1) >> 1;
+      if (!mbar_wait_warp(bar(KV_FULL), itc & 1u, abort, WAIT_LIMIT_NS)) {
+        ok = false;
+        break;
+      }
+      for (int pp = 0; pp < np; ++pp, ++g) {
+        const uint32_t s = g & 1u;
+        if (!mbar_wait_warp(bar(QDO_FULL0 + s), (g >> 1) & 1u, abort, WAIT_LIMIT_NS)) {
+          ok = false;
+          break;
         }
-        umma_commit(bar(SDP_FULL));
-      };
-      // dQ^T = K_j^T dS^T of step gs into TMEM buffer gs & 1; then its P/dS buffer is free.
-      auto issue_dq = [&](uint32_t gs) -> bool {
-        const uint32_t b = gs & 1u;
-        if (!mbar_wait_bounded(bar(DQ_FREE0 + b), ((gs >> 1) & 1u) ^ 1u, abort, WAIT_LIMIT_NS))
-          return false;
         tc_fence_after_sync();
-        const uint64_t dsb = sdesc_advance(ds_kmaj, b * 16384u);
-        const uint32_t t_dq = tmem + TM_DQT + b * 128u;
-        umma_f16_c<false>(t_dq, k_mn, dsb, IDESC_DQ);
-#pragma unroll
-        for (int kk = 1; kk < 4; ++kk)
-          umma_f16_c<true>(t_dq, sdesc_advance(k_mn, kk * 2048u), sdesc_advance(dsb, kk * 32u),
-                           IDESC_DQ);
-        umma_commit(bar(DQ_FULL0 + b));
-        umma_commit(bar(PDS_FREE0 + b));
-        return true;
-      };
-      // dV^T += dO_p^T P and dK^T += Q_p^T dS of step gs; the first step of an item overwrites.
-      auto issue_dvdk = [&](uint32_t gs, bool first) {
-        const uint32_t so = (gs & 1u) * 32768u;
-        const uint64_t da = sdesc_advance(do_mn, so), qa = sdesc_advance(q_mn, so);
-        const uint64_t dsb = sdesc_advance(ds_mn, (gs & 1u) * 16384u);
-        if (first)
-          umma_f16_c<false>(t_dv, da, p_mn, IDESC_DVK);
-        else
-          umma_f16_c<true>(t_dv, da, p_mn, IDESC_DVK);
-#pragma unroll
-        for (int kk = 1; kk < 8; ++kk)
-          umma_f16_c<true>(t_dv, sdesc_advance(da, kk * 2048u), sdesc_advance(p_mn, kk * 2048u),
-                           IDESC_DVK);
-        if (first)
-          umma_f16_c<false>(t_dk, qa, dsb, IDESC_DVK);
-        else
-          umma_f16_c<true>(t_dk, qa, dsb, IDESC_DVK);
-#pragma unroll
-        for (int kk = 1; kk < 8; ++kk)
-          umma_f16_c<true>(t_dk, sdesc_advance(qa, kk * 2048u), sdesc_advance(dsb, kk * 2048u),
-                           IDESC_DVK);
-      };
-      for (uint32_t k = 0;; ++k) {
-        int w;
-        if (!take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, &w)) {
+        // The softmax finished reading S/dP(g-1) before it arrived on P_READY(g-1).
+        issue_sdp(g);
+        issued = true;
+        if (pp > 0 && !issue_dq(g - 1)) {
           ok = false;
           break;
         }
-        if (w >= p.total) break;
-        const Item it = decode_item(p, w);
-        if (it.n == 0) continue;
-        const int np = (it.n + 1) >> 1;
-        if (!mbar_wait_bounded(bar(KV_FULL), itc & 1u, abort, WAIT_LIMIT_NS)) {
+        if (!mbar_wait_warp(bar(P_READY), g & 1u, abort, WAIT_LIMIT_NS)) {
           ok = false;
           break;
         }
-        for (int pp = 0; pp < np; ++pp, ++g) {
-          const uint32_t s = g & 1u;
-          if (!mbar_wait_bounded(bar(QDO_FULL0 + s), (g >> 1) & 1u, abort, WAIT_LIMIT_NS)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-          // The softmax finished reading S/dP(g-1) before it arrived on P_READY(g-1).
-          issue_sdp(g);
-          issued = true;
-          if (pp > 0 && !issue_dq(g - 1)) {
-            ok = false;
-            break;
-          }
-          if (!mbar_wait_bounded(bar(P_READY), g & 1u, abort, WAIT_LIMIT_NS)) {
-            ok = false;
-            break;
-          }
-          if (pp == 0 &&
-              !mbar_wait_bounded(bar(ACC_EMPTY), (itc & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-          issue_dvdk(g, pp == 0);
-          umma_commit(bar(QDO_EMPTY0 + s));  // Q_p and dO_p of step g are no longer read
-        }
-        if (!ok) break;
-        if (!issue_dq(g - 1)) {
+        if (pp == 0 &&
+            !mbar_wait_warp(bar(ACC_EMPTY), (itc & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) {
           ok = false;
           break;
         }
-        umma_commit(bar(ACC_FULL));
-        umma_commit(bar(KV_EMPTY));
-        ++itc;
+        tc_fence_after_sync();
+        issue_dvdk(g, pp == 0);
+        umma_commit_elect(bar(QDO_EMPTY0 + s));  // Q_p and dO_p of step g are no longer read
       }
-      if (!ok) raise_abort(abort, p.err);
-      if (issued) {
-        // Every UMMA has completed before TMEM is released.
-        umma_commit(bar(DRAIN));
-        volatile int never = 0;
-        mbar_wait_bounded(bar(DRAIN), 0, &never, DRAIN_LIMIT_NS);
+      if (!ok) break;
+      if (!issue_dq(g - 1)) {
+        ok = false;
+        break;
       }
+      umma_commit_elect(bar(ACC_FULL));
+      umma_commit_elect(bar(KV_EMPTY));
+      ++itc;
     }
-    __syncwarp();
+    if (!ok && lane == 0) raise_abort(abort, p.err);
+    if (issued) {
+      // Every UMMA has completed before TMEM is released.
+      umma_commit_elect(bar(DRAIN));
+      volatile int never = 0;
+      if (lane == 0) mbar_wait_bounded(bar(DRAIN), 0, &never, DRAIN_LIMIT_NS);
+      __syncwarp();
+    }
   } else if (warp < SOFTMAX_WARPS) {
     // ------------------------------------------------------------------ softmax / dS
     const int quarter = warp & 3, h = warp >> 2;  // TMEM lane quarter; S/dP column half

@@ -13,15 +13,24 @@
 //   2^(m_old - m_new) first (otherwise m stays, so P stays below 2^(RESCALE + KPF));
 //   P = 2^(s - m + KPF) in fp16, written to TMEM, where it is the A operand of
 //   O += P V_j (B = V_j from shared memory, MN-major).
-// At the end O / l and lse = m + log2(l).  P never passes through shared memory, so per kv block
-// the tensor pipe reads Q_p, K_j and V_j only.
+// P never passes through shared memory, so per kv block the tensor pipe reads Q_p, K_j and V_j
+// only.
 //
-// Roles (320 threads): warps 0-7 softmax -- warps w and w+4 share TMEM lane quarter w (query
-// rows 32w..32w+31) and split the 64 kv columns of S (and the 128 columns of O) in halves,
-// exchanging their block maxima through shared memory; warp 8 TMA producer, TMEM owner and work
-// claimer; warp 9 UMMA issuer, which issues S of the next kv block before P.V of the current one
-// so the softmax of one block overlaps the tensor work of its neighbours.
-// TMEM (512 columns allocated): O [0,128), S x2 [128,256), P x2 [256,320).
+// The union's kv blocks alternate between two softmax groups (block t of the CTA goes to group
+// t & 1), each with its own online-softmax state (m, l) and its own O accumulator, the split of
+// the kv range that flash-decoding uses.  The two groups' chains are independent, so one group's
+// softmax overlaps the other's and the tensor pipe always has work queued.  At the end of the
+// item the two partial results merge:
+//   M = max(m_0, m_1),  w_g = 2^(m_g - M),  O = (w_0 O_0 + w_1 O_1) / (w_0 l_0 + w_1 l_1),
+//   lse = M + log2(w_0 l_0 + w_1 l_1).
+//
+// Roles (352 threads): warps 0-3 softmax group 0 and warps 4-7 group 1 -- warp w owns TMEM lane
+// quarter w % 4 (query rows 32(w%4) .. +31), one full row of S per thread; warp 8 work claimer,
+// TMEM owner and TMA producer of Q and K; warp 9 UMMA issuer, which keeps S two kv blocks ahead
+// of P.V; warp 10 TMA producer of V.  K and V have rings of their own: a K stage is free once S
+// has been computed, two kv blocks before P.V frees the V stage of the same block, so the K
+// loads run that much further ahead.
+// TMEM (512 columns allocated): O x2 [0,256), S x2 [256,384), P x2 [384,448).
 #include "ptx.cuh"
 #include "queue.cuh"
 #include "vsa_internal.cuh"
@@ -30,45 +39,51 @@ namespace vsa {
 
 namespace {
 
-constexpr int NUM_THREADS = 320;
+constexpr int NUM_THREADS = 352;
 constexpr int SOFTMAX_WARPS = 8;
 constexpr int TMA_WARP = 8;
 constexpr int MMA_WARP = 9;
-constexpr int KV_STAGES = 4;
+constexpr int V_WARP = 10;
+constexpr int K_STAGES = 4;
+constexpr int V_STAGES = 5;
 constexpr int KPF = 7;               // P is carried as P * 2^KPF: below 2^(RESCALE + KPF) = 2^15
 constexpr float RESCALE = 8.0f;      // log2 units the block maximum may exceed m by before a rescale
 
-constexpr uint32_t SM_Q = 0;                          // 2 stages x 2 chunks x [128 q x 128 B]
-constexpr uint32_t SM_KV = 2 * 32768;                 // stages x (K 16 KB, V 16 KB)
-constexpr uint32_t SM_XCH = SM_KV + KV_STAGES * 32768;  // [2 parity][2 halves][128 rows] float
-constexpr uint32_t SM_BAR = SM_XCH + 2 * 2 * 128 * 4;
+constexpr uint32_t SM_Q = 0;                         // 2 stages x 2 chunks x [128 q x 128 B]
+constexpr uint32_t SM_K = 2 * 32768;                 // K stages x 2 chunks x [64 kv x 128 B]
+constexpr uint32_t SM_V = SM_K + K_STAGES * 16384;   // V stages, same layout
+constexpr uint32_t SM_XCH = SM_V + V_STAGES * 16384;  // [2 parity][2 groups][128 rows] (m, l)
+constexpr uint32_t SM_BAR = SM_XCH + 2 * 2 * 128 * 8;
 
 enum Bar : uint32_t {
   Q_FULL0 = 0,
   Q_EMPTY0 = Q_FULL0 + 2,
-  KV_FULL0 = Q_EMPTY0 + 2,
-  KV_EMPTY0 = KV_FULL0 + KV_STAGES,
-  S_FULL0 = KV_EMPTY0 + KV_STAGES,
+  K_FULL0 = Q_EMPTY0 + 2,
+  K_EMPTY0 = K_FULL0 + K_STAGES,
+  V_FULL0 = K_EMPTY0 + K_STAGES,
+  V_EMPTY0 = V_FULL0 + V_STAGES,
+  S_FULL0 = V_EMPTY0 + V_STAGES,
   S_FREE0 = S_FULL0 + 2,
   P_READY0 = S_FREE0 + 2,
   P_FREE0 = P_READY0 + 2,
-  PV_DONE = P_FREE0 + 2,  // one phase per P.V, for the rescale of O
-  O_FULL,
+  O_FULL = P_FREE0 + 2,
   O_EMPTY,
   DRAIN,
-  XCH0,  // one per lane quarter: both column-half warps have published a value
+  XCH0,  // one per lane quarter: both groups' warps have published (m, l) of the item
   ITEM_FULL0 = XCH0 + 4,
   ITEM_EMPTY0 = ITEM_FULL0 + ITEM_SLOTS,
   NUM_BARS = ITEM_EMPTY0 + ITEM_SLOTS
 };
-constexpr uint32_t ITEM_CONSUMERS = 1 + SOFTMAX_WARPS;  // the UMMA thread and the softmax warps
+// The UMMA thread, the softmax warps and the V producer.
+constexpr uint32_t ITEM_CONSUMERS = 1 + SOFTMAX_WARPS + 1;
+constexpr uint32_t GROUP_WARPS = SOFTMAX_WARPS / 2;
 constexpr uint32_t SM_TMEM_SLOT = SM_BAR + NUM_BARS * 8;
 constexpr uint32_t SM_ABORT = SM_TMEM_SLOT + 4;
 constexpr uint32_t SM_QUEUE = SM_ABORT + 4;
 constexpr uint32_t SMEM_BYTES = SM_QUEUE + 4 * ITEM_SLOTS + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-constexpr uint32_t TM_O = 0, TM_S = 128, TM_P = 256;
+constexpr uint32_t TM_O = 0, TM_S = 256, TM_P = 384;  // each x2: group g at + g * width
 constexpr uint32_t IDESC_S = idesc_f16_f32acc(128, 64, false, false);
 constexpr uint32_t IDESC_PV = idesc_f16_f32acc(128, 128, false, true);
 
@@ -175,15 +190,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(bar(Q_FULL0 + s), 1);
       mbar_init(bar(Q_EMPTY0 + s), 1);
       mbar_init(bar(S_FULL0 + s), 1);
-      mbar_init(bar(S_FREE0 + s), SOFTMAX_WARPS);
-      mbar_init(bar(P_READY0 + s), SOFTMAX_WARPS);
+      mbar_init(bar(S_FREE0 + s), GROUP_WARPS);
+      mbar_init(bar(P_READY0 + s), GROUP_WARPS);
       mbar_init(bar(P_FREE0 + s), 1);
     }
-    for (int s = 0; s < KV_STAGES; ++s) {
-      mbar_init(bar(KV_FULL0 + s), 1);
-      mbar_init(bar(KV_EMPTY0 + s), 1);
+    for (int s = 0; s < K_STAGES; ++s) {
+      mbar_init(bar(K_FULL0 + s), 1);
+      mbar_init(bar(K_EMPTY0 + s), 1);
     }
-    mbar_init(bar(PV_DONE), 1);
+    for (int s = 0; s < V_STAGES; ++s) {
+      mbar_init(bar(V_FULL0 + s), 1);
+      mbar_init(bar(V_EMPTY0 + s), 1);
+    }
     mbar_init(bar(O_FULL), 1);
     mbar_init(bar(O_EMPTY), SOFTMAX_WARPS);
     mbar_init(bar(DRAIN), 1);
@@ -209,11 +227,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == TMA_WARP) {
-    // ------------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------------ TMA producer: Q, K
     if (lane == 0) {
       uint32_t lg = 0, itc = 0;  // kv blocks loaded; items with a non-empty union
-      int64_t last_lg[KV_STAGES], last_q[2] = {-1, -1};
-      for (int s = 0; s < KV_STAGES; ++s) last_lg[s] = -1;
+      int64_t last_lg[K_STAGES], last_q[2] = {-1, -1};
+      for (int s = 0; s < K_STAGES; ++s) last_lg[s] = -1;
       bool ok = true;
       for (uint32_t k = 0;; ++k) {
         int w;
@@ -240,17 +258,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_load_2d(qd + 24576, &tm_q, bar(Q_FULL0 + qs), 64, r1);
         last_q[qs] = itc;
         ok = for_union(p, q, [&](int j) {
-          const uint32_t st = lg % KV_STAGES;
-          if (!mbar_wait_bounded(bar(KV_EMPTY0 + st), ((lg / KV_STAGES) & 1u) ^ 1u, abort,
+          const uint32_t st = lg % K_STAGES;
+          if (!mbar_wait_bounded(bar(K_EMPTY0 + st), ((lg / K_STAGES) & 1u) ^ 1u, abort,
                                  WAIT_LIMIT_NS))
             return false;
           const int rk = q.bh * S + j * BLOCK;
-          const uint32_t kd = base + SM_KV + st * 32768u;
-          mbar_arrive_expect_tx(bar(KV_FULL0 + st), 32768u);
-          tma_load_2d(kd, &tm_k, bar(KV_FULL0 + st), 0, rk);
-          tma_load_2d(kd + 8192, &tm_k, bar(KV_FULL0 + st), 64, rk);
-          tma_load_2d(kd + 16384, &tm_v, bar(KV_FULL0 + st), 0, rk);
-          tma_load_2d(kd + 24576, &tm_v, bar(KV_FULL0 + st), 64, rk);
+          const uint32_t kd = base + SM_K + st * 16384u;
+          mbar_arrive_expect_tx(bar(K_FULL0 + st), 16384u);
+          tma_load_2d(kd, &tm_k, bar(K_FULL0 + st), 0, rk);
+          tma_load_2d(kd + 8192, &tm_k, bar(K_FULL0 + st), 64, rk);
           last_lg[st] = lg;
           ++lg;
           return true;
@@ -266,66 +282,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (last_q[s] >= 0)
             mbar_wait_bounded(bar(Q_FULL0 + s), (static_cast<uint32_t>(last_q[s]) >> 1) & 1u,
                               &never, DRAIN_LIMIT_NS);
-        for (int s = 0; s < KV_STAGES; ++s)
+        for (int s = 0; s < K_STAGES; ++s)
           if (last_lg[s] >= 0)
-            mbar_wait_bounded(bar(KV_FULL0 + s),
-                              (static_cast<uint32_t>(last_lg[s]) / KV_STAGES) & 1u, &never,
-                              DRAIN_LIMIT_NS);
+            mbar_wait_bounded(bar(K_FULL0 + s), (static_cast<uint32_t>(last_lg[s]) / K_STAGES) & 1u,
+                              &never, DRAIN_LIMIT_NS);
       }
     }
     __syncwarp();
-  } else if (warp == MMA_WARP) {
-    // ------------------------------------------------------------------ UMMA issuer
+  } else if (warp == V_WARP) {
+    // ------------------------------------------------------------------ TMA producer: V
     if (lane == 0) {
-      uint32_t t = 0, itc = 0;  // kv blocks issued (one S and one P.V each); items
-      bool ok = true, issued = false;
-      const uint64_t q_kmaj = sdesc_sw128(base + SM_Q, 16, 1024);
-      const uint64_t k_kmaj = sdesc_sw128(base + SM_KV, 16, 1024);           // K of stage 0
-      const uint64_t v_mn = sdesc_sw128(base + SM_KV + 16384u, 8192, 1024);  // V of stage 0
-      // S = Q_p K_j^T of kv block tb into S buffer tb & 1; Q from stage qs.
-      auto issue_s = [&](uint32_t tb, uint32_t qs) -> bool {
-        const uint32_t st = tb % KV_STAGES, sb = tb & 1u;
-        if (!mbar_wait_bounded(bar(KV_FULL0 + st), (tb / KV_STAGES) & 1u, abort, WAIT_LIMIT_NS))
-          return false;
-        if (!mbar_wait_bounded(bar(S_FREE0 + sb), ((tb >> 1) & 1u) ^ 1u, abort, WAIT_LIMIT_NS))
-          return false;
-        tc_fence_after_sync();
-        const uint64_t qa = sdesc_advance(q_kmaj, qs * 32768u);
-        const uint64_t kd = sdesc_advance(k_kmaj, st * 32768u);
-        const uint32_t ts = tmem + TM_S + sb * 64u;
-        umma_f16_c<false>(ts, qa, kd, IDESC_S);
-#pragma unroll
-        for (int kk = 1; kk < 8; ++kk) {
-          const uint32_t off = (kk & 3) * 32u;
-          umma_f16_c<true>(ts, sdesc_advance(qa, (kk >> 2) * 16384u + off),
-                           sdesc_advance(kd, (kk >> 2) * 8192u + off), IDESC_S);
-        }
-        umma_commit(bar(S_FULL0 + sb));
-        issued = true;
-        return true;
-      };
-      // O += P V_j of kv block tb: A = P buffer tb & 1 in TMEM (8 columns per 16 kv), B = V_j.
-      auto issue_pv = [&](uint32_t tb, bool first) -> bool {
-        const uint32_t pb = tb & 1u, st = tb % KV_STAGES;
-        if (!mbar_wait_bounded(bar(P_READY0 + pb), (tb >> 1) & 1u, abort, WAIT_LIMIT_NS))
-          return false;
-        if (first && !mbar_wait_bounded(bar(O_EMPTY), (itc & 1u) ^ 1u, abort, WAIT_LIMIT_NS))
-          return false;
-        tc_fence_after_sync();
-        const uint32_t pa = tmem + TM_P + pb * 32u;
-        const uint64_t vb = sdesc_advance(v_mn, st * 32768u);
-        if (first)
-          umma_f16_ta<false>(tmem + TM_O, pa, vb, IDESC_PV);
-        else
-          umma_f16_ta<true>(tmem + TM_O, pa, vb, IDESC_PV);
-#pragma unroll
-        for (int kk = 1; kk < 4; ++kk)
-          umma_f16_ta<true>(tmem + TM_O, pa + kk * 8u, sdesc_advance(vb, kk * 2048u), IDESC_PV);
-        umma_commit(bar(P_FREE0 + pb));
-        umma_commit(bar(KV_EMPTY0 + st));
-        umma_commit(bar(PV_DONE));
-        return true;
-      };
+      uint32_t lg = 0;
+      int64_t last_lg[V_STAGES];
+      for (int s = 0; s < V_STAGES; ++s) last_lg[s] = -1;
+      bool ok = true;
       for (uint32_t k = 0;; ++k) {
         int w;
         if (!take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, &w)) {
@@ -334,66 +304,143 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (w >= p.total) break;
         const Pair q = decode_pair(p, w);
-        const int nu = union_size(p, q);
-        if (nu == 0) continue;
-        const uint32_t qs = itc & 1u;
-        if (!mbar_wait_bounded(bar(Q_FULL0 + qs), (itc >> 1) & 1u, abort, WAIT_LIMIT_NS)) {
-          ok = false;
-          break;
-        }
-        const uint32_t t0 = t;
-        if (!issue_s(t0, qs)) {
-          ok = false;
-          break;
-        }
-        for (int e = 0; e < nu; ++e) {
-          if (e + 1 < nu) {
-            if (!issue_s(t0 + e + 1, qs)) {
-              ok = false;
-              break;
-            }
-          } else {
-            umma_commit(bar(Q_EMPTY0 + qs));  // every S of the item has been issued
-          }
-          if (!issue_pv(t0 + e, e == 0)) {
-            ok = false;
-            break;
-          }
-        }
+        ok = for_union(p, q, [&](int j) {
+          const uint32_t st = lg % V_STAGES;
+          if (!mbar_wait_bounded(bar(V_EMPTY0 + st), ((lg / V_STAGES) & 1u) ^ 1u, abort,
+                                 WAIT_LIMIT_NS))
+            return false;
+          const int rk = q.bh * S + j * BLOCK;
+          const uint32_t vd = base + SM_V + st * 16384u;
+          mbar_arrive_expect_tx(bar(V_FULL0 + st), 16384u);
+          tma_load_2d(vd, &tm_v, bar(V_FULL0 + st), 0, rk);
+          tma_load_2d(vd + 8192, &tm_v, bar(V_FULL0 + st), 64, rk);
+          last_lg[st] = lg;
+          ++lg;
+          return true;
+        });
         if (!ok) break;
-        umma_commit(bar(O_FULL));
-        t = t0 + nu;
-        ++itc;
       }
-      if (!ok) raise_abort(abort, p.err);
-      if (issued) {
-        // Every UMMA has completed before TMEM is released.
-        umma_commit(bar(DRAIN));
+      if (!ok) {
+        raise_abort(abort, p.err);
         volatile int never = 0;
-        mbar_wait_bounded(bar(DRAIN), 0, &never, DRAIN_LIMIT_NS);
+        for (int s = 0; s < V_STAGES; ++s)
+          if (last_lg[s] >= 0)
+            mbar_wait_bounded(bar(V_FULL0 + s), (static_cast<uint32_t>(last_lg[s]) / V_STAGES) & 1u,
+                              &never, DRAIN_LIMIT_NS);
       }
     }
     __syncwarp();
-  } else {
-    // ------------------------------------------------------------------ softmax (warps 0-7)
-    const int quarter = warp & 3, h = warp >> 2;  // TMEM lane quarter; column half
-    const int r = quarter * 32 + lane;            // query row of the pair == TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    float* xch = reinterpret_cast<float*>(gbase + SM_XCH);
-    uint32_t t = 0, itc = 0, xc = 0;  // kv blocks seen; items with a non-empty union; exchanges
-    // The partner warp's value of this row (the other column half).  Slots alternate with the
-    // exchange count, so a slot is rewritten only after the partner has read it.
-    auto exchange = [&](float x, float* y) -> bool {
-      float* slot = xch + (xc & 1u) * 256u;
-      slot[h * 128 + r] = x;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(XCH0 + quarter));
-      if (!warp_wait(bar(XCH0 + quarter), xc & 1u, abort, lane)) return false;
-      __syncwarp();
-      *y = slot[(1 - h) * 128 + r];
-      ++xc;
+  } else if (warp == MMA_WARP) {
+    // ------------------------------------------------------------------ UMMA issuer
+    // The whole warp runs this role in lockstep; every lane polls the barriers and one elected
+    // lane issues each UMMA and commit.
+    uint32_t t = 0, itc = 0;  // kv blocks issued (one S and one P.V each); items
+    bool ok = true, issued = false;
+    const uint64_t q_kmaj = sdesc_sw128(base + SM_Q, 16, 1024);
+    const uint64_t k_kmaj = sdesc_sw128(base + SM_K, 16, 1024);   // K of stage 0
+    const uint64_t v_mn = sdesc_sw128(base + SM_V, 8192, 1024);   // V of stage 0
+    // S = Q_p K_j^T of kv block tb into S buffer tb & 1; Q from stage qs.
+    auto issue_s = [&](uint32_t tb, uint32_t qs) -> bool {
+      const uint32_t st = tb % K_STAGES, sb = tb & 1u;
+      if (!mbar_wait_warp(bar(K_FULL0 + st), (tb / K_STAGES) & 1u, abort, WAIT_LIMIT_NS))
+        return false;
+      if (!mbar_wait_warp(bar(S_FREE0 + sb), ((tb >> 1) & 1u) ^ 1u, abort, WAIT_LIMIT_NS))
+        return false;
+      tc_fence_after_sync();
+      const uint64_t qa = sdesc_advance(q_kmaj, qs * 32768u);
+      const uint64_t kd = sdesc_advance(k_kmaj, st * 16384u);
+      const uint32_t ts = tmem + TM_S + sb * 64u;
+      umma_ss_elect<false>(ts, qa, kd, IDESC_S);
+#pragma unroll
+      for (int kk = 1; kk < 8; ++kk) {
+        const uint32_t off = (kk & 3) * 32u;
+        umma_ss_elect<true>(ts, sdesc_advance(qa, (kk >> 2) * 16384u + off),
+                         sdesc_advance(kd, (kk >> 2) * 8192u + off), IDESC_S);
+      }
+      umma_commit_elect(bar(S_FULL0 + sb));
+      umma_commit_elect(bar(K_EMPTY0 + st));
+      issued = true;
       return true;
     };
+    // O_g += P V_j of kv block tb, g = tb & 1: A = P buffer g in TMEM (8 columns per 16 kv),
+    // B = V_j.  `fresh`: the group's first block of the item overwrites O_g; `first`: the
+    // item's first P.V waits until the previous item's O buffers have been read.
+    auto issue_pv = [&](uint32_t tb, bool fresh, bool first) -> bool {
+      const uint32_t g = tb & 1u, st = tb % V_STAGES;
+      if (!mbar_wait_warp(bar(V_FULL0 + st), (tb / V_STAGES) & 1u, abort, WAIT_LIMIT_NS))
+        return false;
+      if (!mbar_wait_warp(bar(P_READY0 + g), (tb >> 1) & 1u, abort, WAIT_LIMIT_NS))
+        return false;
+      if (first && !mbar_wait_warp(bar(O_EMPTY), (itc & 1u) ^ 1u, abort, WAIT_LIMIT_NS))
+        return false;
+      tc_fence_after_sync();
+      const uint32_t pa = tmem + TM_P + g * 32u, to = tmem + TM_O + g * 128u;
+      const uint64_t vb = sdesc_advance(v_mn, st * 16384u);
+      if (fresh)
+        umma_ts_elect<false>(to, pa, vb, IDESC_PV);
+      else
+        umma_ts_elect<true>(to, pa, vb, IDESC_PV);
+#pragma unroll
+      for (int kk = 1; kk < 4; ++kk)
+        umma_ts_elect<true>(to, pa + kk * 8u, sdesc_advance(vb, kk * 2048u), IDESC_PV);
+      umma_commit_elect(bar(P_FREE0 + g));
+      umma_commit_elect(bar(V_EMPTY0 + st));
+      return true;
+    };
+    for (uint32_t k = 0;; ++k) {
+      int w;
+      if (!warp_take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, lane, &w)) {
+        ok = false;
+        break;
+      }
+      if (w >= p.total) break;
+      const Pair q = decode_pair(p, w);
+      const int nu = union_size(p, q);
+      if (nu == 0) continue;
+      const uint32_t qs = itc & 1u;
+      if (!mbar_wait_warp(bar(Q_FULL0 + qs), (itc >> 1) & 1u, abort, WAIT_LIMIT_NS)) {
+        ok = false;
+        break;
+      }
+      // S runs two kv blocks ahead of P.V: S(e + 2) goes in as soon as group (e & 1) has
+      // read S(e), so that group finds its next S ready when it finishes P(e).
+      const uint32_t t0 = t;
+      const int ahead = nu < 2 ? nu : 2;
+      for (int e = 0; e < ahead && ok; ++e) ok = issue_s(t0 + e, qs);
+      if (ok && ahead == nu) umma_commit_elect(bar(Q_EMPTY0 + qs));  // every S has been issued
+      for (int e = 0; e < nu && ok; ++e) {
+        if (e + 2 < nu) {
+          if (!issue_s(t0 + e + 2, qs)) {
+            ok = false;
+            break;
+          }
+          if (e + 3 == nu) umma_commit_elect(bar(Q_EMPTY0 + qs));
+        }
+        ok = issue_pv(t0 + e, e < 2, e == 0);
+      }
+      if (!ok) break;
+      umma_commit_elect(bar(O_FULL));
+      t = t0 + nu;
+      ++itc;
+    }
+    if (!ok && lane == 0) raise_abort(abort, p.err);
+    if (issued) {
+      // Every UMMA has completed before TMEM is released.
+      umma_commit_elect(bar(DRAIN));
+      volatile int never = 0;
+      if (lane == 0) mbar_wait_bounded(bar(DRAIN), 0, &never, DRAIN_LIMIT_NS);
+      __syncwarp();
+    }
+  } else {
+    // ------------------------------------------------------------------ softmax (warps 0-7)
+    const int quarter = warp & 3, grp = warp >> 2;  // TMEM lane quarter; softmax group
+    const int r = quarter * 32 + lane;              // query row of the pair == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + TM_S + grp * 64u;
+    const uint32_t t_p = tmem + lane_off + TM_P + grp * 32u;
+    const uint32_t t_o = tmem + lane_off + TM_O + grp * 128u;
+    float2* xch = reinterpret_cast<float2*>(gbase + SM_XCH);  // [item parity][group][row] (m, l)
+    uint32_t t = 0, itc = 0;  // kv blocks of the CTA so far (both groups); items
     for (uint32_t k = 0;; ++k) {
       int w;
       if (!warp_take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, lane, &w)) {
@@ -407,11 +454,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const size_t grow = static_cast<size_t>(q.bh) * S +
                           static_cast<size_t>(r < 64 ? q.i0 : (q.i1 >= 0 ? q.i1 : q.i0)) * BLOCK +
                           (r & 63);
-      uint4* orow = reinterpret_cast<uint4*>(p.o + grow * HEAD_DIM) + h * 8;
-      if (union_size(p, q) == 0) {
+      uint4* orow = reinterpret_cast<uint4*>(p.o + grow * HEAD_DIM) + grp * 8;
+      const int nu = union_size(p, q);
+      if (nu == 0) {
         if (valid) {
           for (int c = 0; c < 8; ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
-          if (h == 0) p.lse[grow] = -INFINITY;
+          if (grp == 0) p.lse[grow] = -INFINITY;
         }
         continue;
       }
@@ -419,45 +467,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int eq = operand_exponent(am[0]), ek = operand_exponent(am[1]);
       const int ev = operand_exponent(am[2]);
       const float c1 = p.sm_scale * LOG2E_F * exp2i(eq + ek);  // S' -> s (log2 units)
-      float m = -INFINITY, l = 0.f;  // reference maximum; this half's sum of P * 2^KPF
-      bool first = true;
+      float m = -INFINITY, l = 0.f;  // this group's reference maximum and sum of P * 2^KPF
+      bool first = true;             // no block of this group in the item yet
       const bool ok = for_union(p, q, [&](int j) {
-        const uint32_t sb = t & 1u;
-        if (!warp_wait(bar(S_FULL0 + sb), (t >> 1) & 1u, abort, lane)) return false;
+        const uint32_t tb = t++;
+        if ((tb & 1u) != static_cast<uint32_t>(grp)) return true;  // the other group's block
+        if (!warp_wait(bar(S_FULL0 + grp), (tb >> 1) & 1u, abort, lane)) return false;
         tc_fence_after_sync();
         const bool mine = valid && ((own[j >> 5] >> (j & 31)) & 1u);
-        const int vb = mine ? clamp_vbs(p.vbs[j]) - h * 32 : 0;  // visible columns in my half
-        uint32_t sv[32];
-        tmem_ld_32x32b_x32(tmem + lane_off + TM_S + sb * 64u + h * 32u, sv);
+        const int vb = mine ? clamp_vbs(p.vbs[j]) : 0;  // visible columns of the row
+        uint32_t sv[64];
+        tmem_ld_32x32b_x32(t_s, sv);
+        tmem_ld_32x32b_x32(t_s + 32u, sv + 32);
         tmem_wait_ld();
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(S_FREE0 + sb));
-        float mloc = -INFINITY;
+        if (lane == 0) mbar_arrive(bar(S_FREE0 + grp));
+        float mb = -INFINITY;  // the row's maximum over this kv block
 #pragma unroll
-        for (int u = 0; u < 32; ++u)
-          if (u < vb) mloc = fmaxf(mloc, __uint_as_float(sv[u]) * c1);
-        float mo;
-        if (!exchange(mloc, &mo)) return false;
-        const float mb = fmaxf(mloc, mo);  // the row's maximum over this kv block
+        for (int u = 0; u < 64; ++u)
+          if (u < vb) mb = fmaxf(mb, __uint_as_float(sv[u]) * c1);
         const bool need = mb > m + RESCALE;
-        // P buffer sb is free once P.V of block t-2 has completed; from then on P.V of block
-        // t-1 is the only one that can still be accumulating into O.
-        if (!warp_wait(bar(P_FREE0 + sb), ((t >> 1) & 1u) ^ 1u, abort, lane)) return false;
+        // P buffer grp is free once the group's previous P.V has completed, and then O_grp
+        // holds every block of the group so far.
+        if (!warp_wait(bar(P_FREE0 + grp), ((tb >> 1) & 1u) ^ 1u, abort, lane)) return false;
         if (__any_sync(0xffffffffu, need)) {
           const float f = need ? ex2(m - mb) : 1.f;  // m = -inf: f = 0 (nothing accumulated)
           if (!first) {
-            if (!warp_wait(bar(PV_DONE), (t - 1) & 1u, abort, lane)) return false;
             tc_fence_after_sync();
 #pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < 4; ++c) {
               uint32_t ov[32];
-              const uint32_t ta = tmem + lane_off + TM_O + h * 64u + c * 32u;
-              tmem_ld_32x32b_x32(ta, ov);
+              tmem_ld_32x32b_x32(t_o + c * 32u, ov);
               tmem_wait_ld();
 #pragma unroll
               for (int u = 0; u < 32; ++u) ov[u] = __float_as_uint(__uint_as_float(ov[u]) * f);
-              tmem_st_32x32b_x32(ta, ov);
+              tmem_st_32x32b_x32(t_o + c * 32u, ov);
             }
             tmem_wait_st();
           }
@@ -465,58 +510,84 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (need) m = mb;
         }
         const float off = static_cast<float>(KPF) - m;
-        uint32_t pk[16];
+        uint32_t pk[32];
         float acc = 0.f;
 #pragma unroll
-        for (int u = 0; u < 32; u += 2) {
+        for (int u = 0; u < 64; u += 2) {
           const float p0 = (u < vb) ? ex2(fmaf(__uint_as_float(sv[u]), c1, off)) : 0.f;
           const float p1 = (u + 1 < vb) ? ex2(fmaf(__uint_as_float(sv[u + 1]), c1, off)) : 0.f;
           acc += p0 + p1;
           pk[u >> 1] = pack_half2(p0, p1);
         }
         l += acc;
-        tmem_st_32x32b_x16(tmem + lane_off + TM_P + sb * 32u + h * 16u, pk);
+        tmem_st_32x32b_x32(t_p, pk);
         tmem_wait_st();
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(P_READY0 + sb));
-        ++t;
+        if (lane == 0) mbar_arrive(bar(P_READY0 + grp));
         first = false;
         return true;
       });
-      float lo = 0.f;
-      if (!ok || !exchange(l, &lo)) {
+      if (!ok) {
         if (lane == 0) raise_abort(abort, p.err);
         break;
       }
-      const float lt = l + lo;
+      // Merge the two groups' partial results of each row.  Slots alternate with the item, so a
+      // slot is rewritten only after the partner warp passed the next exchange, i.e. read it.
+      float2* slot = xch + (itc & 1u) * 256u;
+      slot[grp * 128 + r] = make_float2(m, l);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(XCH0 + quarter));
+      if (!warp_wait(bar(XCH0 + quarter), itc & 1u, abort, lane)) {
+        if (lane == 0) raise_abort(abort, p.err);
+        break;
+      }
+      __syncwarp();
+      const float2 mo = slot[(1 - grp) * 128 + r];
       if (!warp_wait(bar(O_FULL), itc & 1u, abort, lane)) {
         if (lane == 0) raise_abort(abort, p.err);
         break;
       }
       tc_fence_after_sync();
-      uint32_t v[64];  // O columns h*64 .. h*64+63 of row r
-      tmem_ld_32x32b_x32(tmem + lane_off + TM_O + h * 64u, v);
-      tmem_ld_32x32b_x32(tmem + lane_off + TM_O + h * 64u + 32u, v + 32);
-      tmem_wait_ld();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(O_EMPTY));
-      if (valid) {
-        // O = (sum P 2^KPF V') 2^ev / (sum P 2^KPF); an empty row (lt = 0) gives O = 0 and
-        // lse = -inf.
-        const float os = lt > 0.f ? exp2i(ev) / lt : 0.f;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const int u = 8 * c;
-          orow[c] = make_uint4(
-              pack_bf162(__uint_as_float(v[u]) * os, __uint_as_float(v[u + 1]) * os),
-              pack_bf162(__uint_as_float(v[u + 2]) * os, __uint_as_float(v[u + 3]) * os),
-              pack_bf162(__uint_as_float(v[u + 4]) * os, __uint_as_float(v[u + 5]) * os),
-              pack_bf162(__uint_as_float(v[u + 6]) * os, __uint_as_float(v[u + 7]) * os));
+      const float m0 = grp == 0 ? m : mo.x, l0 = grp == 0 ? l : mo.y;
+      const float m1 = grp == 0 ? mo.x : m, l1 = grp == 0 ? mo.y : l;
+      const float mm = fmaxf(m0, m1);
+      // A group without any visible column (l = 0; also one without blocks: its O buffer
+      // holds stale data) gets weight 0 and its O is not read.
+      const float w0 = l0 > 0.f ? ex2(m0 - mm) : 0.f, w1 = l1 > 0.f ? ex2(m1 - mm) : 0.f;
+      const float lt = w0 * l0 + w1 * l1;
+      const float os = lt > 0.f ? exp2i(ev) / lt : 0.f;
+      const float a0 = w0 * os, a1 = w1 * os;
+      // This warp writes O columns grp*64 .. grp*64+63 of row r, from both groups' buffers.
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        uint32_t v0[32], v1[32];
+        const uint32_t col = TM_O + grp * 64u + c * 32u;
+        tmem_ld_32x32b_x32(tmem + lane_off + col, v0);
+        tmem_ld_32x32b_x32(tmem + lane_off + col + 128u, v1);
+        tmem_wait_ld();
+        if (c == 1) {
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(O_EMPTY));
         }
-        if (h == 0) p.lse[grow] = lt > 0.f ? m + log2f(lt) - static_cast<float>(KPF) : -INFINITY;
+        if (valid) {
+#pragma unroll
+          for (int u = 0; u < 32; u += 8) {
+            float o8[8];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+              const float f0 = a0 != 0.f ? __uint_as_float(v0[u + x]) * a0 : 0.f;
+              const float f1 = a1 != 0.f ? __uint_as_float(v1[u + x]) * a1 : 0.f;
+              o8[x] = f0 + f1;
+            }
+            orow[c * 4 + u / 8] = make_uint4(pack_bf162(o8[0], o8[1]), pack_bf162(o8[2], o8[3]),
+                                             pack_bf162(o8[4], o8[5]), pack_bf162(o8[6], o8[7]));
+          }
+        }
       }
+      if (valid && grp == 0)
+        p.lse[grow] = lt > 0.f ? mm + log2f(lt) - static_cast<float>(KPF) : -INFINITY;
       ++itc;
     }
   }

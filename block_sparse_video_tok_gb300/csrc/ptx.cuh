@@ -69,6 +69,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// mbar_wait_bounded for a converged warp in which every lane polls: true only if the phase
+// completed for all lanes.  Cheaper for the issuing warp of a pipeline than one lane waiting and
+// broadcasting the result.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort,
+                                               uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abort, limit_ns));
+}
+
 // ------------------------------------------------------------------------------ proxy fences
 
 // Generic-proxy writes to shared memory become visible to the async proxy (UMMA, TMA).
@@ -190,6 +198,44 @@ __device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, ui
         "r"(a_tmem), "l"(b_desc), "r"(idesc)
         : "memory");
   }
+}
+
+// The same UMMAs issued from a converged warp: every lane calls with identical operands and one
+// lane, chosen by elect.sync, issues.  Keeping the issuing role warp-uniform lets the operands
+// live in uniform registers instead of being moved there before every instruction.
+template <bool ACCUMULATE>
+__device__ __forceinline__ void umma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred e, a;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 a, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, a;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "n"(ACCUMULATE ? 1 : 0)
+      : "memory");
+}
+
+template <bool ACCUMULATE>
+__device__ __forceinline__ void umma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred e, a;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 a, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, a;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "n"(ACCUMULATE ? 1 : 0)
+      : "memory");
+}
+
+// umma_commit from a converged warp, by the lane elect.sync chooses (the lowest active lane,
+// the same one that issued the UMMAs above).
+__device__ __forceinline__ void umma_commit_elect(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          bar)
+      : "memory");
 }
 
 // Advance a shared-memory descriptor's start address by `bytes` (a multiple of 16).  The start
