@@ -70,8 +70,10 @@ enum Bar : uint32_t {
   QDO_FULL1,
   QDO_EMPTY0,
   QDO_EMPTY1,
-  SDP_FULL,
-  P_READY,
+  S_FULL,    // S of the step is in TMEM
+  DP_FULL,   // dP of the step is in TMEM
+  P_READY,   // the softmax warps have stored P of the step
+  DS_READY,  // ... and dS
   PDS_FREE0,
   PDS_FREE1,
   DQ_FULL0,
@@ -193,8 +195,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(bar(DQ_FULL0 + s), 1);
       mbar_init(bar(DQ_FREE0 + s), 4);
     }
-    mbar_init(bar(SDP_FULL), 1);
+    mbar_init(bar(S_FULL), 1);
+    mbar_init(bar(DP_FULL), 1);
     mbar_init(bar(P_READY), SOFTMAX_WARPS);
+    mbar_init(bar(DS_READY), SOFTMAX_WARPS);
     mbar_init(bar(ACC_FULL), 1);
     mbar_init(bar(ACC_EMPTY), 4);
     mbar_init(bar(DRAIN), 1);
@@ -331,6 +335,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         umma_ss_elect<true>(t_s, sdesc_advance(qa, off),
                          sdesc_advance(k_kmaj, (kk >> 2) * 8192u + (kk & 3) * 32u), IDESC_SDP);
       }
+      umma_commit_elect(bar(S_FULL));
       umma_ss_elect<false>(t_dp, da, v_kmaj, IDESC_SDP);
 #pragma unroll
       for (int kk = 1; kk < 8; ++kk) {
@@ -338,7 +343,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         umma_ss_elect<true>(t_dp, sdesc_advance(da, off),
                          sdesc_advance(v_kmaj, (kk >> 2) * 8192u + (kk & 3) * 32u), IDESC_SDP);
       }
-      umma_commit_elect(bar(SDP_FULL));
+      umma_commit_elect(bar(DP_FULL));
     };
     // dQ^T = K_j^T dS^T of step gs into TMEM buffer gs & 1; then its P/dS buffer is free.
     auto issue_dq = [&](uint32_t gs) -> bool {
@@ -357,11 +362,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       umma_commit_elect(bar(PDS_FREE0 + b));
       return true;
     };
-    // dV^T += dO_p^T P and dK^T += Q_p^T dS of step gs; the first step of an item overwrites.
-    auto issue_dvdk = [&](uint32_t gs, bool first) {
-      const uint32_t so = (gs & 1u) * 32768u;
-      const uint64_t da = sdesc_advance(do_mn, so), qa = sdesc_advance(q_mn, so);
-      const uint64_t dsb = sdesc_advance(ds_mn, (gs & 1u) * 16384u);
+    // dV^T += dO_p^T P of step gs; the first step of an item overwrites.
+    auto issue_dv = [&](uint32_t gs, bool first) {
+      const uint64_t da = sdesc_advance(do_mn, (gs & 1u) * 32768u);
       if (first)
         umma_ss_elect<false>(t_dv, da, p_mn, IDESC_DVK);
       else
@@ -370,6 +373,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int kk = 1; kk < 8; ++kk)
         umma_ss_elect<true>(t_dv, sdesc_advance(da, kk * 2048u), sdesc_advance(p_mn, kk * 2048u),
                          IDESC_DVK);
+    };
+    // dK^T += Q_p^T dS of step gs; the first step of an item overwrites.
+    auto issue_dk = [&](uint32_t gs, bool first) {
+      const uint64_t qa = sdesc_advance(q_mn, (gs & 1u) * 32768u);
+      const uint64_t dsb = sdesc_advance(ds_mn, (gs & 1u) * 16384u);
       if (first)
         umma_ss_elect<false>(t_dk, qa, dsb, IDESC_DVK);
       else
@@ -400,7 +408,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         tc_fence_after_sync();
-        // The softmax finished reading S/dP(g-1) before it arrived on P_READY(g-1).
+        // The softmax finished reading S/dP(g-1) before it arrived on DS_READY(g-1).  In the
+        // tensor pipe S(g) follows dV(g-1), so the softmax may overwrite P once S(g) is done.
         issue_sdp(g);
         issued = true;
         if (pp > 0 && !issue_dq(g - 1)) {
@@ -417,7 +426,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         tc_fence_after_sync();
-        issue_dvdk(g, pp == 0);
+        issue_dv(g, pp == 0);
+        if (!mbar_wait_warp(bar(DS_READY), g & 1u, abort, WAIT_LIMIT_NS)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        issue_dk(g, pp == 0);
         umma_commit_elect(bar(QDO_EMPTY0 + s));  // Q_p and dO_p of step g are no longer read
       }
       if (!ok) break;
@@ -470,41 +485,59 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const float nlse = static_cast<float>(KP) - p.lse[grow];
         const float dl = p.delta[grow] * dscale;  // Delta in the units of dP' = dO'.V'
         const bool full = valid && (vb == BLOCK);
-        if (!warp_wait(bar(SDP_FULL), g & 1u, abort, lane)) {
+        // Phase 1: P from S, as soon as S is in TMEM (dP and dQ^T(g-1) are still running).
+        if (!warp_wait(bar(S_FULL), g & 1u, abort, lane)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         const uint32_t prow = base + SM_P + static_cast<uint32_t>(r) * 128u;
         const uint32_t dsrow = base + SM_DS + s * 16384u + static_cast<uint32_t>(r) * 128u;
+        float pv[32];  // P of this warp's 32 columns (0 where masked), kept for dS
         {
-          uint32_t sv[32], dpv[32];
+          uint32_t sv[32];
           tmem_ld_32x32b_x32(tmem + lane_off + TM_S + h * 32u, sv);
-          tmem_ld_32x32b_x32(tmem + lane_off + TM_DP + h * 32u, dpv);
           tmem_wait_ld();
-          uint32_t pk[16], dk[16];  // P and dS of this warp's 32 columns, fp16 pairs
+          uint32_t pk[16];
           if (full) {  // every column visible: no masking
 #pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-              const float p0 = ex2(fmaf(__uint_as_float(sv[c]), c1, nlse));
-              const float p1 = ex2(fmaf(__uint_as_float(sv[c + 1]), c1, nlse));
-              pk[c >> 1] = pack_half2(p0, p1);
-              dk[c >> 1] = pack_half2(p0 * (__uint_as_float(dpv[c]) - dl),
-                                      p1 * (__uint_as_float(dpv[c + 1]) - dl));
-            }
+            for (int c = 0; c < 32; ++c) pv[c] = ex2(fmaf(__uint_as_float(sv[c]), c1, nlse));
           } else {
 #pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-              const int u = h * 32 + c;
-              const bool v0 = valid && (u < vb), v1 = valid && (u + 1 < vb);
-              const float p0 = v0 ? ex2(fmaf(__uint_as_float(sv[c]), c1, nlse)) : 0.f;
-              const float p1 = v1 ? ex2(fmaf(__uint_as_float(sv[c + 1]), c1, nlse)) : 0.f;
-              const float d0 = p0 * (__uint_as_float(dpv[c]) - dl);
-              const float d1 = p1 * (__uint_as_float(dpv[c + 1]) - dl);
-              pk[c >> 1] = pack_half2(p0, p1);
-              dk[c >> 1] = pack_half2(v0 ? d0 : 0.f, v1 ? d1 : 0.f);
-            }
+            for (int c = 0; c < 32; ++c)
+              pv[c] = (valid && h * 32 + c < vb) ? ex2(fmaf(__uint_as_float(sv[c]), c1, nlse)) : 0.f;
           }
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) pk[c >> 1] = pack_half2(pv[c], pv[c + 1]);
+          // P's buffer was last read by dV^T(g-1), which precedes S(g) in the tensor pipe.
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            const uint32_t phys = ((static_cast<uint32_t>(h * 4 + ch)) ^ sw) * 16u;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + phys),
+                         "r"(pk[4 * ch]), "r"(pk[4 * ch + 1]), "r"(pk[4 * ch + 2]),
+                         "r"(pk[4 * ch + 3])
+                         : "memory");
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(P_READY));
+        // Phase 2: dS = P (dP - Delta) while dV^T(g) runs.
+        if (!warp_wait(bar(DP_FULL), g & 1u, abort, lane)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        {
+          uint32_t dpv[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + TM_DP + h * 32u, dpv);
+          tmem_wait_ld();
+          uint32_t dk[16];  // dS, fp16 pairs (masked columns have P = 0, so dS = 0 exactly)
+#pragma unroll
+          for (int c = 0; c < 32; c += 2)
+            dk[c >> 1] = pack_half2(pv[c] * (__uint_as_float(dpv[c]) - dl),
+                                    pv[c + 1] * (__uint_as_float(dpv[c + 1]) - dl));
           // The buffer's previous contents (step g-2) must have been consumed by dQ^T(g-2).
           if (!warp_wait(bar(PDS_FREE0 + s), ((g >> 1) & 1u) ^ 1u, abort, lane)) {
             ok = false;
@@ -513,21 +546,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
             const uint32_t phys = ((static_cast<uint32_t>(h * 4 + ch)) ^ sw) * 16u;
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + phys),
-                         "r"(pk[4 * ch]), "r"(pk[4 * ch + 1]), "r"(pk[4 * ch + 2]),
-                         "r"(pk[4 * ch + 3])
-                         : "memory");
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dsrow + phys),
                          "r"(dk[4 * ch]), "r"(dk[4 * ch + 1]), "r"(dk[4 * ch + 2]),
                          "r"(dk[4 * ch + 3])
                          : "memory");
           }
         }
-        if (!ok) break;
         fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(P_READY));
+        if (lane == 0) mbar_arrive(bar(DS_READY));
       }
       if (!ok) {
         if (lane == 0) raise_abort(abort, p.err);
