@@ -60,7 +60,7 @@ constexpr uint32_t SM_Q = 32768;                // 2 stages x 2 chunks x [128 q 
 constexpr uint32_t SM_DO = SM_Q + 2 * 32768;    // 2 stages, same layout
 constexpr uint32_t SM_P = SM_DO + 2 * 32768;    // [128 q x 128 B]
 constexpr uint32_t SM_DS = SM_P + 16384;        // 2 buffers x [128 q x 128 B]
-constexpr uint32_t SM_STG = SM_DS + 2 * 16384;  // dQ staging: 4 warps x [32 q x 32 fp32]
+constexpr uint32_t SM_STG = SM_DS + 2 * 16384;  // dQ staging: 4 warps x 2 x [16 q x 32 fp32]
 constexpr uint32_t SM_BAR = SM_STG + 4 * 4096;  // mbarriers
 
 enum Bar : uint32_t {
@@ -324,24 +324,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint64_t ds_kmaj = sdesc_sw128(base + SM_DS, 16, 1024);
     const uint32_t t_s = tmem + TM_S, t_dp = tmem + TM_DP, t_dv = tmem + TM_DVT,
                    t_dk = tmem + TM_DKT;
-    // S = Q_p K_j^T and dP = dO_p V_j^T of step gs (stage gs & 1).
-    auto issue_sdp = [&](uint32_t gs) {
-      const uint32_t so = (gs & 1u) * 32768u;
-      const uint64_t qa = sdesc_advance(q_kmaj, so), da = sdesc_advance(do_kmaj, so);
+    // S = Q_p K_j^T of step gs (stage gs & 1).
+    auto issue_s = [&](uint32_t gs) {
+      const uint64_t qa = sdesc_advance(q_kmaj, (gs & 1u) * 32768u);
       umma_ss_elect<false>(t_s, qa, k_kmaj, IDESC_SDP);
 #pragma unroll
       for (int kk = 1; kk < 8; ++kk) {
         const uint32_t off = (kk >> 2) * 16384u + (kk & 3) * 32u;
         umma_ss_elect<true>(t_s, sdesc_advance(qa, off),
-                         sdesc_advance(k_kmaj, (kk >> 2) * 8192u + (kk & 3) * 32u), IDESC_SDP);
+                            sdesc_advance(k_kmaj, (kk >> 2) * 8192u + (kk & 3) * 32u), IDESC_SDP);
       }
       umma_commit_elect(bar(S_FULL));
+    };
+    // dP = dO_p V_j^T of step gs.
+    auto issue_dp = [&](uint32_t gs) {
+      const uint64_t da = sdesc_advance(do_kmaj, (gs & 1u) * 32768u);
       umma_ss_elect<false>(t_dp, da, v_kmaj, IDESC_SDP);
 #pragma unroll
       for (int kk = 1; kk < 8; ++kk) {
         const uint32_t off = (kk >> 2) * 16384u + (kk & 3) * 32u;
         umma_ss_elect<true>(t_dp, sdesc_advance(da, off),
-                         sdesc_advance(v_kmaj, (kk >> 2) * 8192u + (kk & 3) * 32u), IDESC_SDP);
+                            sdesc_advance(v_kmaj, (kk >> 2) * 8192u + (kk & 3) * 32u), IDESC_SDP);
       }
       umma_commit_elect(bar(DP_FULL));
     };
@@ -401,21 +404,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ok = false;
         break;
       }
+      // The tensor pipe runs, per step g of the item:  dV^T(g)  S(g+1)  dK^T(g)  dP(g+1)  dQ^T(g),
+      // so the softmax of step g+1 (which needs S(g+1), then dP(g+1)) overlaps dK^T, dP and
+      // dQ^T of step g.  S and dP of the item's first step go in up front.
+      const uint32_t g0 = g;
+      if (!mbar_wait_warp(bar(QDO_FULL0 + (g0 & 1u)), (g0 >> 1) & 1u, abort, WAIT_LIMIT_NS)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      issue_s(g0);
+      issue_dp(g0);
+      issued = true;
       for (int pp = 0; pp < np; ++pp, ++g) {
-        const uint32_t s = g & 1u;
-        if (!mbar_wait_warp(bar(QDO_FULL0 + s), (g >> 1) & 1u, abort, WAIT_LIMIT_NS)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        // The softmax finished reading S/dP(g-1) before it arrived on DS_READY(g-1).  In the
-        // tensor pipe S(g) follows dV(g-1), so the softmax may overwrite P once S(g) is done.
-        issue_sdp(g);
-        issued = true;
-        if (pp > 0 && !issue_dq(g - 1)) {
-          ok = false;
-          break;
-        }
+        const bool more = pp + 1 < np;
+        // The softmax read S(g) before P_READY(g); P(g) is in shared memory.
         if (!mbar_wait_warp(bar(P_READY), g & 1u, abort, WAIT_LIMIT_NS)) {
           ok = false;
           break;
@@ -427,19 +430,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after_sync();
         issue_dv(g, pp == 0);
+        if (more) {
+          // S(g+1) overwrites S(g), already read.  P(g+1) is written by the softmax only once
+          // S(g+1) is done, which in the tensor pipe follows dV^T(g).
+          if (!mbar_wait_warp(bar(QDO_FULL0 + ((g + 1) & 1u)), ((g + 1) >> 1) & 1u, abort,
+                              WAIT_LIMIT_NS)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          issue_s(g + 1);
+        }
+        // The softmax read dP(g) before DS_READY(g); dS(g) is in shared memory.
         if (!mbar_wait_warp(bar(DS_READY), g & 1u, abort, WAIT_LIMIT_NS)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         issue_dk(g, pp == 0);
-        umma_commit_elect(bar(QDO_EMPTY0 + s));  // Q_p and dO_p of step g are no longer read
+        umma_commit_elect(bar(QDO_EMPTY0 + (g & 1u)));  // Q_p and dO_p of step g are no longer read
+        if (more) issue_dp(g + 1);
+        if (!issue_dq(g)) {
+          ok = false;
+          break;
+        }
       }
       if (!ok) break;
-      if (!issue_dq(g - 1)) {
-        ok = false;
-        break;
-      }
       umma_commit_elect(bar(ACC_FULL));
       umma_commit_elect(bar(KV_EMPTY));
       ++itc;
@@ -608,37 +624,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after_sync();
         // Four 32-column chunks of dQ^T: chunks 0, 1 are rows 0-31, 32-63 of q block i0,
-        // chunks 2, 3 those of i1.  Each goes TMEM -> registers -> this warp's staging box
+        // chunks 2, 3 those of i1.  Each goes TMEM -> registers -> this warp's staging area
         // (row q: 32 fp32 of head dims 32*wq .. 32*wq+31, so the 32 lanes' stores of one row
-        // are 128 contiguous bytes) -> one TMA reduce-add into the accumulator.
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem + lane_off + TM_DQT + buf * 128u + c * 32u, v);
-          tmem_wait_ld();
-          if (c == 3) {  // the TMEM buffer is free once all four chunks are in registers
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(DQ_FREE0 + buf));
-          }
-          if (c >= 2 && !has2) continue;
-          if (lane == 0) bulk_wait_read_all();  // the previous box has left the staging area
-          __syncwarp();
+        // are 128 contiguous bytes) -> TMA reduce-adds into the accumulator, one per half of
+        // 16 rows.  The load of chunk c+1 is in flight while chunk c is staged, and each half
+        // of the staging area is rewritten as soon as the reduce that last read it is done.
+        auto stage = [&](const uint32_t* v, int c) {
+          if (c >= 2 && !has2) return;
+          const int row0 = it.bh * S + ((c < 2) ? i0 : i1) * BLOCK + (c & 1) * 32;
 #pragma unroll
-          for (int q = 0; q < 32; ++q)
-            asm volatile("st.shared.b32 [%0], %1;" ::"r"(stg + static_cast<uint32_t>(q) * 128u +
-                                                          static_cast<uint32_t>(lane) * 4u),
-                         "r"(v[q])
-                         : "memory");
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            const int qb = (c < 2) ? i0 : i1;
-            tma_reduce_add_2d(&tm_dq, stg, wq * 32,
-                              it.bh * S + qb * BLOCK + (c & 1) * 32);
-            bulk_commit_group();
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint32_t st = stg + static_cast<uint32_t>(hh) * 2048u;
+            if (lane == 0) bulk_wait_read<1>();  // the reduce before last has read this half
+            __syncwarp();
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+              asm volatile("st.shared.b32 [%0], %1;" ::"r"(st + static_cast<uint32_t>(q) * 128u +
+                                                            static_cast<uint32_t>(lane) * 4u),
+                           "r"(v[hh * 16 + q])
+                           : "memory");
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_reduce_add_2d(&tm_dq, st, wq * 32, row0 + hh * 16);
+              bulk_commit_group();
+            }
           }
-        }
+        };
+        const uint32_t tq = tmem + lane_off + TM_DQT + buf * 128u;
+        uint32_t va[32], vb[32];
+        tmem_ld_32x32b_x32(tq, va);
+        tmem_wait_ld_regs(va);
+        tmem_ld_32x32b_x32(tq + 32u, vb);
+        stage(va, 0);
+        tmem_wait_ld_regs(vb);
+        tmem_ld_32x32b_x32(tq + 64u, va);
+        stage(vb, 1);
+        tmem_wait_ld_regs(va);
+        tmem_ld_32x32b_x32(tq + 96u, vb);
+        stage(va, 2);
+        tmem_wait_ld_regs(vb);
+        // The TMEM buffer is free once all four chunks are in registers.
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(DQ_FREE0 + buf));
+        stage(vb, 3);
       }
       if (!ok) {
         if (lane == 0) raise_abort(abort, p.err);
@@ -700,13 +730,13 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return encode;
 }
 
-// [rows, 128] fp32 (the dQ accumulator), box 32 columns x 32 rows, no swizzle.
+// [rows, 128] fp32 (the dQ accumulator), box 32 columns x 16 rows, no swizzle.
 cudaError_t make_tmap_rows128_f32(CUtensorMap* map, const void* ptr, long rows) {
   auto encode = tensor_map_encoder();
   if (!encode) return cudaErrorNotSupported;
   const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(HEAD_DIM), static_cast<cuuint64_t>(rows)};
   const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(HEAD_DIM) * sizeof(float)};
-  const cuuint32_t box[2] = {32u, 32u};
+  const cuuint32_t box[2] = {32u, 16u};
   const cuuint32_t estride[2] = {1u, 1u};
   CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), gdim,
                       gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
