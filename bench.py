@@ -37,7 +37,9 @@ if ROOT not in sys.path:
 
 FLOP_PER_PAIR = 5 * 2 * 64 * 64 * 128
 METRIC = "bwd TFLOPS on selected blocks (5 GEMMs/pair) and % of BF16 tensor peak, 1 GB300"
-PAGES_TFLOPS = {"32k_25pct": 794.0, "4k_25pct": 381.0}   # sm_100a kernel on the pages (GB200)
+# The sm_100a kernel's published TFLOPS at the same shapes (B=1, H=8, D=128, 25 % density).
+PAGES_TFLOPS = {"4k_25pct": 381.0, "32k_25pct": 794.0, "131k_25pct": 736.0, "262k_25pct": 784.0,
+                "524k_25pct": 771.0}
 
 
 def parse():
@@ -306,7 +308,8 @@ def main():
     torch.cuda.set_device(device)
     stream = torch.cuda.current_stream()
 
-    cfg = dict(wl.CONFIGS[args.config])
+    cfg = dict(wl.CONFIGS[args.config] if args.config in wl.CONFIGS else
+               wl.LONG_CONFIGS[args.config])
     case = wl.make_config(args.config, seed=cfg["seed"] + rank)
     B, H, S, nb = case["B"], case["H"], case["S"], case["nb"]
     pairs = wl.selected_pairs(case["q2k_idx"], case["q2k_num"], nb)

@@ -2,77 +2,76 @@
 // block_sparse_attn_backward_sm100a: "k2q_idx, k2q_num = invert_indices(...)"; the row order is
 // ascending as in the compare page's tests, invert_indices_torch).
 //
-// One CTA per (head, 32-column slice of kv blocks).  Phase 1 scans the head's q2k rows and sets
+// One CTA per (head, slice of kv-block columns).  Phase 1 scans the head's q2k rows and sets
 // bit i of column j in a shared-memory bitmap (column-major: one run of nq bits per kv block), so
-// duplicate ids collapse and the set semantics come for free.  Phase 2 gives each warp whole
+// duplicate ids collapse and the set semantics come for free.  Every slice rescans the head's q2k,
+// so slices are as wide as shared memory allows while the grid still fills about two waves of
+// SMs: 32 columns at 32k tokens, about 200 at 524k.  Phase 2 gives each warp whole
 // columns: lane l owns 32-bit word l (and l+32, ...) of the column, a warp prefix sum of the
 // popcounts gives every lane its output offset, and the lane writes its set bits in ascending
 // order.  The result is deterministic (no atomics decide positions) and rows come out sorted.
-// HBM traffic per head: q2k read once per slice (L2-resident), k2q written once.
+// Traffic per head: q2k read once per slice (from L2), k2q written once.
 #include "vsa_internal.cuh"
 
 namespace vsa {
 
 namespace {
 
-constexpr int INV_COLS = 32;     // kv blocks per CTA
-constexpr int INV_THREADS = 256;
+constexpr int INV_MIN_COLS = 32;  // kv blocks per CTA, at least (unless shared memory is short)
+constexpr int INV_THREADS = 1024;  // 32 warps: many q2k rows in flight per CTA
+constexpr size_t INV_SMEM_CAP = 200 * 1024;
 
 __global__ void __launch_bounds__(INV_THREADS) invert_kernel(const int32_t* __restrict__ q2k_idx,
                                                              const int32_t* __restrict__ q2k_num,
-                                                             int topk, int nb,
+                                                             int topk, int nb, int cols,
                                                              int32_t* __restrict__ k2q_idx,
                                                              int32_t* __restrict__ k2q_num,
                                                              uint32_t* err) {
-  extern __shared__ uint32_t bm[];  // [INV_COLS][words]
+  extern __shared__ uint32_t bm[];  // [cols][words]
   const int nq = nb;
   const int words = (nq + 31) >> 5;
   const int bh = blockIdx.x;
-  const int j0 = blockIdx.y * INV_COLS;
-  const int ncols = min(INV_COLS, nb - j0);
+  const int j0 = blockIdx.y * cols;
+  const int ncols = min(cols, nb - j0);
 
-  for (int x = threadIdx.x; x < INV_COLS * words; x += blockDim.x) bm[x] = 0u;
+  for (int x = threadIdx.x; x < cols * words; x += blockDim.x) bm[x] = 0u;
   __syncthreads();
 
   uint32_t bad = 0;
   const int32_t* idx = q2k_idx + static_cast<size_t>(bh) * nq * topk;
   const int32_t* num = q2k_num + static_cast<size_t>(bh) * nq;
-  const int entries = nq * topk;
-  // Sixteen independent loads per thread before any is used, so the scan is not bound by one
-  // L2 round trip per entry.
-  constexpr int U = 16;
-  for (int e0 = 0; e0 < entries; e0 += U * INV_THREADS) {
-    int jv[U], cv[U], sv[U], iv[U];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  // One warp per q2k row: coalesced loads of the row's active prefix, four in flight per lane.
+  for (int i = warp; i < nq; i += nwarps) {
+    const int c = num[i];
+    const int cnt = c < 0 ? 0 : (c > topk ? topk : c);
+    if (cnt != c) bad |= VSA_DEVERR_Q2K_COUNT;
+    const int32_t* row = idx + static_cast<size_t>(i) * topk;
+    const uint32_t bit = 1u << (i & 31);
+    for (int s0 = 0; s0 < cnt; s0 += 4 * 32) {
+      int jv[4];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int e = e0 + u * INV_THREADS + static_cast<int>(threadIdx.x);
-      const bool in = e < entries;
-      const int i = in ? e / topk : 0;
-      iv[u] = i;
-      sv[u] = in ? e - i * topk : topk;  // topk: never an active slot
-      jv[u] = in ? idx[e] : 0;
-      cv[u] = in ? num[i] : 0;
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int c = cv[u];
-      const int cnt = c < 0 ? 0 : (c > topk ? topk : c);
-      if (sv[u] == 0 && cnt != c) bad |= VSA_DEVERR_Q2K_COUNT;
-      if (sv[u] >= cnt) continue;
-      const int j = jv[u];
-      if (j < 0 || j >= nb) {
-        bad |= VSA_DEVERR_Q2K_ID;
-        continue;
+      for (int u = 0; u < 4; ++u) {
+        const int s = s0 + u * 32 + lane;
+        jv[u] = s < cnt ? row[s] : 0;  // unused: lanes past the count skip it below
       }
-      const int jj = j - j0;
-      if (jj >= 0 && jj < ncols) atomicOr(&bm[jj * words + (iv[u] >> 5)], 1u << (iv[u] & 31));
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (s0 + u * 32 + lane >= cnt) continue;
+        const int j = jv[u];
+        if (j < 0 || j >= nb) {
+          bad |= VSA_DEVERR_Q2K_ID;
+          continue;
+        }
+        const int jj = j - j0;
+        if (jj >= 0 && jj < ncols) atomicOr(&bm[jj * words + (i >> 5)], bit);
+      }
     }
   }
   // Report invalid entries once per head (the first slice sees all of them).
   if (bad && blockIdx.y == 0 && err) atomicOr(err, bad);
   __syncthreads();
 
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   for (int jj = warp; jj < ncols; jj += nwarps) {
     const int j = j0 + jj;
     int32_t* out = k2q_idx + (static_cast<size_t>(bh) * nb + j) * nq;
@@ -105,16 +104,25 @@ __global__ void __launch_bounds__(INV_THREADS) invert_kernel(const int32_t* __re
 cudaError_t launch_invert(const int32_t* q2k_idx, const int32_t* q2k_num, int topk, int BH,
                           int nb, int32_t* k2q_idx, int32_t* k2q_num, uint32_t* err,
                           cudaStream_t stream) {
-  const int words = (nb + 31) / 32;
-  const size_t smem = static_cast<size_t>(INV_COLS) * words * sizeof(uint32_t);
+  const size_t col_bytes = static_cast<size_t>((nb + 31) / 32) * sizeof(uint32_t);
+  // Widest slice shared memory holds, but no wider than two waves of CTAs need.
+  const long fit = static_cast<long>(INV_SMEM_CAP / col_bytes);
+  const long two_waves = (static_cast<long>(BH) * nb + 2L * device_sm_count() - 1) /
+                         (2L * device_sm_count());
+  long cols = two_waves > INV_MIN_COLS ? two_waves : INV_MIN_COLS;
+  if (cols > fit) cols = fit;
+  if (cols > nb) cols = nb;
+  if (cols < 1) return cudaErrorInvalidValue;  // nb beyond 1.6 M blocks: a column exceeds smem
+  const size_t smem = static_cast<size_t>(cols) * col_bytes;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(invert_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>((nb + INV_COLS - 1) / INV_COLS));
-  invert_kernel<<<grid, INV_THREADS, smem, stream>>>(q2k_idx, q2k_num, topk, nb, k2q_idx,
-                                                      k2q_num, err);
+  dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>((nb + cols - 1) / cols));
+  invert_kernel<<<grid, INV_THREADS, smem, stream>>>(q2k_idx, q2k_num, topk, nb,
+                                                      static_cast<int>(cols), k2q_idx, k2q_num,
+                                                      err);
   return cudaGetLastError();
 }
 

@@ -36,6 +36,16 @@ CONFIGS = {
                                seed=0),
 }
 
+# Long sequences at 25 % density (B=1, H=8, D=128), the shapes of the sm_100a kernel's published
+# table beyond 65k tokens.  Benchmark workloads only: their inputs take several GB to draw.
+LONG_CONFIGS = {
+    "131k_25pct": dict(B=1, H=8, nb=2048, topk=512, select="uniform", vbs="full", seed=0),
+    "262k_25pct": dict(B=1, H=8, nb=4096, topk=1024, select="uniform", vbs="full", seed=0),
+    "524k_25pct": dict(B=1, H=8, nb=8192, topk=2048, select="uniform", vbs="full", seed=0),
+    # 524k tokens at low density: long-sequence index arithmetic at a size the oracle can sample.
+    "524k_sparse": dict(B=1, H=2, nb=8192, topk=16, select="uniform", vbs="ragged33", seed=0),
+}
+
 VIDEO_GRID = (21, 30, 52)
 VIDEO_CUBE = (4, 4, 4)
 
@@ -60,8 +70,15 @@ def _select(rng, kind, B, H, nb, topk, kv_pool=None):
     if kind == "uniform":
         pool = np.arange(nb) if kv_pool is None else np.asarray(kv_pool)
         assert topk <= pool.size
-        keys = rng.random((rows, pool.size))
-        pick = pool[np.argsort(keys, axis=1, kind="stable")[:, :topk]]
+        # The topk smallest of uniform keys per row; rows in chunks so the keys of long sequences
+        # never sit in memory at once (the draws are the same as one (rows, pool) call).
+        pick = np.empty((rows, topk), np.int64)
+        chunk = max(1, (1 << 24) // pool.size)
+        for r0 in range(0, rows, chunk):
+            keys = rng.random((min(chunk, rows - r0), pool.size))
+            part = np.argpartition(keys, topk - 1, axis=1)[:, :topk] if topk < pool.size else \
+                np.argsort(keys, axis=1)
+            pick[r0:r0 + keys.shape[0]] = pool[part]
     elif kind == "zipf":
         pick = np.empty((rows, topk), np.int64)
         n_zero = int(round(0.05 * nb))
@@ -117,8 +134,14 @@ def make_case(B, H, nb, topk, select="uniform", vbs="full", seed=0, kv_pool=None
     return case
 
 
+def make_selection(B, H, nb, topk, select="uniform", seed=0):
+    """Only a q2k selection (int32 [B,H,nb,topk], counts all topk), from its own generator."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return _select(rng, select, B, H, nb, topk), np.full((B, H, nb), topk, np.int32)
+
+
 def make_config(name, seed=None):
-    cfg = dict(CONFIGS[name])
+    cfg = dict(CONFIGS[name] if name in CONFIGS else LONG_CONFIGS[name])
     if seed is not None:
         cfg["seed"] = seed
     return make_case(cfg["B"], cfg["H"], cfg["nb"], cfg["topk"], cfg["select"], cfg["vbs"],

@@ -55,6 +55,23 @@ def test_invert_bit_exact_on_workloads(vsa, name):
     assert int(err.item()) == 0
 
 
+@pytest.mark.parametrize("H,nb,topk", [(2, 8192, 16), (8, 4096, 16), (2, 2048, 256),
+                                        (2, 333, 100)])
+def test_invert_bit_exact_long(vsa, H, nb, topk):
+    """Long sequences, where the inversion's column slices are wider than 32 kv blocks, and an
+    odd nb.  (The oracle's plain membership scan bounds nb * nb * topk here.)"""
+    q2k_idx, q2k_num = wl.make_selection(1, H, nb, topk, seed=nb + topk)
+    k_idx, k_num, bad = orc.invert(q2k_idx, q2k_num, nb)
+    assert bad == 0
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g_idx, g_num = vsa.vsa_invert_indices(torch.from_numpy(q2k_idx).cuda(),
+                                          torch.from_numpy(q2k_num).cuda(), nb, dev_err=err)
+    torch.cuda.synchronize()
+    assert np.array_equal(g_num.cpu().numpy(), k_num)
+    assert np.array_equal(g_idx.cpu().numpy(), k_idx)
+    assert int(err.item()) == 0
+
+
 @pytest.mark.parametrize("seed", [0, 1])
 def test_invert_invalid_entries(vsa, seed):
     rng = np.random.default_rng(seed)
@@ -273,6 +290,12 @@ def _full_size(vsa, name, n_heads=2, n_q=3, n_kv=2, seed=0):
 @pytest.mark.parametrize("name", ["32k_25pct", "65k_12pct_zipf", "video_dit_21x30x52"])
 def test_full_size_sampled(vsa, name):
     _full_size(vsa, name)
+
+
+def test_long_sequence_sampled(vsa):
+    """524,288 tokens (8192 kv blocks, so the work order is sorted) at low density: sampled
+    parity of O, lse, dQ, dK and dV, and exact zeros for unselected kv blocks."""
+    _full_size(vsa, "524k_sparse")
 
 
 def test_two_runs_agree_at_65k(vsa):
