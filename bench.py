@@ -427,6 +427,31 @@ def main():
     e2e_ms = reduce_max(dist, e0.elapsed_time(e1), device) / K_e2e
     e2e_value = all_pairs * FLOP_PER_PAIR / (e2e_ms / 1e3) / 1e12
 
+    # A training step through the autograd binding: forward, then inversion and backward.
+    from block_sparse_video_tok_gb300.autograd import block_sparse_attention
+    qg, kg, vg = (dev[n].clone().requires_grad_(True) for n in ("q", "k", "v"))
+
+    def train_step():
+        for t in (qg, kg, vg):
+            t.grad = None
+        block_sparse_attention(qg, kg, vg, q2k_idx, q2k_num, vbs, sc).backward(dev["do"])
+
+    for _ in range(3):
+        train_step()
+    torch.cuda.synchronize()
+    K_train = max(3, min(K, 20))
+    t0_, t1_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist, device)
+    torch.cuda.synchronize()
+    t0_.record(stream)
+    for _ in range(K_train):
+        train_step()
+    t1_.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist, device)
+    train_ms = reduce_max(dist, t0_.elapsed_time(t1_), device) / K_train
+    train_tflops = all_pairs * FLOP_PER_PAIR * 7 / 5 / (train_ms / 1e3) / 1e12
+
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -461,6 +486,9 @@ def main():
                      "peak_source": "%s bf16_tflops (burst); fp16 dense rate = bf16" % peak_src,
                      "frac_of_sustained": achieved / peak_sus},
         "fwd": {"ms": fwd_ms, "note": "operand producer, timed alone; not in the step"},
+        "train_step": {"ms": train_ms, "tflops": train_tflops, "steps": K_train,
+                       "note": "forward + inversion + backward through the autograd binding; "
+                               "2 + 5 GEMMs per selected pair"},
         "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": K_e2e},
         "gpu_launches": kernels_per_step * K,

@@ -16,7 +16,8 @@ Selection patterns (all rows hold distinct kv block ids, sorted ascending, count
            weights (Gumbel top-k), which makes k2q list lengths strongly skewed;
   scores   top-k of uniform random block scores (the video-DiT selection).
 Block-size patterns: full (all 64), last40 (all 64, last block 40), ragged (uniform integers in
-[lo, 64]), cubes (a latent video grid tiled into 4x4x4 cubes, clipped at the grid edges).
+[lo, 64]), cubes (a latent video grid tiled into 4x4x4 cubes, clipped at the grid edges;
+"cubes:TxHxW" names the grid, plain "cubes" is 21x30x52).
 """
 import math
 
@@ -44,6 +45,12 @@ LONG_CONFIGS = {
     "524k_25pct": dict(B=1, H=8, nb=8192, topk=2048, select="uniform", vbs="full", seed=0),
     # 524k tokens at low density: long-sequence index arithmetic at a size the oracle can sample.
     "524k_sparse": dict(B=1, H=2, nb=8192, topk=16, select="uniform", vbs="ragged33", seed=0),
+    # Wan2.1-1.3B-like layers (12 heads of 128): an 81-frame 480P latent (21 x 60 x 104) and a
+    # 720P one (21 x 90 x 160) in 4x4x4 cubes, each q block attending to 12.5 % of the cubes.
+    "wan480p_h12": dict(B=1, H=12, nb=2340, topk=293, select="scores", vbs="cubes:21x60x104",
+                        seed=0),
+    "wan720p_h12": dict(B=1, H=12, nb=5520, topk=690, select="scores", vbs="cubes:21x90x160",
+                        seed=0),
 }
 
 VIDEO_GRID = (21, 30, 52)
@@ -90,8 +97,14 @@ def _select(rng, kind, B, H, nb, topk, kv_pool=None):
             keys = logw[None, :] + g
             pick[bh * nb:(bh + 1) * nb] = np.argsort(-keys, axis=1, kind="stable")[:, :topk]
     elif kind == "scores":
-        scores = rng.random((rows, nb))
-        pick = np.argsort(-scores, axis=1, kind="stable")[:, :topk]
+        # The topk largest of uniform scores per row, in row chunks like "uniform".
+        pick = np.empty((rows, topk), np.int64)
+        chunk = max(1, (1 << 24) // nb)
+        for r0 in range(0, rows, chunk):
+            scores = rng.random((min(chunk, rows - r0), nb))
+            pick[r0:r0 + scores.shape[0]] = (
+                np.argpartition(-scores, topk - 1, axis=1)[:, :topk] if topk < nb else
+                np.argsort(-scores, axis=1))
     else:
         raise ValueError(kind)
     pick = np.sort(pick, axis=1).astype(np.int32)
@@ -108,8 +121,9 @@ def _block_sizes(rng, kind, nb):
     if kind.startswith("ragged"):
         lo = int(kind[len("ragged"):])
         return rng.integers(lo, BLOCK + 1, size=nb).astype(np.int32)
-    if kind == "cubes":
-        v = video_cube_sizes()
+    if kind.startswith("cubes"):
+        grid = VIDEO_GRID if kind == "cubes" else tuple(int(x) for x in kind[6:].split("x"))
+        v = video_cube_sizes(grid)
         assert v.size == nb, (v.size, nb)
         return v
     raise ValueError(kind)
