@@ -59,9 +59,9 @@ constexpr uint32_t SM_V = 16384;                // V_j
 constexpr uint32_t SM_Q = 32768;                // 2 stages x 2 chunks x [128 q x 128 B]
 constexpr uint32_t SM_DO = SM_Q + 2 * 32768;    // 2 stages, same layout
 constexpr uint32_t SM_P = SM_DO + 2 * 32768;    // [128 q x 128 B]
-constexpr uint32_t SM_DS = SM_P + 16384;        // 2 buffers x [128 q x 128 B]
-constexpr uint32_t SM_STG = SM_DS + 2 * 16384;  // dQ staging: 4 warps x 2 x [16 q x 32 fp32]
-constexpr uint32_t SM_BAR = SM_STG + 4 * 4096;  // mbarriers
+constexpr uint32_t SM_DS = SM_P + 16384;        // [128 q x 128 B]
+constexpr uint32_t SM_STG = SM_DS + 16384;      // dQ staging: 4 warps x [64 q x 32 fp32]
+constexpr uint32_t SM_BAR = SM_STG + 4 * 8192;  // mbarriers
 
 enum Bar : uint32_t {
   KV_FULL = 0,
@@ -74,8 +74,7 @@ enum Bar : uint32_t {
   DP_FULL,   // dP of the step is in TMEM
   P_READY,   // the softmax warps have stored P of the step
   DS_READY,  // ... and dS
-  PDS_FREE0,
-  PDS_FREE1,
+  DS_FREE,   // dQ^T of the previous step has read dS
   DQ_FULL0,
   DQ_FULL1,
   DQ_FREE0,
@@ -191,7 +190,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(QDO_FULL0 + s), 1);
       mbar_init(bar(QDO_EMPTY0 + s), 1);
-      mbar_init(bar(PDS_FREE0 + s), 1);
       mbar_init(bar(DQ_FULL0 + s), 1);
       mbar_init(bar(DQ_FREE0 + s), 4);
     }
@@ -202,6 +200,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(bar(ACC_FULL), 1);
     mbar_init(bar(ACC_EMPTY), 4);
     mbar_init(bar(DRAIN), 1);
+    mbar_init(bar(DS_FREE), 1);
     for (int s = 0; s < ITEM_SLOTS; ++s) {
       mbar_init(bar(ITEM_FULL0 + s), 1);
       mbar_init(bar(ITEM_EMPTY0 + s), ITEM_CONSUMERS);
@@ -226,81 +225,87 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == TMA_WARP) {
     // ------------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      uint32_t g = 0;      // global pair-step counter
-      uint32_t itc = 0;    // items with a non-empty list
-      uint32_t kv_loads = 0;
-      int64_t last_g[2] = {-1, -1};
-      bool ok = true;
-      // Items are handed out dynamically: the next one is claimed from the global counter once
-      // the loads of the current one are issued, so the CTAs that finish early take more.
-      for (uint32_t k = 0;; ++k) {
-        int w;
-        if (!publish_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, p.sched, abort, &w)) {
-          ok = false;
-          break;
-        }
-        if (w >= p.total) break;  // the end marker
-        const Item it = decode_item(p, w);
-        const int raw_n = p.k2q_num[p.order ? p.order[w] : w];
-        uint32_t bad = 0;
-        if (raw_n != it.n) bad |= VSA_DEVERR_K2Q_COUNT;
+    // The whole warp runs this role; lane 0 claims items and registers the expected bytes, and
+    // each tile of a load goes out from a lane of its own (a thread's bulk copies are processed
+    // one after another, so spreading them over lanes keeps them in flight together).
+    uint32_t g = 0;      // global pair-step counter
+    uint32_t itc = 0;    // items with a non-empty list
+    uint32_t kv_loads = 0;
+    int64_t last_g[2] = {-1, -1};
+    bool ok = true;
+    // Items are handed out dynamically: the next one is claimed from the global counter once
+    // the loads of the current one are issued, so the CTAs that finish early take more.
+    for (uint32_t k = 0;; ++k) {
+      int w = 0, okp = 1;
+      if (lane == 0)
+        okp = publish_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, p.sched, abort, &w) ? 1
+                                                                                             : 0;
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (!__shfl_sync(0xffffffffu, okp, 0)) {
+        ok = false;
+        break;
+      }
+      if (w >= p.total) break;  // the end marker
+      const Item it = decode_item(p, w);
+      uint32_t bad = 0;
+      if (lane == 0) {
+        if (p.k2q_num[p.order ? p.order[w] : w] != it.n) bad |= VSA_DEVERR_K2Q_COUNT;
         const int vb = p.vbs[it.j];
         if (vb != clamp_vbs(vb)) bad |= VSA_DEVERR_VBS;
-        for (int x = 0; x < it.n; ++x) {
-          const int i = it.list[x];
-          if (i < 0 || i >= nq) bad |= VSA_DEVERR_K2Q_ID;
-        }
-        if (bad) atomicOr(p.err, bad);
-        if (it.n == 0) continue;
-        if (!mbar_wait_bounded(bar(KV_EMPTY), (itc & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) {
+      }
+      for (int x = lane; x < it.n; x += 32) {
+        const int i = it.list[x];
+        if (i < 0 || i >= nq) bad |= VSA_DEVERR_K2Q_ID;
+      }
+      bad = __reduce_or_sync(0xffffffffu, bad);
+      if (bad && lane == 0) atomicOr(p.err, bad);
+      if (it.n == 0) continue;
+      if (!mbar_wait_warp(bar(KV_EMPTY), (itc & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) {
+        ok = false;
+        break;
+      }
+      const int row_kv = it.bh * S + it.j * BLOCK;
+      if (lane == 0) mbar_arrive_expect_tx(bar(KV_FULL), 32768);
+      __syncwarp();
+      if (lane < 4)  // lanes 0, 1: K chunks; 2, 3: V chunks
+        tma_load_2d(base + ((lane < 2) ? SM_K : SM_V) + (lane & 1) * 8192u,
+                    (lane < 2) ? &tm_k : &tm_v, bar(KV_FULL), (lane & 1) * 64, row_kv);
+      ++kv_loads;
+      const int np = (it.n + 1) >> 1;
+      for (int pp = 0; pp < np; ++pp, ++g) {
+        const uint32_t s = g & 1u;
+        if (!mbar_wait_warp(bar(QDO_EMPTY0 + s), ((g >> 1) & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) {
           ok = false;
           break;
         }
-        const int row_kv = it.bh * S + it.j * BLOCK;
-        mbar_arrive_expect_tx(bar(KV_FULL), 32768);
-        tma_load_2d(base + SM_K, &tm_k, bar(KV_FULL), 0, row_kv);
-        tma_load_2d(base + SM_K + 8192, &tm_k, bar(KV_FULL), 64, row_kv);
-        tma_load_2d(base + SM_V, &tm_v, bar(KV_FULL), 0, row_kv);
-        tma_load_2d(base + SM_V + 8192, &tm_v, bar(KV_FULL), 64, row_kv);
-        ++kv_loads;
-        const int np = (it.n + 1) >> 1;
-        for (int pp = 0; pp < np; ++pp, ++g) {
-          const uint32_t s = g & 1u;
-          if (!mbar_wait_bounded(bar(QDO_EMPTY0 + s), ((g >> 1) & 1u) ^ 1u, abort,
-                                 WAIT_LIMIT_NS)) {
-            ok = false;
-            break;
-          }
-          const int i0 = q_block(it, 2 * pp, nq);
-          const int i1 = (2 * pp + 1 < it.n) ? q_block(it, 2 * pp + 1, nq) : i0;
-          const int r0 = it.bh * S + i0 * BLOCK, r1 = it.bh * S + i1 * BLOCK;
-          const uint32_t qs = base + SM_Q + s * 32768u, ds = base + SM_DO + s * 32768u;
-          mbar_arrive_expect_tx(bar(QDO_FULL0 + s), 65536);
-          tma_load_2d(qs, &tm_q, bar(QDO_FULL0 + s), 0, r0);
-          tma_load_2d(qs + 8192, &tm_q, bar(QDO_FULL0 + s), 0, r1);
-          tma_load_2d(qs + 16384, &tm_q, bar(QDO_FULL0 + s), 64, r0);
-          tma_load_2d(qs + 24576, &tm_q, bar(QDO_FULL0 + s), 64, r1);
-          tma_load_2d(ds, &tm_do, bar(QDO_FULL0 + s), 0, r0);
-          tma_load_2d(ds + 8192, &tm_do, bar(QDO_FULL0 + s), 0, r1);
-          tma_load_2d(ds + 16384, &tm_do, bar(QDO_FULL0 + s), 64, r0);
-          tma_load_2d(ds + 24576, &tm_do, bar(QDO_FULL0 + s), 64, r1);
-          last_g[s] = g;
+        const int i0 = q_block(it, 2 * pp, nq);
+        const int i1 = (2 * pp + 1 < it.n) ? q_block(it, 2 * pp + 1, nq) : i0;
+        const int r0 = it.bh * S + i0 * BLOCK, r1 = it.bh * S + i1 * BLOCK;
+        if (lane == 0) mbar_arrive_expect_tx(bar(QDO_FULL0 + s), 65536);
+        __syncwarp();
+        if (lane < 8) {
+          // Lanes 0-3: Q, 4-7: dO.  Tile t = lane & 3 sits at byte t * 8192 of the stage:
+          // (cols 0-63, block i0), (cols 0-63, i1), (cols 64-127, i0), (cols 64-127, i1).
+          const uint32_t t = static_cast<uint32_t>(lane & 3);
+          tma_load_2d(base + ((lane < 4) ? SM_Q : SM_DO) + s * 32768u + t * 8192u,
+                      (lane < 4) ? &tm_q : &tm_do, bar(QDO_FULL0 + s), (t & 2u) ? 64 : 0,
+                      (t & 1u) ? r1 : r0);
         }
-        if (!ok) break;
-        ++itc;
+        last_g[s] = g;
       }
-      if (!ok) {
-        raise_abort(abort, p.err);
-        // Let the copies already issued land before the CTA's shared memory goes away.
-        volatile int never = 0;
-        if (kv_loads > 0)
-          mbar_wait_bounded(bar(KV_FULL), (kv_loads - 1) & 1u, &never, DRAIN_LIMIT_NS);
-        for (int s = 0; s < 2; ++s)
-          if (last_g[s] >= 0)
-            mbar_wait_bounded(bar(QDO_FULL0 + s), (static_cast<uint32_t>(last_g[s]) >> 1) & 1u,
-                              &never, DRAIN_LIMIT_NS);
-      }
+      if (!ok) break;
+      ++itc;
+    }
+    if (!ok && lane == 0) {
+      raise_abort(abort, p.err);
+      // Let the copies already issued land before the CTA's shared memory goes away.
+      volatile int never = 0;
+      if (kv_loads > 0)
+        mbar_wait_bounded(bar(KV_FULL), (kv_loads - 1) & 1u, &never, DRAIN_LIMIT_NS);
+      for (int s = 0; s < 2; ++s)
+        if (last_g[s] >= 0)
+          mbar_wait_bounded(bar(QDO_FULL0 + s), (static_cast<uint32_t>(last_g[s]) >> 1) & 1u,
+                            &never, DRAIN_LIMIT_NS);
     }
     __syncwarp();
   } else if (warp == MMA_WARP) {
@@ -348,13 +353,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       umma_commit_elect(bar(DP_FULL));
     };
-    // dQ^T = K_j^T dS^T of step gs into TMEM buffer gs & 1; then its P/dS buffer is free.
+    // dQ^T = K_j^T dS^T of step gs into TMEM buffer gs & 1; then the dS buffer is free.
     auto issue_dq = [&](uint32_t gs) -> bool {
       const uint32_t b = gs & 1u;
       if (!mbar_wait_warp(bar(DQ_FREE0 + b), ((gs >> 1) & 1u) ^ 1u, abort, WAIT_LIMIT_NS))
         return false;
       tc_fence_after_sync();
-      const uint64_t dsb = sdesc_advance(ds_kmaj, b * 16384u);
+      const uint64_t dsb = ds_kmaj;
       const uint32_t t_dq = tmem + TM_DQT + b * 128u;
       umma_ss_elect<false>(t_dq, k_mn, dsb, IDESC_DQ);
 #pragma unroll
@@ -362,7 +367,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         umma_ss_elect<true>(t_dq, sdesc_advance(k_mn, kk * 2048u), sdesc_advance(dsb, kk * 32u),
                          IDESC_DQ);
       umma_commit_elect(bar(DQ_FULL0 + b));
-      umma_commit_elect(bar(PDS_FREE0 + b));
+      umma_commit_elect(bar(DS_FREE));
       return true;
     };
     // dV^T += dO_p^T P of step gs; the first step of an item overwrites.
@@ -380,7 +385,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // dK^T += Q_p^T dS of step gs; the first step of an item overwrites.
     auto issue_dk = [&](uint32_t gs, bool first) {
       const uint64_t qa = sdesc_advance(q_mn, (gs & 1u) * 32768u);
-      const uint64_t dsb = sdesc_advance(ds_mn, (gs & 1u) * 16384u);
+      const uint64_t dsb = ds_mn;
       if (first)
         umma_ss_elect<false>(t_dk, qa, dsb, IDESC_DVK);
       else
@@ -493,7 +498,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int np = (it.n + 1) >> 1;
       bool ok = true;
       for (int pp = 0; pp < np; ++pp, ++g) {
-        const uint32_t s = g & 1u;
         const bool has2 = (2 * pp + 1 < it.n);
         const bool valid = (r < 64) || has2;
         const int qb = q_block(it, 2 * pp + ((r >= 64 && has2) ? 1 : 0), nq);
@@ -508,7 +512,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after_sync();
         const uint32_t prow = base + SM_P + static_cast<uint32_t>(r) * 128u;
-        const uint32_t dsrow = base + SM_DS + s * 16384u + static_cast<uint32_t>(r) * 128u;
+        const uint32_t dsrow = base + SM_DS + static_cast<uint32_t>(r) * 128u;
         float pv[32];  // P of this warp's 32 columns (0 where masked), kept for dS
         {
           uint32_t sv[32];
@@ -554,8 +558,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int c = 0; c < 32; c += 2)
             dk[c >> 1] = pack_half2(pv[c] * (__uint_as_float(dpv[c]) - dl),
                                     pv[c + 1] * (__uint_as_float(dpv[c + 1]) - dl));
-          // The buffer's previous contents (step g-2) must have been consumed by dQ^T(g-2).
-          if (!warp_wait(bar(PDS_FREE0 + s), ((g >> 1) & 1u) ^ 1u, abort, lane)) {
+          // The buffer's previous contents (step g-1) must have been consumed by dQ^T(g-1).
+          if (!warp_wait(bar(DS_FREE), (g & 1u) ^ 1u, abort, lane)) {
             ok = false;
             break;
           }
@@ -582,7 +586,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------------ dQ drain + epilogue
     const int wq = warp - DRAIN_WARP0;  // lane quarter (DRAIN_WARP0 % 4 == 0)
     const int d = wq * 32 + lane;  // head-dim row == TMEM lane (dK/dV epilogue column)
-    const uint32_t stg = base + SM_STG + static_cast<uint32_t>(wq) * 4096u;
+    const uint32_t stg = base + SM_STG + static_cast<uint32_t>(wq) * 8192u;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     uint32_t g = 0, itc = 0;
     for (uint32_t k = 0;; ++k) {
@@ -624,29 +628,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after_sync();
         // Four 32-column chunks of dQ^T: chunks 0, 1 are rows 0-31, 32-63 of q block i0,
-        // chunks 2, 3 those of i1.  Each goes TMEM -> registers -> this warp's staging area
+        // chunks 2, 3 those of i1.  Each goes TMEM -> registers -> this warp's staging box
         // (row q: 32 fp32 of head dims 32*wq .. 32*wq+31, so the 32 lanes' stores of one row
-        // are 128 contiguous bytes) -> TMA reduce-adds into the accumulator, one per half of
-        // 16 rows.  The load of chunk c+1 is in flight while chunk c is staged, and each half
-        // of the staging area is rewritten as soon as the reduce that last read it is done.
+        // are 128 contiguous bytes).  A q block's two chunks fill the box (64 rows, 8 KB), which
+        // one TMA reduce adds into the accumulator: a thread's bulk requests are processed one
+        // after another, so few large requests move more than many small ones.  The load of
+        // chunk c+1 is in flight while chunk c is staged.
         auto stage = [&](const uint32_t* v, int c) {
           if (c >= 2 && !has2) return;
-          const int row0 = it.bh * S + ((c < 2) ? i0 : i1) * BLOCK + (c & 1) * 32;
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const uint32_t st = stg + static_cast<uint32_t>(hh) * 2048u;
-            if (lane == 0) bulk_wait_read<1>();  // the reduce before last has read this half
+          const uint32_t rows = stg + static_cast<uint32_t>(c & 1) * 4096u;
+          if ((c & 1) == 0) {
+            if (lane == 0) bulk_wait_read<0>();  // the previous reduce has read the box
             __syncwarp();
+          }
 #pragma unroll
-            for (int q = 0; q < 16; ++q)
-              asm volatile("st.shared.b32 [%0], %1;" ::"r"(st + static_cast<uint32_t>(q) * 128u +
-                                                            static_cast<uint32_t>(lane) * 4u),
-                           "r"(v[hh * 16 + q])
-                           : "memory");
+          for (int q = 0; q < 32; ++q)
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(rows + static_cast<uint32_t>(q) * 128u +
+                                                          static_cast<uint32_t>(lane) * 4u),
+                         "r"(v[q])
+                         : "memory");
+          if (c & 1) {
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_reduce_add_2d(&tm_dq, st, wq * 32, row0 + hh * 16);
+              tma_reduce_add_2d(&tm_dq, stg, wq * 32, it.bh * S + ((c < 2) ? i0 : i1) * BLOCK);
               bulk_commit_group();
             }
           }
@@ -730,13 +735,13 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return encode;
 }
 
-// [rows, 128] fp32 (the dQ accumulator), box 32 columns x 16 rows, no swizzle.
+// [rows, 128] fp32 (the dQ accumulator), box 32 columns x 64 rows, no swizzle.
 cudaError_t make_tmap_rows128_f32(CUtensorMap* map, const void* ptr, long rows) {
   auto encode = tensor_map_encoder();
   if (!encode) return cudaErrorNotSupported;
   const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(HEAD_DIM), static_cast<cuuint64_t>(rows)};
   const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(HEAD_DIM) * sizeof(float)};
-  const cuuint32_t box[2] = {32u, 16u};
+  const cuuint32_t box[2] = {32u, 64u};
   const cuuint32_t estride[2] = {1u, 1u};
   CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), gdim,
                       gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
