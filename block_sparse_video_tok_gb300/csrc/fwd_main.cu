@@ -228,106 +228,106 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == TMA_WARP) {
     // ------------------------------------------------------------------ TMA producer: Q, K
-    if (lane == 0) {
-      uint32_t lg = 0, itc = 0;  // kv blocks loaded; items with a non-empty union
-      int64_t last_lg[K_STAGES], last_q[2] = {-1, -1};
-      for (int s = 0; s < K_STAGES; ++s) last_lg[s] = -1;
-      bool ok = true;
-      for (uint32_t k = 0;; ++k) {
-        int w;
-        if (!publish_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, p.sched, abort, &w)) {
-          ok = false;
-          break;
-        }
-        if (w >= p.total) break;  // the end marker
-        const Pair q = decode_pair(p, w);
-        if (union_size(p, q) == 0) continue;
-        const uint32_t qs = itc & 1u;
-        if (!mbar_wait_bounded(bar(Q_EMPTY0 + qs), ((itc >> 1) & 1u) ^ 1u, abort,
-                               WAIT_LIMIT_NS)) {
-          ok = false;
-          break;
-        }
-        const int r0 = q.bh * S + q.i0 * BLOCK;
-        const int r1 = q.bh * S + (q.i1 >= 0 ? q.i1 : q.i0) * BLOCK;
-        const uint32_t qd = base + SM_Q + qs * 32768u;
-        mbar_arrive_expect_tx(bar(Q_FULL0 + qs), 32768);
-        tma_load_2d(qd, &tm_q, bar(Q_FULL0 + qs), 0, r0);
-        tma_load_2d(qd + 8192, &tm_q, bar(Q_FULL0 + qs), 0, r1);
-        tma_load_2d(qd + 16384, &tm_q, bar(Q_FULL0 + qs), 64, r0);
-        tma_load_2d(qd + 24576, &tm_q, bar(Q_FULL0 + qs), 64, r1);
-        last_q[qs] = itc;
-        ok = for_union(p, q, [&](int j) {
-          const uint32_t st = lg % K_STAGES;
-          if (!mbar_wait_bounded(bar(K_EMPTY0 + st), ((lg / K_STAGES) & 1u) ^ 1u, abort,
-                                 WAIT_LIMIT_NS))
-            return false;
-          const int rk = q.bh * S + j * BLOCK;
-          const uint32_t kd = base + SM_K + st * 16384u;
-          mbar_arrive_expect_tx(bar(K_FULL0 + st), 16384u);
-          tma_load_2d(kd, &tm_k, bar(K_FULL0 + st), 0, rk);
-          tma_load_2d(kd + 8192, &tm_k, bar(K_FULL0 + st), 64, rk);
-          last_lg[st] = lg;
-          ++lg;
-          return true;
-        });
-        if (!ok) break;
-        ++itc;
+    // Warp-wide: lane 0 claims items and registers the expected bytes; each tile goes out from
+    // a lane of its own (a thread's bulk copies are processed one after another).
+    uint32_t lg = 0, itc = 0;  // kv blocks loaded; items with a non-empty union
+    int64_t last_lg[K_STAGES], last_q[2] = {-1, -1};
+    for (int s = 0; s < K_STAGES; ++s) last_lg[s] = -1;
+    bool ok = true;
+    for (uint32_t k = 0;; ++k) {
+      int w = 0, okp = 1;
+      if (lane == 0)
+        okp = publish_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, p.sched, abort, &w) ? 1
+                                                                                             : 0;
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (!__shfl_sync(0xffffffffu, okp, 0)) {
+        ok = false;
+        break;
       }
-      if (!ok) {
-        raise_abort(abort, p.err);
-        // Let the copies already issued land before the CTA's shared memory goes away.
-        volatile int never = 0;
-        for (int s = 0; s < 2; ++s)
-          if (last_q[s] >= 0)
-            mbar_wait_bounded(bar(Q_FULL0 + s), (static_cast<uint32_t>(last_q[s]) >> 1) & 1u,
-                              &never, DRAIN_LIMIT_NS);
-        for (int s = 0; s < K_STAGES; ++s)
-          if (last_lg[s] >= 0)
-            mbar_wait_bounded(bar(K_FULL0 + s), (static_cast<uint32_t>(last_lg[s]) / K_STAGES) & 1u,
-                              &never, DRAIN_LIMIT_NS);
+      if (w >= p.total) break;  // the end marker
+      const Pair q = decode_pair(p, w);
+      if (union_size(p, q) == 0) continue;
+      const uint32_t qs = itc & 1u;
+      if (!mbar_wait_warp(bar(Q_EMPTY0 + qs), ((itc >> 1) & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) {
+        ok = false;
+        break;
       }
+      const int r0 = q.bh * S + q.i0 * BLOCK;
+      const int r1 = q.bh * S + (q.i1 >= 0 ? q.i1 : q.i0) * BLOCK;
+      if (lane == 0) mbar_arrive_expect_tx(bar(Q_FULL0 + qs), 32768);
+      __syncwarp();
+      if (lane < 4)  // tile t = lane at byte t * 8192: (cols 0-63, i0), (0-63, i1), (64-127, i0), ...
+        tma_load_2d(base + SM_Q + qs * 32768u + static_cast<uint32_t>(lane) * 8192u, &tm_q,
+                    bar(Q_FULL0 + qs), (lane & 2) ? 64 : 0, (lane & 1) ? r1 : r0);
+      last_q[qs] = itc;
+      ok = for_union(p, q, [&](int j) {
+        const uint32_t st = lg % K_STAGES;
+        if (!mbar_wait_warp(bar(K_EMPTY0 + st), ((lg / K_STAGES) & 1u) ^ 1u, abort,
+                            WAIT_LIMIT_NS))
+          return false;
+        if (lane == 0) mbar_arrive_expect_tx(bar(K_FULL0 + st), 16384u);
+        __syncwarp();
+        if (lane < 2)
+          tma_load_2d(base + SM_K + st * 16384u + static_cast<uint32_t>(lane) * 8192u, &tm_k,
+                      bar(K_FULL0 + st), lane * 64, q.bh * S + j * BLOCK);
+        last_lg[st] = lg;
+        ++lg;
+        return true;
+      });
+      if (!ok) break;
+      ++itc;
+    }
+    if (!ok && lane == 0) {
+      raise_abort(abort, p.err);
+      // Let the copies already issued land before the CTA's shared memory goes away.
+      volatile int never = 0;
+      for (int s = 0; s < 2; ++s)
+        if (last_q[s] >= 0)
+          mbar_wait_bounded(bar(Q_FULL0 + s), (static_cast<uint32_t>(last_q[s]) >> 1) & 1u,
+                            &never, DRAIN_LIMIT_NS);
+      for (int s = 0; s < K_STAGES; ++s)
+        if (last_lg[s] >= 0)
+          mbar_wait_bounded(bar(K_FULL0 + s), (static_cast<uint32_t>(last_lg[s]) / K_STAGES) & 1u,
+                            &never, DRAIN_LIMIT_NS);
     }
     __syncwarp();
   } else if (warp == V_WARP) {
     // ------------------------------------------------------------------ TMA producer: V
-    if (lane == 0) {
-      uint32_t lg = 0;
-      int64_t last_lg[V_STAGES];
-      for (int s = 0; s < V_STAGES; ++s) last_lg[s] = -1;
-      bool ok = true;
-      for (uint32_t k = 0;; ++k) {
-        int w;
-        if (!take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, &w)) {
-          ok = false;
-          break;
-        }
-        if (w >= p.total) break;
-        const Pair q = decode_pair(p, w);
-        ok = for_union(p, q, [&](int j) {
-          const uint32_t st = lg % V_STAGES;
-          if (!mbar_wait_bounded(bar(V_EMPTY0 + st), ((lg / V_STAGES) & 1u) ^ 1u, abort,
-                                 WAIT_LIMIT_NS))
-            return false;
-          const int rk = q.bh * S + j * BLOCK;
-          const uint32_t vd = base + SM_V + st * 16384u;
-          mbar_arrive_expect_tx(bar(V_FULL0 + st), 16384u);
-          tma_load_2d(vd, &tm_v, bar(V_FULL0 + st), 0, rk);
-          tma_load_2d(vd + 8192, &tm_v, bar(V_FULL0 + st), 64, rk);
-          last_lg[st] = lg;
-          ++lg;
-          return true;
-        });
-        if (!ok) break;
+    uint32_t lg = 0;
+    int64_t last_lg[V_STAGES];
+    for (int s = 0; s < V_STAGES; ++s) last_lg[s] = -1;
+    bool ok = true;
+    for (uint32_t k = 0;; ++k) {
+      int w;
+      if (!warp_take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, lane, &w)) {
+        ok = false;
+        break;
       }
-      if (!ok) {
-        raise_abort(abort, p.err);
-        volatile int never = 0;
-        for (int s = 0; s < V_STAGES; ++s)
-          if (last_lg[s] >= 0)
-            mbar_wait_bounded(bar(V_FULL0 + s), (static_cast<uint32_t>(last_lg[s]) / V_STAGES) & 1u,
-                              &never, DRAIN_LIMIT_NS);
-      }
+      if (w >= p.total) break;
+      const Pair q = decode_pair(p, w);
+      ok = for_union(p, q, [&](int j) {
+        const uint32_t st = lg % V_STAGES;
+        if (!mbar_wait_warp(bar(V_EMPTY0 + st), ((lg / V_STAGES) & 1u) ^ 1u, abort,
+                            WAIT_LIMIT_NS))
+          return false;
+        if (lane == 0) mbar_arrive_expect_tx(bar(V_FULL0 + st), 16384u);
+        __syncwarp();
+        if (lane < 2)
+          tma_load_2d(base + SM_V + st * 16384u + static_cast<uint32_t>(lane) * 8192u, &tm_v,
+                      bar(V_FULL0 + st), lane * 64, q.bh * S + j * BLOCK);
+        last_lg[st] = lg;
+        ++lg;
+        return true;
+      });
+      if (!ok) break;
+    }
+    if (!ok && lane == 0) {
+      raise_abort(abort, p.err);
+      volatile int never = 0;
+      for (int s = 0; s < V_STAGES; ++s)
+        if (last_lg[s] >= 0)
+          mbar_wait_bounded(bar(V_FULL0 + s), (static_cast<uint32_t>(last_lg[s]) / V_STAGES) & 1u,
+                            &never, DRAIN_LIMIT_NS);
     }
     __syncwarp();
   } else if (warp == MMA_WARP) {
