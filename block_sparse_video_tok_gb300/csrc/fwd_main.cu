@@ -44,14 +44,14 @@ constexpr int SOFTMAX_WARPS = 8;
 constexpr int TMA_WARP = 8;
 constexpr int MMA_WARP = 9;
 constexpr int V_WARP = 10;
-constexpr int K_STAGES = 4;
+constexpr int K_STAGES = 2;  // stages of a PAIR of kv blocks (32 KB each)
 constexpr int V_STAGES = 5;
 constexpr int KPF = 7;               // P is carried as P * 2^KPF: below 2^(RESCALE + KPF) = 2^15
 constexpr float RESCALE = 8.0f;      // log2 units the block maximum may exceed m by before a rescale
 
 constexpr uint32_t SM_Q = 0;                         // 2 stages x 2 chunks x [128 q x 128 B]
-constexpr uint32_t SM_K = 2 * 32768;                 // K stages x 2 chunks x [64 kv x 128 B]
-constexpr uint32_t SM_V = SM_K + K_STAGES * 16384;   // V stages, same layout
+constexpr uint32_t SM_K = 2 * 32768;                 // K pair stages x 2 chunks x [128 kv x 128 B]
+constexpr uint32_t SM_V = SM_K + K_STAGES * 32768;   // V stages x 2 chunks x [64 kv x 128 B]
 constexpr uint32_t SM_XCH = SM_V + V_STAGES * 16384;  // [2 parity][2 groups][128 rows] (m, l)
 constexpr uint32_t SM_BAR = SM_XCH + 2 * 2 * 128 * 8;
 
@@ -62,9 +62,9 @@ enum Bar : uint32_t {
   K_EMPTY0 = K_FULL0 + K_STAGES,
   V_FULL0 = K_EMPTY0 + K_STAGES,
   V_EMPTY0 = V_FULL0 + V_STAGES,
-  S_FULL0 = V_EMPTY0 + V_STAGES,
-  S_FREE0 = S_FULL0 + 2,
-  P_READY0 = S_FREE0 + 2,
+  S_FULL = V_EMPTY0 + V_STAGES,  // S of a kv-block pair is in TMEM
+  S_FREE,                        // ... and has been read by both groups
+  P_READY0,
   P_FREE0 = P_READY0 + 2,
   O_FULL = P_FREE0 + 2,
   O_EMPTY,
@@ -83,8 +83,8 @@ constexpr uint32_t SM_QUEUE = SM_ABORT + 4;
 constexpr uint32_t SMEM_BYTES = SM_QUEUE + 4 * ITEM_SLOTS + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-constexpr uint32_t TM_O = 0, TM_S = 256, TM_P = 384;  // each x2: group g at + g * width
-constexpr uint32_t IDESC_S = idesc_f16_f32acc(128, 64, false, false);
+constexpr uint32_t TM_O = 0, TM_S = 256, TM_P = 384;  // O, P x2: group g at + g * width
+constexpr uint32_t IDESC_S = idesc_f16_f32acc(128, 128, false, false);
 constexpr uint32_t IDESC_PV = idesc_f16_f32acc(128, 128, false, true);
 
 struct Params {
@@ -189,8 +189,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(Q_FULL0 + s), 1);
       mbar_init(bar(Q_EMPTY0 + s), 1);
-      mbar_init(bar(S_FULL0 + s), 1);
-      mbar_init(bar(S_FREE0 + s), GROUP_WARPS);
       mbar_init(bar(P_READY0 + s), GROUP_WARPS);
       mbar_init(bar(P_FREE0 + s), 1);
     }
@@ -202,6 +200,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(bar(V_FULL0 + s), 1);
       mbar_init(bar(V_EMPTY0 + s), 1);
     }
+    mbar_init(bar(S_FULL), 1);
+    mbar_init(bar(S_FREE), SOFTMAX_WARPS);
     mbar_init(bar(O_FULL), 1);
     mbar_init(bar(O_EMPTY), SOFTMAX_WARPS);
     mbar_init(bar(DRAIN), 1);
@@ -260,20 +260,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_load_2d(base + SM_Q + qs * 32768u + static_cast<uint32_t>(lane) * 8192u, &tm_q,
                     bar(Q_FULL0 + qs), (lane & 2) ? 64 : 0, (lane & 1) ? r1 : r0);
       last_q[qs] = itc;
-      ok = for_union(p, q, [&](int j) {
+      // K of the union's kv blocks two at a time: block 2p in rows 0-63 of pair stage p, block
+      // 2p+1 (if any) in rows 64-127, each as (cols 0-63) and (cols 64-127) chunks of 16 KB.
+      int ja = -1, e = 0;
+      auto load_pair = [&](int j0, int j1) -> bool {
         const uint32_t st = lg % K_STAGES;
         if (!mbar_wait_warp(bar(K_EMPTY0 + st), ((lg / K_STAGES) & 1u) ^ 1u, abort,
                             WAIT_LIMIT_NS))
           return false;
-        if (lane == 0) mbar_arrive_expect_tx(bar(K_FULL0 + st), 16384u);
+        if (lane == 0) mbar_arrive_expect_tx(bar(K_FULL0 + st), j1 >= 0 ? 32768u : 16384u);
         __syncwarp();
-        if (lane < 2)
-          tma_load_2d(base + SM_K + st * 16384u + static_cast<uint32_t>(lane) * 8192u, &tm_k,
-                      bar(K_FULL0 + st), lane * 64, q.bh * S + j * BLOCK);
+        if (lane < 4 && (lane < 2 || j1 >= 0))  // lane: (block b = lane >> 1, chunk c = lane & 1)
+          tma_load_2d(base + SM_K + st * 32768u + static_cast<uint32_t>(lane & 1) * 16384u +
+                          static_cast<uint32_t>(lane >> 1) * 8192u,
+                      &tm_k, bar(K_FULL0 + st), (lane & 1) * 64,
+                      q.bh * S + ((lane >> 1) ? j1 : j0) * BLOCK);
         last_lg[st] = lg;
         ++lg;
         return true;
+      };
+      ok = for_union(p, q, [&](int j) {
+        if ((e++ & 1) == 0) {
+          ja = j;
+          return true;
+        }
+        return load_pair(ja, j);
       });
+      if (ok && (e & 1)) ok = load_pair(ja, -1);
       if (!ok) break;
       ++itc;
     }
@@ -334,43 +347,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------------ UMMA issuer
     // The whole warp runs this role in lockstep; every lane polls the barriers and one elected
     // lane issues each UMMA and commit.
-    uint32_t t = 0, itc = 0;  // kv blocks issued (one S and one P.V each); items
+    uint32_t pc = 0, vc = 0, itc = 0;  // kv-block pairs (S), kv blocks (P.V), items
+    uint32_t bc[2] = {0, 0};           // kv blocks of each softmax group
     bool ok = true, issued = false;
     const uint64_t q_kmaj = sdesc_sw128(base + SM_Q, 16, 1024);
-    const uint64_t k_kmaj = sdesc_sw128(base + SM_K, 16, 1024);   // K of stage 0
+    const uint64_t k_kmaj = sdesc_sw128(base + SM_K, 16, 1024);   // K pair of stage 0
     const uint64_t v_mn = sdesc_sw128(base + SM_V, 8192, 1024);   // V of stage 0
-    // S = Q_p K_j^T of kv block tb into S buffer tb & 1; Q from stage qs.
-    auto issue_s = [&](uint32_t tb, uint32_t qs) -> bool {
-      const uint32_t st = tb % K_STAGES, sb = tb & 1u;
-      if (!mbar_wait_warp(bar(K_FULL0 + st), (tb / K_STAGES) & 1u, abort, WAIT_LIMIT_NS))
+    // S = Q_p [K_a; K_b]^T of kv-block pair pb (N = 128: columns 0-63 block a, 64-127 block b);
+    // Q from stage qs.
+    auto issue_s = [&](uint32_t pb, uint32_t qs) -> bool {
+      const uint32_t st = pb % K_STAGES;
+      if (!mbar_wait_warp(bar(K_FULL0 + st), (pb / K_STAGES) & 1u, abort, WAIT_LIMIT_NS))
         return false;
-      if (!mbar_wait_warp(bar(S_FREE0 + sb), ((tb >> 1) & 1u) ^ 1u, abort, WAIT_LIMIT_NS))
-        return false;
+      if (!mbar_wait_warp(bar(S_FREE), (pb & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) return false;
       tc_fence_after_sync();
       const uint64_t qa = sdesc_advance(q_kmaj, qs * 32768u);
-      const uint64_t kd = sdesc_advance(k_kmaj, st * 16384u);
-      const uint32_t ts = tmem + TM_S + sb * 64u;
+      const uint64_t kd = sdesc_advance(k_kmaj, st * 32768u);
+      const uint32_t ts = tmem + TM_S;
       umma_ss_elect<false>(ts, qa, kd, IDESC_S);
 #pragma unroll
       for (int kk = 1; kk < 8; ++kk) {
         const uint32_t off = (kk & 3) * 32u;
         umma_ss_elect<true>(ts, sdesc_advance(qa, (kk >> 2) * 16384u + off),
-                         sdesc_advance(kd, (kk >> 2) * 8192u + off), IDESC_S);
+                            sdesc_advance(kd, (kk >> 2) * 16384u + off), IDESC_S);
       }
-      umma_commit_elect(bar(S_FULL0 + sb));
+      umma_commit_elect(bar(S_FULL));
       umma_commit_elect(bar(K_EMPTY0 + st));
       issued = true;
       return true;
     };
-    // O_g += P V_j of kv block tb, g = tb & 1: A = P buffer g in TMEM (8 columns per 16 kv),
-    // B = V_j.  `fresh`: the group's first block of the item overwrites O_g; `first`: the
-    // item's first P.V waits until the previous item's O buffers have been read.
-    auto issue_pv = [&](uint32_t tb, bool fresh, bool first) -> bool {
-      const uint32_t g = tb & 1u, st = tb % V_STAGES;
-      if (!mbar_wait_warp(bar(V_FULL0 + st), (tb / V_STAGES) & 1u, abort, WAIT_LIMIT_NS))
+    // O_g += P V_j of the group's next kv block (V stage from the global block count): A = P
+    // buffer g in TMEM (8 columns per 16 kv), B = V_j.  `fresh`: the group's first block of the
+    // item overwrites O_g; `first`: the item's first P.V waits until the previous item's O
+    // buffers have been read.
+    auto issue_pv = [&](uint32_t g, bool fresh, bool first) -> bool {
+      const uint32_t st = vc % V_STAGES;
+      if (!mbar_wait_warp(bar(V_FULL0 + st), (vc / V_STAGES) & 1u, abort, WAIT_LIMIT_NS))
         return false;
-      if (!mbar_wait_warp(bar(P_READY0 + g), (tb >> 1) & 1u, abort, WAIT_LIMIT_NS))
-        return false;
+      if (!mbar_wait_warp(bar(P_READY0 + g), bc[g] & 1u, abort, WAIT_LIMIT_NS)) return false;
       if (first && !mbar_wait_warp(bar(O_EMPTY), (itc & 1u) ^ 1u, abort, WAIT_LIMIT_NS))
         return false;
       tc_fence_after_sync();
@@ -385,6 +399,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         umma_ts_elect<true>(to, pa + kk * 8u, sdesc_advance(vb, kk * 2048u), IDESC_PV);
       umma_commit_elect(bar(P_FREE0 + g));
       umma_commit_elect(bar(V_EMPTY0 + st));
+      ++vc;
+      ++bc[g];
       return true;
     };
     for (uint32_t k = 0;; ++k) {
@@ -397,30 +413,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const Pair q = decode_pair(p, w);
       const int nu = union_size(p, q);
       if (nu == 0) continue;
+      const int npr = (nu + 1) >> 1;
       const uint32_t qs = itc & 1u;
       if (!mbar_wait_warp(bar(Q_FULL0 + qs), (itc >> 1) & 1u, abort, WAIT_LIMIT_NS)) {
         ok = false;
         break;
       }
-      // S runs two kv blocks ahead of P.V: S(e + 2) goes in as soon as group (e & 1) has
-      // read S(e), so that group finds its next S ready when it finishes P(e).
-      const uint32_t t0 = t;
-      const int ahead = nu < 2 ? nu : 2;
-      for (int e = 0; e < ahead && ok; ++e) ok = issue_s(t0 + e, qs);
-      if (ok && ahead == nu) umma_commit_elect(bar(Q_EMPTY0 + qs));  // every S has been issued
-      for (int e = 0; e < nu && ok; ++e) {
-        if (e + 2 < nu) {
-          if (!issue_s(t0 + e + 2, qs)) {
+      // S of pair p+1 goes in as soon as both groups have read S of pair p, ahead of the two
+      // P.V of pair p (group 0: block 2p, group 1: block 2p+1).
+      const uint32_t p0 = pc;
+      ok = issue_s(p0, qs);
+      for (int pr = 0; pr < npr && ok; ++pr) {
+        if (pr + 1 < npr) {
+          if (!issue_s(p0 + pr + 1, qs)) {
             ok = false;
             break;
           }
-          if (e + 3 == nu) umma_commit_elect(bar(Q_EMPTY0 + qs));
+        } else {
+          umma_commit_elect(bar(Q_EMPTY0 + qs));  // every S of the item has been issued
         }
-        ok = issue_pv(t0 + e, e < 2, e == 0);
+        ok = issue_pv(0, pr == 0, pr == 0);
+        if (ok && 2 * pr + 1 < nu) ok = issue_pv(1, pr == 0, false);
       }
       if (!ok) break;
       umma_commit_elect(bar(O_FULL));
-      t = t0 + nu;
+      pc = p0 + npr;
       ++itc;
     }
     if (!ok && lane == 0) raise_abort(abort, p.err);
@@ -440,7 +457,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t t_p = tmem + lane_off + TM_P + grp * 32u;
     const uint32_t t_o = tmem + lane_off + TM_O + grp * 128u;
     float2* xch = reinterpret_cast<float2*>(gbase + SM_XCH);  // [item parity][group][row] (m, l)
-    uint32_t t = 0, itc = 0;  // kv blocks of the CTA so far (both groups); items
+    uint32_t pc = 0, bc = 0, itc = 0;  // kv-block pairs; this group's kv blocks; items
     for (uint32_t k = 0;; ++k) {
       int w;
       if (!warp_take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, lane, &w)) {
@@ -469,10 +486,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const float c1 = p.sm_scale * LOG2E_F * exp2i(eq + ek);  // S' -> s (log2 units)
       float m = -INFINITY, l = 0.f;  // this group's reference maximum and sum of P * 2^KPF
       bool first = true;             // no block of this group in the item yet
-      const bool ok = for_union(p, q, [&](int j) {
-        const uint32_t tb = t++;
-        if ((tb & 1u) != static_cast<uint32_t>(grp)) return true;  // the other group's block
-        if (!warp_wait(bar(S_FULL0 + grp), (tb >> 1) & 1u, abort, lane)) return false;
+      // The union's kv blocks in pairs (block 2p for group 0, 2p+1 for group 1).
+      auto do_pair = [&](int j) -> bool {
+        if (!warp_wait(bar(S_FULL), pc & 1u, abort, lane)) return false;
+        ++pc;
+        if (j < 0) {  // odd tail: group 1 has no block, but S is free as far as it is concerned
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(S_FREE));
+          return true;
+        }
         tc_fence_after_sync();
         const bool mine = valid && ((own[j >> 5] >> (j & 31)) & 1u);
         const int vb = mine ? clamp_vbs(p.vbs[j]) : 0;  // visible columns of the row
@@ -482,7 +505,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_wait_ld();
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(S_FREE0 + grp));
+        if (lane == 0) mbar_arrive(bar(S_FREE));
         float mb = -INFINITY;  // the row's maximum over this kv block
 #pragma unroll
         for (int u = 0; u < 64; ++u)
@@ -490,7 +513,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const bool need = mb > m + RESCALE;
         // P buffer grp is free once the group's previous P.V has completed, and then O_grp
         // holds every block of the group so far.
-        if (!warp_wait(bar(P_FREE0 + grp), ((tb >> 1) & 1u) ^ 1u, abort, lane)) return false;
+        if (!warp_wait(bar(P_FREE0 + grp), (bc & 1u) ^ 1u, abort, lane)) return false;
         if (__any_sync(0xffffffffu, need)) {
           const float f = need ? ex2(m - mb) : 1.f;  // m = -inf: f = 0 (nothing accumulated)
           if (!first) {
@@ -525,9 +548,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(P_READY0 + grp));
+        ++bc;
         first = false;
         return true;
+      };
+      int e = 0, jprev = -1;
+      bool ok = for_union(p, q, [&](int j) {
+        const bool odd = (e++ & 1) != 0;
+        if (!odd) {
+          jprev = j;
+          return true;
+        }
+        return do_pair(grp == 0 ? jprev : j);
       });
+      if (ok && (e & 1)) ok = do_pair(grp == 0 ? jprev : -1);
       if (!ok) {
         if (lane == 0) raise_abort(abort, p.err);
         break;
