@@ -87,13 +87,13 @@ def test_invert_brute_force(oracle, seed):
 # ----------------------------------------------------------------------------- forward
 
 
-@pytest.mark.parametrize("ragged", [False, True])
-def test_forward_matches_dense_masked(oracle, ragged):
-    rng = np.random.default_rng(10 + ragged)
-    q, k, v, do, idx, num, vbs = rand_case(rng, 1, 2, 4, 2, ragged=ragged)
+@pytest.mark.parametrize("ragged,blk", [(False, 64), (True, 64), (True, 128)])
+def test_forward_matches_dense_masked(oracle, ragged, blk):
+    rng = np.random.default_rng(10 + ragged + blk)
+    q, k, v, do, idx, num, vbs = rand_case(rng, 1, 2, 4, 2, blk=blk, ragged=ragged)
     sc = 0.0883883476483184
-    o, lse = oracle.fwd(q, k, v, idx, num, vbs, sc)
-    o_ref, lse_ref, *_ = dense_forward_backward(q, k, v, do, block_mask(idx, num, vbs, 64), sc)
+    o, lse = oracle.fwd(q, k, v, idx, num, vbs, sc, blk=blk)
+    o_ref, lse_ref, *_ = dense_forward_backward(q, k, v, do, block_mask(idx, num, vbs, blk), sc)
     assert rel_err(o, o_ref) < 1e-12
     assert np.abs(lse - lse_ref).max() < 1e-12
 
@@ -163,15 +163,17 @@ def test_set_semantics_and_invalid_entries(oracle):
 # ----------------------------------------------------------------------------- backward
 
 
-@pytest.mark.parametrize("ragged,zero_pool", [(False, None), (True, None), (True, (1,))])
-def test_backward_matches_autograd(oracle, ragged, zero_pool):
-    rng = np.random.default_rng(20 + ragged)
-    q, k, v, do, idx, num, vbs = rand_case(rng, 1, 2, 4, 2, ragged=ragged, zero_pool=zero_pool)
+@pytest.mark.parametrize("ragged,zero_pool,blk", [(False, None, 64), (True, None, 64),
+                                                   (True, (1,), 64), (True, (2,), 128)])
+def test_backward_matches_autograd(oracle, ragged, zero_pool, blk):
+    rng = np.random.default_rng(20 + ragged + blk)
+    q, k, v, do, idx, num, vbs = rand_case(rng, 1, 2, 4, 2, blk=blk, ragged=ragged,
+                                           zero_pool=zero_pool)
     sc = 0.0883883476483184
-    mask = block_mask(idx, num, vbs, 64)
+    mask = block_mask(idx, num, vbs, blk)
     o_ref, lse_ref, dq_ref, dk_ref, dv_ref = dense_forward_backward(q, k, v, do, mask, sc)
-    o, lse = oracle.fwd(q, k, v, idx, num, vbs, sc)
-    dq, dk, dv = oracle.bwd(q, k, v, o, do, lse, idx, num, vbs, sc)
+    o, lse = oracle.fwd(q, k, v, idx, num, vbs, sc, blk=blk)
+    dq, dk, dv = oracle.bwd(q, k, v, o, do, lse, idx, num, vbs, sc, blk=blk)
     assert rel_err(dq, dq_ref) < 1e-10
     assert rel_err(dk, dk_ref) < 1e-10
     assert rel_err(dv, dv_ref) < 1e-10
