@@ -35,7 +35,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-FLOP_PER_PAIR = 5 * 2 * 64 * 64 * 128
+
+
+def flop_per_pair(blk):
+    """5 GEMMs of a selected (q block, kv block) pair of `blk`-token blocks, head_dim 128."""
+    return 5 * 2 * blk * blk * 128
 METRIC = "bwd TFLOPS on selected blocks (5 GEMMs/pair) and % of BF16 tensor peak, 1 GB300"
 # The sm_100a kernel's published TFLOPS at the same shapes (B=1, H=8, D=128, 25 % density).
 PAGES_TFLOPS = {"4k_25pct": 381.0, "32k_25pct": 794.0, "131k_25pct": 736.0, "262k_25pct": 784.0,
@@ -195,6 +199,7 @@ class OracleSampler:
         self.idx = case["q2k_idx"][b:b + 1, h:h + 1]
         self.num = case["q2k_num"][b:b + 1, h:h + 1]
         self.nb, self.vbs, self.sc = case["nb"], case["vbs"], case["sm_scale"]
+        self.blk = case.get("blk", 64)
         self.k2q_idx, self.k2q_num, _ = orc.invert(self.idx, self.num, self.nb)
         S, D = self.sub["q"].shape[2:]
         self.o = np.zeros((1, 1, S, D))
@@ -206,9 +211,9 @@ class OracleSampler:
         if not blocks:
             return
         o, lse = self.orc.fwd(self.sub["q"], self.sub["k"], self.sub["v"], self.idx, self.num,
-                              self.vbs, self.sc, qblocks=blocks)
+                              self.vbs, self.sc, blk=self.blk, qblocks=blocks)
         for i in blocks:
-            r = slice(64 * i, 64 * (i + 1))
+            r = slice(self.blk * i, self.blk * (i + 1))
             self.o[0, 0, r] = torch.from_numpy(o[0, 0, r]).to(torch.bfloat16).to(
                 torch.float64).numpy()
             self.lse[0, 0, r] = lse[0, 0, r].astype(np.float32)
@@ -231,12 +236,13 @@ class OracleSampler:
         s = self.sub
         t0 = time.perf_counter()
         self.orc.bwd(s["q"], s["k"], s["v"], self.o, s["do"], self.lse, self.idx, self.num,
-                     self.vbs, self.sc, qblocks=list(range(m)), kvblocks=list(range(m)))
+                     self.vbs, self.sc, blk=self.blk, qblocks=list(range(m)),
+                     kvblocks=list(range(m)))
         t = time.perf_counter() - t0
         # The oracle's dQ loop recomputes S, dP and forms dQ (3 GEMM-sized products per pair);
         # its dK/dV loop recomputes S, dP and forms dV, dK (4 per pair): a pair completed = 7.
         done = (3 * self.pairs_q(m) + 4 * self.pairs_kv(m)) / 7.0
-        return done * FLOP_PER_PAIR / t / 1e12, t
+        return done * flop_per_pair(self.blk) / t / 1e12, t
 
     def size_for(self, target_s):
         """m whose sample takes about target_s seconds (from a small calibration run)."""
@@ -387,7 +393,8 @@ def main():
     post_ms = [e["after_main"].elapsed_time(e["end"]) for e in ev]
     inv_ms = [a.elapsed_time(b_) for a, b_ in inv]
     all_pairs = reduce_sum(dist, float(pairs), device)
-    value = all_pairs * FLOP_PER_PAIR / (total_ms / K / 1e3) / 1e12
+    fpp = flop_per_pair(case.get("blk", 64))
+    value = all_pairs * fpp / (total_ms / K / 1e3) / 1e12
 
     # End to end through the public API with host buffers.
     host_in = {n: dev[n].cpu().pin_memory() for n in ("q", "k", "v", "do")}
@@ -425,7 +432,7 @@ def main():
     torch.cuda.synchronize()
     barrier(dist, device)
     e2e_ms = reduce_max(dist, e0.elapsed_time(e1), device) / K_e2e
-    e2e_value = all_pairs * FLOP_PER_PAIR / (e2e_ms / 1e3) / 1e12
+    e2e_value = all_pairs * fpp / (e2e_ms / 1e3) / 1e12
 
     # A training step through the autograd binding: forward, then inversion and backward.
     from block_sparse_video_tok_gb300.autograd import block_sparse_attention
@@ -450,7 +457,7 @@ def main():
     torch.cuda.synchronize()
     barrier(dist, device)
     train_ms = reduce_max(dist, t0_.elapsed_time(t1_), device) / K_train
-    train_tflops = all_pairs * FLOP_PER_PAIR * 7 / 5 / (train_ms / 1e3) / 1e12
+    train_tflops = all_pairs * fpp * 7 / 5 / (train_ms / 1e3) / 1e12
 
     if rank != 0:
         if dist is not None:
@@ -459,7 +466,7 @@ def main():
 
     peak, peak_sus, hbm, peak_src = peaks()
     main_avg = float(np.mean(main_ms))
-    achieved = pairs * FLOP_PER_PAIR / (main_avg / 1e3) / 1e12
+    achieved = pairs * fpp / (main_avg / 1e3) / 1e12
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         sampler = OracleSampler(case)

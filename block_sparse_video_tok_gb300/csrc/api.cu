@@ -35,15 +35,20 @@ vsa_status cuda_fail(cudaError_t e) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Shape rules: B, H >= 1; head_dim 128; S a positive multiple of 64; B*H*S rows addressable with
-// 32-bit TMA coordinates.
-vsa_status check_shape(const vsa_shape& s, int* nb) {
+// Shape rules: B, H >= 1; head_dim 128; block 64 or 128 (0 read as 64); S a positive multiple of
+// the block; B*H*S rows addressable with 32-bit TMA coordinates.  *nb counts sparse blocks of
+// *blk tokens.  The kernels work on 64-token tiles: a 128-token block is two of them with the
+// same selection.
+vsa_status check_shape(const vsa_shape& s, int* nb, int* blk = nullptr) {
   if (s.batch < 1 || s.heads < 1 || s.seqlen < 1) return VSA_ERR_INVALID_ARG;
   if (s.head_dim != vsa::HEAD_DIM) return VSA_ERR_UNSUPPORTED;
-  if (s.seqlen % vsa::BLOCK != 0) return VSA_ERR_UNSUPPORTED;
+  const int b = s.block == 0 ? vsa::BLOCK : s.block;
+  if (b != vsa::BLOCK && b != 2 * vsa::BLOCK) return VSA_ERR_UNSUPPORTED;
+  if (s.seqlen % b != 0) return VSA_ERR_UNSUPPORTED;
   const long long rows = static_cast<long long>(s.batch) * s.heads * s.seqlen;
   if (rows > INT_MAX / 2) return VSA_ERR_UNSUPPORTED;
-  *nb = s.seqlen / vsa::BLOCK;
+  *nb = s.seqlen / b;
+  if (blk) *blk = b;
   return VSA_OK;
 }
 
@@ -129,8 +134,8 @@ vsa_status vsa_fwd(const void* q, const void* k, const void* v, const int32_t* q
                    const int32_t* q2k_num, int32_t topk, const int32_t* vbs, float sm_scale,
                    vsa_shape shape, void* o, float* lse, void* workspace, size_t workspace_bytes,
                    void* stream) {
-  int nb = 0;
-  vsa_status st = check_shape(shape, &nb);
+  int nb = 0, blk = 0;
+  vsa_status st = check_shape(shape, &nb, &blk);
   if (st != VSA_OK) return st;
   if (!q || !k || !v || !q2k_idx || !q2k_num || !vbs || !o || !lse) return VSA_ERR_INVALID_ARG;
   if (topk < 1 || !std::isfinite(sm_scale)) return VSA_ERR_INVALID_ARG;
@@ -146,6 +151,7 @@ vsa_status vsa_fwd(const void* q, const void* k, const void* v, const int32_t* q
   uint32_t* err = ws_at<uint32_t>(workspace, L.err);
   uint32_t* absmax = ws_at<uint32_t>(workspace, L.absmax);
   uint32_t* bitmap = ws_at<uint32_t>(workspace, L.bitmap);
+  int32_t* vbs64 = ws_at<int32_t>(workspace, L.vbs64);
   __half* q16 = ws_at<__half>(workspace, L.q16);
   __half* k16 = ws_at<__half>(workspace, L.k16);
   __half* v16 = ws_at<__half>(workspace, L.v16);
@@ -161,14 +167,17 @@ vsa_status vsa_fwd(const void* q, const void* k, const void* v, const int32_t* q
   const __nv_bfloat16* src[3] = {qb, kb, vb};
   __half* dst[3] = {q16, k16, v16};
   if ((e = vsa::launch_convert(src, dst, 3, BH, S, absmax, s)) != cudaSuccess) return cuda_fail(e);
-  if ((e = vsa::launch_fwd_bitmap(q2k_idx, q2k_num, topk, BH, nb, bitmap, err, s)) != cudaSuccess)
+  if ((e = vsa::launch_vbs_expand(vbs, nb, blk / vsa::BLOCK, vbs64, err, s)) != cudaSuccess)
+    return cuda_fail(e);
+  if ((e = vsa::launch_fwd_bitmap(q2k_idx, q2k_num, topk, BH, nb, blk / vsa::BLOCK, bitmap, err,
+                                  s)) != cudaSuccess)
     return cuda_fail(e);
   vsa::FwdMainArgs a{};
   a.q16 = q16;
   a.k16 = k16;
   a.v16 = v16;
   a.bitmap = bitmap;
-  a.vbs = vbs;
+  a.vbs = vbs64;
   a.absmax = absmax;
   a.o = static_cast<__nv_bfloat16*>(o);
   a.lse = lse;
@@ -177,7 +186,7 @@ vsa_status vsa_fwd(const void* q, const void* k, const void* v, const int32_t* q
   a.B = shape.batch;
   a.H = shape.heads;
   a.S = S;
-  a.nb = nb;
+  a.nb = S / vsa::BLOCK;
   a.sm_scale = sm_scale;
   if ((e = vsa::launch_fwd_main(a, s)) != cudaSuccess) return cuda_fail(e);
   return VSA_OK;
@@ -198,8 +207,8 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
                          float sm_scale, vsa_shape shape, void* dq, void* dk, void* dv,
                          void* workspace, size_t workspace_bytes, const vsa_bwd_events* events,
                          void* stream) {
-  int nb = 0;
-  vsa_status st = check_shape(shape, &nb);
+  int nb = 0, blk = 0;
+  vsa_status st = check_shape(shape, &nb, &blk);
   if (st != VSA_OK) return st;
   if (!dout || !q || !k || !v || !o || !lse || !k2q_idx || !k2q_num || !vbs || !dq || !dk || !dv)
     return VSA_ERR_INVALID_ARG;
@@ -218,6 +227,7 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
   uint32_t* absmax = ws_at<uint32_t>(workspace, L.absmax);
   float* delta = ws_at<float>(workspace, L.delta);
   int32_t* order = ws_at<int32_t>(workspace, L.order);
+  int32_t* vbs64 = ws_at<int32_t>(workspace, L.vbs64);
   float* dqacc = ws_at<float>(workspace, L.dqacc);
   __half* q16 = ws_at<__half>(workspace, L.q16);
   __half* k16 = ws_at<__half>(workspace, L.k16);
@@ -239,8 +249,10 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
   const __nv_bfloat16* src[4] = {qb, kb, vb, dob};
   __half* dst[4] = {q16, k16, v16, do16};
   if ((e = vsa::launch_convert(src, dst, 4, BH, S, absmax, s)) != cudaSuccess) return cuda_fail(e);
+  if ((e = vsa::launch_vbs_expand(vbs, nb, blk / vsa::BLOCK, vbs64, err, s)) != cudaSuccess)
+    return cuda_fail(e);
   const int32_t* work_order = nullptr;
-  if (nb >= vsa::ORDER_MIN_KV_BLOCKS) {
+  if (S / vsa::BLOCK >= vsa::ORDER_MIN_KV_BLOCKS) {
     if ((e = vsa::launch_order(k2q_num, BH, nb, max_q_blocks, order, s)) != cudaSuccess)
       return cuda_fail(e);
     work_order = order;
@@ -253,7 +265,7 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
   a.k2q_idx = k2q_idx;
   a.k2q_num = k2q_num;
   a.order = work_order;
-  a.vbs = vbs;
+  a.vbs = vbs64;
   a.lse = lse;
   a.delta = delta;
   a.absmax = absmax;
@@ -265,7 +277,9 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
   a.B = shape.batch;
   a.H = shape.heads;
   a.S = S;
-  a.nb = nb;
+  a.nb = S / vsa::BLOCK;
+  a.nsel = nb;
+  a.tiles = blk / vsa::BLOCK;
   a.max_q = max_q_blocks;
   a.sm_scale = sm_scale;
   if ((e = record(events ? events->before_main : nullptr, s)) != cudaSuccess) return cuda_fail(e);

@@ -115,29 +115,58 @@ struct Params {
   __nv_bfloat16* dv;
   uint32_t* err;
   int32_t* sched;  // work counter, zero at launch
-  int S, nb, max_q, total;
+  int S;
+  int nb;     // 64-token tiles per sequence; work items are (b, h, kv tile)
+  int nsel;   // sparse blocks per sequence (k2q rows per head)
+  int tiles;  // 64-token tiles per sparse block: 1, or 2 for 128-token blocks
+  int max_q, total;
   float sm_scale;
 };
 
+// A work item: kv tile j of head bh.  Its k2q row `sel` lists selecting q blocks; each step
+// processes a pair of 64-token q tiles: two consecutive list entries (64-token blocks; an odd
+// tail repeats the last one), or the two tiles of one 128-token entry.
 struct Item {
-  int bh, j, n;
+  int bh, j, sel, n, np;
   const int32_t* list;
 };
 
 __device__ __forceinline__ Item decode_item(const Params& p, int w) {
-  const int item = p.order ? p.order[w] : w;
+  int half = 0, ws = w;
+  if (p.tiles == 2) {
+    half = w & 1;
+    ws = w >> 1;
+  }
+  const int sel = p.order ? p.order[ws] : ws;
   Item it;
-  it.bh = item / p.nb;
-  it.j = item - it.bh * p.nb;
-  const int n = p.k2q_num[item];
+  it.bh = sel / p.nsel;
+  it.j = (sel - it.bh * p.nsel) * p.tiles + half;
+  it.sel = sel;
+  const int n = p.k2q_num[sel];
   it.n = n < 0 ? 0 : (n > p.max_q ? p.max_q : n);
-  it.list = p.k2q_idx + static_cast<size_t>(item) * p.max_q;
+  it.np = p.tiles == 2 ? it.n : (it.n + 1) >> 1;
+  it.list = p.k2q_idx + static_cast<size_t>(sel) * p.max_q;
   return it;
 }
 
 __device__ __forceinline__ int q_block(const Item& it, int x, int nq) {
   const int i = it.list[x];
   return (i < 0 || i >= nq) ? 0 : i;
+}
+
+// The two 64-token q tiles of step pp; false if the second one only repeats the first (odd
+// tail of a 64-token list).
+__device__ __forceinline__ bool step_tiles(const Params& p, const Item& it, int pp, int* i0,
+                                           int* i1) {
+  if (p.tiles == 2) {
+    *i0 = 2 * q_block(it, pp, p.nsel);
+    *i1 = *i0 + 1;
+    return true;
+  }
+  *i0 = q_block(it, 2 * pp, p.nsel);
+  const bool has2 = 2 * pp + 1 < it.n;
+  *i1 = has2 ? q_block(it, 2 * pp + 1, p.nsel) : *i0;
+  return has2;
 }
 
 __device__ __forceinline__ int clamp_vbs(int v) { return v < 0 ? 0 : (v > BLOCK ? BLOCK : v); }
@@ -181,7 +210,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto bar = [&](uint32_t b) { return base + SM_BAR + 8u * b; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int S = p.S, nq = p.nb;
+  const int S = p.S, nq = p.nsel;
 
   if (threadIdx.x == 0) {
     *abort = 0;
@@ -248,11 +277,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (w >= p.total) break;  // the end marker
       const Item it = decode_item(p, w);
       uint32_t bad = 0;
-      if (lane == 0) {
-        if (p.k2q_num[p.order ? p.order[w] : w] != it.n) bad |= VSA_DEVERR_K2Q_COUNT;
-        const int vb = p.vbs[it.j];
-        if (vb != clamp_vbs(vb)) bad |= VSA_DEVERR_VBS;
-      }
+      if (lane == 0 && p.k2q_num[it.sel] != it.n) bad |= VSA_DEVERR_K2Q_COUNT;
       for (int x = lane; x < it.n; x += 32) {
         const int i = it.list[x];
         if (i < 0 || i >= nq) bad |= VSA_DEVERR_K2Q_ID;
@@ -271,15 +296,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_load_2d(base + ((lane < 2) ? SM_K : SM_V) + (lane & 1) * 8192u,
                     (lane < 2) ? &tm_k : &tm_v, bar(KV_FULL), (lane & 1) * 64, row_kv);
       ++kv_loads;
-      const int np = (it.n + 1) >> 1;
+      const int np = it.np;
       for (int pp = 0; pp < np; ++pp, ++g) {
         const uint32_t s = g & 1u;
         if (!mbar_wait_warp(bar(QDO_EMPTY0 + s), ((g >> 1) & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) {
           ok = false;
           break;
         }
-        const int i0 = q_block(it, 2 * pp, nq);
-        const int i1 = (2 * pp + 1 < it.n) ? q_block(it, 2 * pp + 1, nq) : i0;
+        int i0, i1;
+        step_tiles(p, it, pp, &i0, &i1);
         const int r0 = it.bh * S + i0 * BLOCK, r1 = it.bh * S + i1 * BLOCK;
         if (lane == 0) mbar_arrive_expect_tx(bar(QDO_FULL0 + s), 65536);
         __syncwarp();
@@ -404,7 +429,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (w >= p.total) break;
       const Item it = decode_item(p, w);
       if (it.n == 0) continue;
-      const int np = (it.n + 1) >> 1;
+      const int np = it.np;
       if (!mbar_wait_warp(bar(KV_FULL), itc & 1u, abort, WAIT_LIMIT_NS)) {
         ok = false;
         break;
@@ -495,12 +520,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int ev = operand_exponent(am[2]), eo = operand_exponent(am[3]);
       const float c1 = p.sm_scale * LOG2E_F * exp2i(eq + ek);
       const float dscale = exp2i(-(eo + ev));
-      const int np = (it.n + 1) >> 1;
+      const int np = it.np;
       bool ok = true;
       for (int pp = 0; pp < np; ++pp, ++g) {
-        const bool has2 = (2 * pp + 1 < it.n);
+        int i0, i1;
+        const bool has2 = step_tiles(p, it, pp, &i0, &i1);
         const bool valid = (r < 64) || has2;
-        const int qb = q_block(it, 2 * pp + ((r >= 64 && has2) ? 1 : 0), nq);
+        const int qb = (r >= 64) ? i1 : i0;
         const size_t grow = static_cast<size_t>(it.bh) * S + static_cast<size_t>(qb) * BLOCK + (r & 63);
         const float nlse = static_cast<float>(KP) - p.lse[grow];
         const float dl = p.delta[grow] * dscale;  // Delta in the units of dP' = dO'.V'
@@ -615,12 +641,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const float sv_scale = exp2i(eo - KP);
       const float sk_scale = p.sm_scale * exp2i(eq + eo + ev - KP);
       const int vb = clamp_vbs(p.vbs[it.j]);
-      const int np = (it.n + 1) >> 1;
+      const int np = it.np;
       bool ok = true;
       for (int pp = 0; pp < np; ++pp, ++g) {
-        const bool has2 = (2 * pp + 1 < it.n);
-        const int i0 = q_block(it, 2 * pp, nq);
-        const int i1 = has2 ? q_block(it, 2 * pp + 1, nq) : i0;
+        int i0, i1;
+        const bool has2 = step_tiles(p, it, pp, &i0, &i1);
         const uint32_t buf = g & 1u;
         if (!warp_wait(bar(DQ_FULL0 + buf), (g >> 1) & 1u, abort, lane)) {
           ok = false;
@@ -797,6 +822,8 @@ cudaError_t launch_bwd_main(const BwdMainArgs& a, cudaStream_t stream) {
   p.sched = a.sched;
   p.S = a.S;
   p.nb = a.nb;
+  p.nsel = a.nsel;
+  p.tiles = a.tiles;
   p.max_q = a.max_q;
   p.total = a.B * a.H * a.nb;
   p.sm_scale = a.sm_scale;

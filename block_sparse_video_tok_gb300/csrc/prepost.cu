@@ -167,16 +167,20 @@ __global__ void __launch_bounds__(256) postprocess_kernel(const float4* __restri
 }
 
 // One thread per q2k entry: set bit j of q block i's row of the selection bitmap.
+// q2k rows count blocks of `tiles` 64-token tiles; the bitmap has one row of nb * tiles bits per
+// 64-token query tile, so a selected (I, J) sets the tiles x tiles bits of that block pair.
 __global__ void __launch_bounds__(256) fwd_bitmap_kernel(const int32_t* __restrict__ q2k_idx,
                                                          const int32_t* __restrict__ q2k_num,
-                                                         int topk, int nb, size_t entries,
+                                                         int topk, int nb, int tiles,
+                                                         size_t entries,
                                                          uint32_t* __restrict__ bitmap,
                                                          uint32_t* err) {
-  const int words = (nb + 31) >> 5;
+  const int nt = nb * tiles;
+  const int words = (nt + 31) >> 5;
   uint32_t bad = 0;
   for (size_t e = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; e < entries;
        e += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const size_t r = e / topk;
+    const size_t r = e / topk;  // bh * nb + I
     const int s = static_cast<int>(e - r * topk);
     const int c = q2k_num[r];
     const int cnt = c < 0 ? 0 : (c > topk ? topk : c);
@@ -187,7 +191,28 @@ __global__ void __launch_bounds__(256) fwd_bitmap_kernel(const int32_t* __restri
       bad |= VSA_DEVERR_Q2K_ID;
       continue;
     }
-    atomicOr(bitmap + r * words + (j >> 5), 1u << (j & 31));
+    const size_t bh = r / nb;
+    const size_t row0 = bh * nt + (r - bh * nb) * tiles;
+    for (int a = 0; a < tiles; ++a)
+      for (int b = 0; b < tiles; ++b) {
+        const int t = j * tiles + b;
+        atomicOr(bitmap + (row0 + a) * words + (t >> 5), 1u << (t & 31));
+      }
+  }
+  if (bad && err) atomicOr(err, bad);
+}
+
+__global__ void __launch_bounds__(256) vbs_expand_kernel(const int32_t* __restrict__ vbs, int nb,
+                                                         int tiles, int32_t* __restrict__ vbs64,
+                                                         uint32_t* err) {
+  const int lim = BLOCK * tiles;
+  uint32_t bad = 0;
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < nb * tiles;
+       t += gridDim.x * blockDim.x) {
+    const int v = vbs[t / tiles];
+    if (v < 0 || v > lim) bad |= VSA_DEVERR_VBS;
+    const int w = (v < 0 ? 0 : (v > lim ? lim : v)) - BLOCK * (t % tiles);
+    vbs64[t] = w < 0 ? 0 : (w > BLOCK ? BLOCK : w);
   }
   if (bad && err) atomicOr(err, bad);
 }
@@ -250,10 +275,18 @@ cudaError_t launch_postprocess(const float* dqacc, const uint32_t* absmax, int B
 }
 
 cudaError_t launch_fwd_bitmap(const int32_t* q2k_idx, const int32_t* q2k_num, int topk, int BH,
-                              int nb, uint32_t* bitmap, uint32_t* err, cudaStream_t stream) {
+                              int nb, int tiles, uint32_t* bitmap, uint32_t* err,
+                              cudaStream_t stream) {
   const size_t entries = static_cast<size_t>(BH) * nb * topk;
   fwd_bitmap_kernel<<<grid_for(entries, 256, 4), 256, 0, stream>>>(q2k_idx, q2k_num, topk, nb,
-                                                                    entries, bitmap, err);
+                                                                    tiles, entries, bitmap, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_vbs_expand(const int32_t* vbs, int nb, int tiles, int32_t* vbs64,
+                              uint32_t* err, cudaStream_t stream) {
+  vbs_expand_kernel<<<grid_for(static_cast<size_t>(nb) * tiles, 256, 1), 256, 0, stream>>>(
+      vbs, nb, tiles, vbs64, err);
   return cudaGetLastError();
 }
 

@@ -29,10 +29,10 @@ constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;   // in-flight copies after an
 // dO), then 1024-byte aligned arrays.
 
 struct BwdLayout {
-  size_t err, sched, absmax, delta, order, dqacc, q16, k16, v16, do16, total;
+  size_t err, sched, absmax, delta, order, vbs64, dqacc, q16, k16, v16, do16, total;
 };
 struct FwdLayout {
-  size_t err, sched, absmax, bitmap, q16, k16, v16, total;
+  size_t err, sched, absmax, bitmap, vbs64, q16, k16, v16, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -50,6 +50,8 @@ inline BwdLayout bwd_layout(long B, long H, long S) {
   off = align_up(off + rows * sizeof(float), 1024);
   L.order = off;
   off = align_up(off + bh * nb * sizeof(int32_t), 1024);
+  L.vbs64 = off;
+  off = align_up(off + nb * sizeof(int32_t), 1024);
   L.dqacc = off;
   off = align_up(off + rows * HEAD_DIM * sizeof(float), 1024);
   L.q16 = off;
@@ -76,6 +78,8 @@ inline FwdLayout fwd_layout(long B, long H, long S) {
   off = align_up(off + bh * 4 * sizeof(uint32_t), 1024);
   L.bitmap = off;
   off = align_up(off + bh * nb * words * sizeof(uint32_t), 1024);
+  L.vbs64 = off;
+  off = align_up(off + nb * sizeof(int32_t), 1024);
   L.q16 = off;
   off = align_up(off + rows * HEAD_DIM * sizeof(__half), 1024);
   L.k16 = off;
@@ -151,13 +155,25 @@ struct BwdMainArgs {
   __nv_bfloat16* dv;
   uint32_t* err;
   int32_t* sched;  // zeroed work counter
-  int B, H, S, nb, max_q;
+  int B, H, S;
+  int nb;     // 64-token tiles per sequence (kv items per head = nb)
+  int nsel;   // sparse blocks per sequence (rows of k2q per head); nb = nsel * tiles
+  int tiles;  // 64-token tiles per sparse block: 1, or 2 for 128-token blocks
+  int max_q;
   float sm_scale;
 };
 cudaError_t launch_bwd_main(const BwdMainArgs& a, cudaStream_t stream);
 
+// Selection bitmap of the forward at 64-token granularity: [BH, nb * tiles, ceil(nb * tiles / 32)]
+// bits from q2k rows that count blocks of `tiles` 64-token tiles (1 or 2).
 cudaError_t launch_fwd_bitmap(const int32_t* q2k_idx, const int32_t* q2k_num, int topk, int BH,
-                              int nb, uint32_t* bitmap, uint32_t* err, cudaStream_t stream);
+                              int nb, int tiles, uint32_t* bitmap, uint32_t* err,
+                              cudaStream_t stream);
+
+// vbs64[t] = valid tokens of 64-token tile t from the per-block sizes of blocks of `tiles`
+// 64-token tiles (block sizes clamped to [0, 64 * tiles]; VSA_DEVERR_VBS when one is outside).
+cudaError_t launch_vbs_expand(const int32_t* vbs, int nb, int tiles, int32_t* vbs64,
+                              uint32_t* err, cudaStream_t stream);
 
 struct FwdMainArgs {
   const __half *q16, *k16, *v16;

@@ -27,7 +27,8 @@ DEVERR_TIMEOUT = 0x20
 
 class VsaShape(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("heads", ctypes.c_int32),
-                ("seqlen", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+                ("seqlen", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("block", ctypes.c_int32)]
 
 
 class VsaBwdEvents(ctypes.Structure):
@@ -114,8 +115,17 @@ def _need(t, name, dtype, ndim=None):
         raise ValueError("%s must be contiguous" % name)
 
 
-def make_shape(batch, heads, seqlen, head_dim=HEAD_DIM):
-    return VsaShape(int(batch), int(heads), int(seqlen), int(head_dim))
+def make_shape(batch, heads, seqlen, head_dim=HEAD_DIM, block=BLOCK):
+    return VsaShape(int(batch), int(heads), int(seqlen), int(head_dim), int(block))
+
+
+def _block_size(S, vbs):
+    """Tokens per sparse block, inferred from the sequence length and the number of blocks (the
+    length of variable_block_sizes): 64 or 128."""
+    nb = vbs.numel()
+    if nb < 1 or S % nb != 0 or S // nb not in (64, 128):
+        raise ValueError("S = %d is not 64 or 128 tokens times len(vbs) = %d" % (S, nb))
+    return S // nb
 
 
 def vsa_fwd_workspace_bytes(batch, heads, seqlen, head_dim=HEAD_DIM):
@@ -171,7 +181,7 @@ def vsa_fwd(q, k, v, q2k_idx, q2k_num, vbs, sm_scale, o=None, lse=None, workspac
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
-    shape = make_shape(B, H, S, D)
+    shape = make_shape(B, H, S, D, _block_size(S, vbs))
     need = int(lib().vsa_fwd_workspace_bytes(shape))
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
@@ -205,12 +215,13 @@ def vsa_bwd(dout, q, k, v, o, lse, k2q_idx, k2q_num, vbs, sm_scale, dq=None, dk=
     _need(vbs, "vbs", torch.int32, 1)
     _need(k2q_idx, "k2q_idx", torch.int32)
     max_q = k2q_idx.shape[-1]
-    if k2q_idx.numel() != B * H * (S // BLOCK) * max_q:
+    blk = _block_size(S, vbs)
+    if k2q_idx.numel() != B * H * (S // blk) * max_q:
         raise ValueError("k2q_idx must hold [B, H, nb, max_q_blocks] entries")
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    shape = make_shape(B, H, S, D)
+    shape = make_shape(B, H, S, D, blk)
     need = int(lib().vsa_bwd_workspace_bytes(shape))
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
@@ -240,14 +251,15 @@ def vsa_bwd_no_alloc(dout, q, k, v, o, lse, k2q_idx, k2q_num, vbs, sm_scale, dq=
     _need(vbs, "vbs", torch.int32, 1)
     _need(k2q_idx, "k2q_idx", torch.int32)
     max_q = k2q_idx.shape[-1]
-    if k2q_idx.numel() != B * H * (S // BLOCK) * max_q:
+    blk = _block_size(S, vbs)
+    if k2q_idx.numel() != B * H * (S // blk) * max_q:
         raise ValueError("k2q_idx must hold [B, H, nb, max_q_blocks] entries")
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     _check(lib().vsa_bwd_no_alloc(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                                   _ptr(k2q_idx), _ptr(k2q_num), max_q, _ptr(vbs), float(sm_scale),
-                                  make_shape(B, H, S, D), _ptr(dq), _ptr(dk), _ptr(dv),
+                                  make_shape(B, H, S, D, blk), _ptr(dq), _ptr(dk), _ptr(dv),
                                   _stream(stream)), "vsa_bwd_no_alloc")
     return dq, dk, dv
 

@@ -45,6 +45,9 @@ LONG_CONFIGS = {
     "524k_25pct": dict(B=1, H=8, nb=8192, topk=2048, select="uniform", vbs="full", seed=0),
     # 524k tokens at low density: long-sequence index arithmetic at a size the oracle can sample.
     "524k_sparse": dict(B=1, H=2, nb=8192, topk=16, select="uniform", vbs="ragged33", seed=0),
+    # 32k tokens in 128-token blocks at 25 % density.
+    "32k_25pct_blk128": dict(B=1, H=8, nb=256, topk=64, select="uniform", vbs="full", seed=0,
+                             blk=128),
     # Wan2.1-1.3B-like layers (12 heads of 128): an 81-frame 480P latent (21 x 60 x 104) and a
     # 720P one (21 x 90 x 160) in 4x4x4 cubes, each q block attending to 12.5 % of the cubes.
     "wan480p_h12": dict(B=1, H=12, nb=2340, topk=293, select="scores", vbs="cubes:21x60x104",
@@ -111,16 +114,16 @@ def _select(rng, kind, B, H, nb, topk, kv_pool=None):
     return pick.reshape(B, H, nb, topk)
 
 
-def _block_sizes(rng, kind, nb):
+def _block_sizes(rng, kind, nb, blk=BLOCK):
     if kind == "full":
-        return np.full(nb, BLOCK, np.int32)
+        return np.full(nb, blk, np.int32)
     if kind == "last40":
-        v = np.full(nb, BLOCK, np.int32)
+        v = np.full(nb, blk, np.int32)
         v[-1] = 40
         return v
     if kind.startswith("ragged"):
         lo = int(kind[len("ragged"):])
-        return rng.integers(lo, BLOCK + 1, size=nb).astype(np.int32)
+        return rng.integers(lo, blk + 1, size=nb).astype(np.int32)
     if kind.startswith("cubes"):
         grid = VIDEO_GRID if kind == "cubes" else tuple(int(x) for x in kind[6:].split("x"))
         v = video_cube_sizes(grid)
@@ -130,11 +133,12 @@ def _block_sizes(rng, kind, nb):
 
 
 def make_case(B, H, nb, topk, select="uniform", vbs="full", seed=0, kv_pool=None,
-              with_grad_out=True):
-    """Draw one case.  Returns a dict with bf16 CPU tensors q, k, v, do ([B,H,S,128]), int32
-    numpy arrays q2k_idx [B,H,nb,topk], q2k_num [B,H,nb], vbs [nb], and sm_scale."""
+              with_grad_out=True, blk=BLOCK):
+    """Draw one case with nb sparse blocks of `blk` tokens (64 or 128).  Returns a dict with bf16
+    CPU tensors q, k, v, do ([B,H,S,128], S = blk * nb), int32 numpy arrays q2k_idx
+    [B,H,nb,topk], q2k_num [B,H,nb], vbs [nb], sm_scale and blk."""
     rng = np.random.Generator(np.random.PCG64(seed))
-    S = nb * BLOCK
+    S = nb * blk
     shape = (B, H, S, HEAD_DIM)
     names = ["q", "k", "v"] + (["do"] if with_grad_out else [])
     case = {}
@@ -142,9 +146,9 @@ def make_case(B, H, nb, topk, select="uniform", vbs="full", seed=0, kv_pool=None
         case[n] = _bf16(rng.standard_normal(shape, dtype=np.float32))
     case["q2k_idx"] = _select(rng, select, B, H, nb, topk, kv_pool)
     case["q2k_num"] = np.full((B, H, nb), topk, np.int32)
-    case["vbs"] = _block_sizes(rng, vbs, nb)
+    case["vbs"] = _block_sizes(rng, vbs, nb, blk)
     case["sm_scale"] = 1.0 / math.sqrt(HEAD_DIM)
-    case.update(B=B, H=H, S=S, nb=nb, topk=topk)
+    case.update(B=B, H=H, S=S, nb=nb, topk=topk, blk=blk)
     return case
 
 
@@ -159,7 +163,7 @@ def make_config(name, seed=None):
     if seed is not None:
         cfg["seed"] = seed
     return make_case(cfg["B"], cfg["H"], cfg["nb"], cfg["topk"], cfg["select"], cfg["vbs"],
-                     cfg["seed"])
+                     cfg["seed"], blk=cfg.get("blk", BLOCK))
 
 
 def selected_pairs(q2k_idx, q2k_num, nb):

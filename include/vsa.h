@@ -1,9 +1,9 @@
 /*
  * vsa.h -- C ABI of the GB300 (sm_103a) block-sparse video attention library (libvsa.so).
  *
- * Block-sparse attention with 64-token blocks ("VSA"): query block i attends only to the kv
- * blocks its q2k row selects, and inside kv block j only to the first variable_block_sizes[j]
- * keys.  The library computes
+ * Block-sparse attention with 64- or 128-token blocks ("VSA"): query block i attends only to
+ * the kv blocks its q2k row selects, and inside kv block j only to the first
+ * variable_block_sizes[j] keys.  The library computes
  *   - the inversion of the block selection (q2k -> k2q),
  *   - the forward (O and the base-2 "M form" log-sum-exp the backward consumes),
  *   - the backward (dQ, dK, dV).
@@ -17,12 +17,17 @@
  *             (reference(), invert_indices_torch()).
  *   [cuDNN]   NVIDIA cudnn-frontend PR #926, Summary (slot validity and clamping) and the
  *             follow-up commit on the no-allocation plan + caller workspace contract.
+ *   [FV-fwd]  FastVideo fastvideo_kernel, the sm_100a/sm_103a forward's description: two
+ *             instantiations, for 64- and 128-token sparse blocks, the block size inferred from
+ *             the metadata.
  *
  * Conventions shared by every entry point:
  *   - Layout: activations are contiguous [B, H, S, 128] bf16 (B batch, H heads, S tokens,
- *     head_dim 128), S = 64 * nb with nb the number of 64-token blocks ([FV-diff]
- *     BlockSparseVsaBwdArgs with VSA_BHSD; the torch binding's "FastVideo pads the sequence up to
- *     whole blocks").  Any nb >= 1 is accepted (no even-nb rule).
+ *     head_dim 128), S = block * nb with nb the number of sparse blocks of `block` tokens (64 or
+ *     128, vsa_shape.block; [FV-diff] BlockSparseVsaBwdArgs with VSA_BHSD; the torch binding's
+ *     "FastVideo pads the sequence up to whole blocks"; [FV-fwd]).  Any nb >= 1 is accepted (no
+ *     even-nb rule).  Block ids, q2k/k2q rows and variable_block_sizes all count blocks of
+ *     `block` tokens.
  *   - Pointers: every buffer is device memory owned and allocated by the caller; activation
  *     and workspace pointers must be 16-byte (activations) / 256-byte (workspace) aligned.
  *     The library never allocates, keeps no per-call state between calls and never
@@ -34,7 +39,7 @@
  *     enqueued ("report an unsupported regime loudly rather than returning plausible-looking
  *     wrong values", [FV-diff] block_sparse_bwd_sm100a.cu).  Problems only visible on the
  *     device never trap: an out-of-range block id is skipped, a count is clamped to its row
- *     width, a block size is clamped to [0, 64] ([cuDNN] Summary: a slot participates only
+ *     width, a block size is clamped to [0, block] ([cuDNN] Summary: a slot participates only
  *     inside the bounded active prefix with its index in [0, nb)), and a bit is set in the
  *     device error word (VSA_DEVERR_*).  Every pipeline wait inside a kernel has a time limit;
  *     a wait that runs out sets VSA_DEVERR_TIMEOUT and the kernel exits (outputs invalid).
@@ -52,7 +57,8 @@ extern "C" {
 typedef enum vsa_status {
   VSA_OK = 0,
   VSA_ERR_INVALID_ARG = 1, /* null pointer, bad size or stride, misalignment, bad sm_scale */
-  VSA_ERR_UNSUPPORTED = 2, /* head_dim != 128, S != 64 * nb, or not an sm_103 device */
+  VSA_ERR_UNSUPPORTED = 2, /* head_dim != 128, block not 64/128, S not a multiple of block, or
+                              not an sm_103 device */
   VSA_ERR_WORKSPACE = 3,   /* workspace NULL, misaligned or smaller than required */
   VSA_ERR_CUDA = 4         /* a CUDA runtime or driver call failed (see vsa_last_cuda_error) */
 } vsa_status;
@@ -62,14 +68,15 @@ typedef enum vsa_status {
 #define VSA_DEVERR_Q2K_COUNT 0x02u /* a q2k count outside [0, topk] was clamped */
 #define VSA_DEVERR_K2Q_ID 0x04u    /* a k2q block id outside [0, nb) was replaced by 0 */
 #define VSA_DEVERR_K2Q_COUNT 0x08u /* a k2q count outside [0, max_q_blocks] was clamped */
-#define VSA_DEVERR_VBS 0x10u       /* a variable_block_sizes entry outside [0, 64] was clamped */
+#define VSA_DEVERR_VBS 0x10u       /* a variable_block_sizes entry outside [0, block] was clamped */
 #define VSA_DEVERR_TIMEOUT 0x20u   /* a pipeline wait ran past its limit; outputs are invalid */
 
 typedef struct vsa_shape {
   int32_t batch;    /* B >= 1 */
   int32_t heads;    /* H >= 1 */
-  int32_t seqlen;   /* S = 64 * nb, nb >= 1 */
+  int32_t seqlen;   /* S = block * nb, nb >= 1 */
   int32_t head_dim; /* must be 128 */
+  int32_t block;    /* tokens per sparse block: 64 or 128 (0 is read as 64) */
 } vsa_shape;
 
 /* Human-readable name of a status code (static storage; never NULL). */
@@ -113,7 +120,7 @@ size_t vsa_fwd_workspace_bytes(vsa_shape shape);
  * A row with no visible key gets O = 0 and lse = -inf.
  *   q, k, v   [B, H, S, 128] bf16 (read).
  *   q2k_idx, q2k_num, topk: the block selection, as for vsa_invert_indices.
- *   vbs       [nb] int32: valid kv tokens per block (clamped to [0, 64]); shared by all (b, h).
+ *   vbs       [nb] int32: valid kv tokens per block (clamped to [0, block]); shared by all (b, h).
  *   sm_scale  finite softmax scale.
  *   o         [B, H, S, 128] bf16 (written, round-to-nearest-even).
  *   lse       [B, H, S] fp32 (written).

@@ -46,13 +46,14 @@ def check_close(name, got, ref64, rel_max=REL_MAX, mean_rel=MEAN_REL):
 def oracle_forward(case, qblocks=None):
     """Oracle O (float64) and lse for a workload case (dict from workloads.make_case)."""
     return orc.fwd(f64(case["q"]), f64(case["k"]), f64(case["v"]), case["q2k_idx"],
-                   case["q2k_num"], case["vbs"], case["sm_scale"], qblocks=qblocks)
+                   case["q2k_num"], case["vbs"], case["sm_scale"], blk=case.get("blk", 64),
+                   qblocks=qblocks)
 
 
 def oracle_backward(case, o_bf16_f64, lse, qblocks=None, kvblocks=None):
     return orc.bwd(f64(case["q"]), f64(case["k"]), f64(case["v"]), o_bf16_f64, f64(case["do"]),
                    lse, case["q2k_idx"], case["q2k_num"], case["vbs"], case["sm_scale"],
-                   qblocks=qblocks, kvblocks=kvblocks)
+                   blk=case.get("blk", 64), qblocks=qblocks, kvblocks=kvblocks)
 
 
 def to_device(case, dev="cuda"):

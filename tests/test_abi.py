@@ -72,6 +72,11 @@ def test_host_side_rejections(vsa):
     # Unsupported head_dim / sequence length.
     assert lib.vsa_bwd(*_bwd_args(vsa, vsa.make_shape(1, 2, 512, 64))) == 2
     assert lib.vsa_bwd(*_bwd_args(vsa, vsa.make_shape(1, 2, 500))) == 2
+    # Block size: 64 or 128 (0 read as 64), and S a multiple of it.
+    assert lib.vsa_bwd(*_bwd_args(vsa, vsa.make_shape(1, 2, 512, 128, 96))) == 2
+    assert lib.vsa_bwd(*_bwd_args(vsa, vsa.make_shape(1, 2, 576, 128, 128))) == 2
+    assert lib.vsa_bwd(*_bwd_args(vsa, vsa.make_shape(1, 2, 512, 128, 128), ws_bytes=1024)) == 3
+    assert lib.vsa_bwd(*_bwd_args(vsa, vsa.make_shape(1, 2, 512, 128, 0), ws_bytes=1024)) == 3
     # Non-finite softmax scale, bad row stride, misaligned pointer.
     assert lib.vsa_bwd(*_bwd_args(vsa, good, scale=math.inf)) == 1
     bad = _bwd_args(vsa, good)

@@ -137,6 +137,13 @@ def _scaled_kv_blocks(case, factor):
     return case
 
 
+# 128-token blocks (each a pair of 64-token tiles with one selection).
+SMALL_CASES["blk128"] = lambda: wl.make_case(1, 2, 4, 2, vbs="ragged65", seed=31, blk=128)
+SMALL_CASES["blk128_odd_nb_topk3"] = lambda: wl.make_case(1, 2, 5, 3, vbs="ragged40", seed=32,
+                                                         blk=128)
+SMALL_CASES["blk128_batch2_zero_kv"] = lambda: wl.make_case(2, 2, 6, 2, vbs="ragged65", seed=33,
+                                                           kv_pool=[0, 2, 3, 5], blk=128)
+
 SMALL_CASES["growing_scores"] = lambda: _scaled_kv_blocks(
     wl.make_case(1, 2, 16, 8, vbs="ragged32", seed=15), lambda j: 1.0 + j)
 SMALL_CASES["shrinking_scores"] = lambda: _scaled_kv_blocks(
@@ -167,12 +174,13 @@ def test_backward_matches_oracle(vsa, name):
     check_close("dk", dk, dk64)
     check_close("dv", dv, dv64)
     # Exact +0.0 for unselected kv blocks and padded kv rows.
-    vbs = np.clip(case["vbs"], 0, 64)
+    blk = case.get("blk", 64)
+    vbs = np.clip(case["vbs"], 0, blk)
     for b in range(case["B"]):
         for h in range(case["H"]):
             for j in range(case["nb"]):
-                lo = 64 * j + (0 if k2q_num[b, h, j] == 0 else int(vbs[j]))
-                rows = slice(lo, 64 * (j + 1))
+                lo = blk * j + (0 if k2q_num[b, h, j] == 0 else int(vbs[j]))
+                rows = slice(lo, blk * (j + 1))
                 assert zero_bits(dk[b, h, rows]).all() and zero_bits(dv[b, h, rows]).all(), (b, h, j)
 
 
@@ -229,6 +237,7 @@ def _head_case(case, b, h):
     sub["q2k_num"] = case["q2k_num"][b:b + 1, h:h + 1]
     sub["vbs"] = case["vbs"]
     sub["sm_scale"] = case["sm_scale"]
+    sub["blk"] = case.get("blk", 64)
     return sub
 
 
@@ -267,8 +276,9 @@ def _full_size(vsa, name, n_heads=2, n_q=3, n_kv=2, seed=0):
         lse32 = lse64.astype(np.float32)
         dq64, dk64, dv64 = oracle_backward(sub, f64(o_b), np.nan_to_num(lse32.astype(np.float64)),
                                            qblocks=q_s, kvblocks=kv_all)
+        blk = case.get("blk", 64)
         for i in q_s:
-            r = slice(64 * i, 64 * (i + 1))
+            r = slice(blk * i, blk * (i + 1))
             results.append(check_close("%s o[%d,%d,q%d]" % (name, b, h, i), o[b, h, r],
                                        o64[0, 0, r]))
             g = lse[b, h, r].cpu().numpy().astype(np.float64)
@@ -276,7 +286,7 @@ def _full_size(vsa, name, n_heads=2, n_q=3, n_kv=2, seed=0):
             results.append(check_close("%s dq[%d,%d,q%d]" % (name, b, h, i), dq[b, h, r],
                                        dq64[0, 0, r]))
         for j in kv_all:
-            r = slice(64 * j, 64 * (j + 1))
+            r = slice(blk * j, blk * (j + 1))
             if cnt[j] == 0:
                 assert zero_bits(dk[b, h, r]).all() and zero_bits(dv[b, h, r]).all()
                 continue
@@ -287,7 +297,8 @@ def _full_size(vsa, name, n_heads=2, n_q=3, n_kv=2, seed=0):
     return dev, case, (o, lse, k2q_idx, k2q_num), (dq, dk, dv)
 
 
-@pytest.mark.parametrize("name", ["32k_25pct", "65k_12pct_zipf", "video_dit_21x30x52"])
+@pytest.mark.parametrize("name", ["32k_25pct", "65k_12pct_zipf", "video_dit_21x30x52",
+                                  "32k_25pct_blk128"])
 def test_full_size_sampled(vsa, name):
     _full_size(vsa, name)
 

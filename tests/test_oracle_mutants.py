@@ -31,6 +31,9 @@ MUTATIONS = {
                        "return n < 0 ? 0 : (n > blk ? blk : n - (n > 1));"),
     "active_prefix_short": ("for (int s = 0; s < cnt; ++s)\n    if (row[s] == j)",
                             "for (int s = 0; s + 1 < cnt; ++s)\n    if (row[s] == j)"),
+    # Right at 64-token blocks only: caught by the 128-token pins.
+    "fwd_key_row_assumes_64": ("long t = (long)j * blk + u;\n          double w = exp2(",
+                               "long t = (long)j * 64 + u;\n          double w = exp2("),
 }
 
 
@@ -53,9 +56,11 @@ class _Bound:
 PIN_TESTS = [
     lambda o: pins.test_invert_golden_fixture(o),
     lambda o: pins.test_invert_brute_force(o, 0),
-    lambda o: pins.test_forward_matches_dense_masked(o, True),
+    lambda o: pins.test_forward_matches_dense_masked(o, True, 64),
+    lambda o: pins.test_forward_matches_dense_masked(o, True, 128),
     lambda o: pins.test_forward_closed_forms(o),
-    lambda o: pins.test_backward_matches_autograd(o, True, None),
+    lambda o: pins.test_backward_matches_autograd(o, True, None, 64),
+    lambda o: pins.test_backward_matches_autograd(o, True, (2,), 128),
     lambda o: pins.test_backward_finite_differences(o),
     lambda o: pins.test_backward_invariants_and_zero_rows(o),
     lambda o: pins.test_backward_closed_forms(o),
