@@ -3,34 +3,34 @@
 // lse = max(qk * sm_scale * log2e) + log2(l); compare main...vsa_bwd_fix, tests,
 // reference(): softmax over the selected blocks with keys past variable_block_sizes masked).
 //
-// Work unit: one (b, h, q pair) item -- q blocks 2x and 2x+1 -- so the UMMA M dimension is 128
-// and row m of every accumulator is TMEM lane m.  The item walks the UNION of the two q blocks'
-// selected kv blocks (ascending); for each row, kv blocks its own q block did not select are
-// masked.  One pass with an online softmax per kv block j:
-//   S = Q_p K_j^T (both operands in shared memory, fp32 accumulator in TMEM);
-//   the row maximum of the block; if it exceeds the row's reference maximum m by more than
-//   RESCALE (log2 units), m moves up to it and the O row and the running sum are scaled by
+// Work unit: one (b, h, q pair) item -- 64-token q tiles 2x and 2x+1 (one 128-token q block when
+// blocks are 128 tokens) -- so the UMMA M dimension is 128 and row m of every accumulator is TMEM
+// lane m.  The item walks the UNION of the two tiles' selected kv tiles (ascending); for each
+// row, kv tiles its own q tile did not select are masked.  The union is taken two kv tiles at a
+// time: S = Q_p [K_a; K_b]^T is one set of 128x128x16 UMMAs (both operands in shared memory,
+// fp32 accumulator in TMEM), and softmax group 0 takes tile a, group 1 tile b.  Per group and kv
+// tile, an online softmax:
+//   the row maximum of the tile; if it exceeds the row's reference maximum m by more than
+//   RESCALE (log2 units), m moves up to it and the group's O row and running sum are scaled by
 //   2^(m_old - m_new) first (otherwise m stays, so P stays below 2^(RESCALE + KPF));
 //   P = 2^(s - m + KPF) in fp16, written to TMEM, where it is the A operand of
-//   O += P V_j (B = V_j from shared memory, MN-major).
-// P never passes through shared memory, so per kv block the tensor pipe reads Q_p, K_j and V_j
+//   O_g += P V_j (B = V_j from shared memory, MN-major).
+// P never passes through shared memory, so per kv tile the tensor pipe reads Q_p, K_j and V_j
 // only.
 //
-// The union's kv blocks alternate between two softmax groups (block t of the CTA goes to group
-// t & 1), each with its own online-softmax state (m, l) and its own O accumulator, the split of
-// the kv range that flash-decoding uses.  The two groups' chains are independent, so one group's
-// softmax overlaps the other's and the tensor pipe always has work queued.  At the end of the
-// item the two partial results merge:
+// Each group has its own online-softmax state (m, l) and its own O accumulator, the split of
+// the kv range that flash-decoding uses, so the two groups work independently.  At the end of
+// the item the two partial results merge:
 //   M = max(m_0, m_1),  w_g = 2^(m_g - M),  O = (w_0 O_0 + w_1 O_1) / (w_0 l_0 + w_1 l_1),
 //   lse = M + log2(w_0 l_0 + w_1 l_1).
 //
 // Roles (352 threads): warps 0-3 softmax group 0 and warps 4-7 group 1 -- warp w owns TMEM lane
 // quarter w % 4 (query rows 32(w%4) .. +31), one full row of S per thread; warp 8 work claimer,
-// TMEM owner and TMA producer of Q and K; warp 9 UMMA issuer, which keeps S two kv blocks ahead
-// of P.V; warp 10 TMA producer of V.  K and V have rings of their own: a K stage is free once S
-// has been computed, two kv blocks before P.V frees the V stage of the same block, so the K
-// loads run that much further ahead.
-// TMEM (512 columns allocated): O x2 [0,256), S x2 [256,384), P x2 [384,448).
+// TMEM owner and TMA producer of Q and K pairs; warp 9 UMMA issuer, which issues S of the next
+// pair as soon as both groups have read S of the current one; warp 10 TMA producer of V.  K and
+// V have rings of their own: a K stage is free once S has been computed, before P.V frees the V
+// stages of the same tiles, so the K loads run further ahead.
+// TMEM (512 columns allocated): O x2 [0,256), S [256,384), P x2 [384,448).
 #include "ptx.cuh"
 #include "queue.cuh"
 #include "vsa_internal.cuh"
