@@ -18,25 +18,28 @@
 // head-dim on the lanes, so each warp's fp32 reduction into the dQ accumulator covers 128
 // contiguous bytes of one query row.
 //
+// Work items are claimed dynamically (queue.cuh).  With 128-token blocks an item is one of the
+// two 64-token kv tiles of a block, and each k2q entry supplies a whole q tile pair.
+//
 // Roles (448 threads):
 //   warps 0-7  softmax: warps w and w+4 share TMEM lane quarter w (query rows 32w..32w+31 of the
-//              pair) and split the 64 kv columns in halves; each thread turns 32 columns of its
-//              S and dP row into P and dS (fp16, swizzled) in shared memory.
-//   warps 8-11 dQ drain + epilogue: thread d owns head-dim row d; moves dQ^T through a 4 KB
-//              per-warp staging box ([32 query rows x 32 head dims] fp32) and adds it into the fp32
-//              accumulator with TMA bulk tensor reductions; at the end of an item writes dK, dV
-//              (bf16, zeros for padded rows; whole zero blocks for items no q block selects).
-//   warp 12    TMA producer (K_j, V_j once per item; Q and dO of each pair into a 2-stage ring);
-//              also allocates TMEM.
-//   warp 13    UMMA issuer (one thread).  Per step g: S/dP(g), then dQ^T(g-1), then (once the
-//              softmax has written P/dS(g)) dV^T/dK^T(g), after which the Q/dO stage of step g is
-//              released -- so a stage's reload has almost a whole step to land, the tensor pipe
-//              works on dQ^T(g-1) while the softmax of step g runs, and the dQ^T drain lags one
-//              step behind in a second TMEM buffer.
+//              pair) and split the 64 kv columns in halves.  Two phases per step: P from S as
+//              soon as S is in TMEM (fp16, swizzled, into shared memory), then dS from dP.
+//   warps 8-11 dQ drain + epilogue: thread d owns head-dim row d; stages dQ^T of each q tile in
+//              an 8 KB per-warp box ([64 query rows x 32 head dims] fp32) and adds it into the
+//              fp32 accumulator with one TMA bulk tensor reduction; at the end of an item writes
+//              dK, dV (bf16, zeros for padded rows; whole zero blocks for unselected kv tiles).
+//   warp 12    TMA producer and work claimer (K_j, V_j once per item; Q and dO of each pair into
+//              a 2-stage ring, each tile issued from its own lane); also allocates TMEM.
+//   warp 13    UMMA issuer, warp-wide (all lanes poll, one elected lane issues).  Per step g the
+//              tensor pipe runs dV^T(g), S(g+1), dK^T(g), dP(g+1), dQ^T(g): dV^T waits for P,
+//              dK^T for dS, so the softmax of step g+1 overlaps dK^T, dP and dQ^T of step g, and
+//              the drain of dQ^T(g) overlaps step g+1 in a second TMEM buffer.
 // TMEM (512 columns): S [0,64), dP [64,128), dV^T [128,192), dK^T [192,256),
-// dQ^T x2 [256,512).  Shared memory: K_j, V_j; a 2-stage Q/dO ring; P (one buffer: when the
-// softmax sees S/dP(g) complete, dV^T(g-1), the only reader of P(g-1), has completed too); dS
-// (two buffers: dQ^T(g-1) still reads dS(g-1) while the softmax of step g runs); dQ staging.
+// dQ^T x2 [256,512).  Shared memory: K_j, V_j; a 2-stage Q/dO ring; P and dS (one buffer each:
+// the tensor pipe runs in issue order, so S(g) completing means dV^T(g-1) has read P(g-1), and
+// the softmax writes dS(g) only after dQ^T(g-1) has read dS(g-1), a barrier it waits on); dQ
+// staging.
 #include <cudaTypedefs.h>
 
 #include "ptx.cuh"
