@@ -396,38 +396,63 @@ def main():
     fpp = flop_per_pair(case.get("blk", 64))
     value = all_pairs * fpp / (total_ms / K / 1e3) / 1e12
 
-    # End to end through the public API with host buffers.
+    # End to end through the public API with host buffers.  Every step uploads its inputs from
+    # pinned host memory and downloads its three gradients; inputs and outputs are
+    # double-buffered on the device and the copies run on their own streams, so the upload of
+    # step k+1 and the download of step k-1 overlap the kernels of step k.
     host_in = {n: dev[n].cpu().pin_memory() for n in ("q", "k", "v", "do")}
     host_in["o"] = o.cpu().pin_memory()
     host_in["lse"] = lse.cpu().pin_memory()
     host_in["q2k_idx"] = q2k_idx.cpu().pin_memory()
     host_in["q2k_num"] = q2k_num.cpu().pin_memory()
     host_in["vbs"] = vbs.cpu().pin_memory()
-    dev_in = {n: torch.empty_like(t, device=device) for n, t in host_in.items()}
+    dev_in = [{n: torch.empty_like(t, device=device) for n, t in host_in.items()}
+              for _ in range(2)]
+    dev_out = [[torch.empty_like(dq) for _ in range(3)] for _ in range(2)]
     host_out = [torch.empty(dq.shape, dtype=dq.dtype).pin_memory() for _ in range(3)]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out)
+    s_up, s_down = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    ev = {k_: [torch.cuda.Event() for _ in range(2)]
+          for k_ in ("in_ready", "in_free", "out_ready", "out_free")}
+    for b_ in range(2):   # all buffers start free
+        ev["in_free"][b_].record(stream)
+        ev["out_free"][b_].record(stream)
 
-    def e2e_step():
-        for n, t in host_in.items():
-            dev_in[n].copy_(t, non_blocking=True)
-        vsa.vsa_invert_indices(dev_in["q2k_idx"], dev_in["q2k_num"], nb, k2q_idx, k2q_num)
-        vsa.vsa_bwd(dev_in["do"], dev_in["q"], dev_in["k"], dev_in["v"], dev_in["o"],
-                    dev_in["lse"], k2q_idx, k2q_num, dev_in["vbs"], sc, dq=dq, dk=dk, dv=dv,
-                    workspace=ws)
-        for h_, d_ in zip(host_out, (dq, dk, dv)):
-            h_.copy_(d_, non_blocking=True)
+    def e2e_step(k_):
+        b_ = k_ & 1
+        di, do_ = dev_in[b_], dev_out[b_]
+        with torch.cuda.stream(s_up):
+            s_up.wait_event(ev["in_free"][b_])
+            for n, t in host_in.items():
+                di[n].copy_(t, non_blocking=True)
+            ev["in_ready"][b_].record(s_up)
+        stream.wait_event(ev["in_ready"][b_])
+        stream.wait_event(ev["out_free"][b_])
+        vsa.vsa_invert_indices(di["q2k_idx"], di["q2k_num"], nb, k2q_idx, k2q_num)
+        vsa.vsa_bwd(di["do"], di["q"], di["k"], di["v"], di["o"], di["lse"], k2q_idx, k2q_num,
+                    di["vbs"], sc, dq=do_[0], dk=do_[1], dv=do_[2], workspace=ws)
+        ev["in_free"][b_].record(stream)
+        ev["out_ready"][b_].record(stream)
+        with torch.cuda.stream(s_down):
+            s_down.wait_event(ev["out_ready"][b_])
+            for h_, d_ in zip(host_out, do_):
+                h_.copy_(d_, non_blocking=True)
+            ev["out_free"][b_].record(s_down)
 
-    for _ in range(3):
-        e2e_step()
+    for k_ in range(3):
+        e2e_step(k_)
     torch.cuda.synchronize()
     K_e2e = max(3, min(K, 50))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist, device)
     torch.cuda.synchronize()
     e0.record(stream)
-    for _ in range(K_e2e):
-        e2e_step()
+    s_up.wait_event(e0)
+    s_down.wait_event(e0)
+    for k_ in range(K_e2e):
+        e2e_step(k_)
+    stream.wait_event(ev["out_free"][(K_e2e - 1) & 1])   # the last download is inside
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(dist, device)
@@ -497,7 +522,9 @@ def main():
                        "note": "forward + inversion + backward through the autograd binding; "
                                "2 + 5 GEMMs per selected pair"},
         "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": K_e2e},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": K_e2e,
+                "copies": "every step uploads its inputs and downloads dQ, dK, dV; double "
+                          "buffers on copy streams overlap them with the neighbouring steps"},
         "gpu_launches": kernels_per_step * K,
         "clocks": clocks,
         "cpu_baseline": cpu,
