@@ -160,6 +160,58 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Packed fp32 pairs (sm_100 family): one instruction operates on both halves of a 64-bit
+// register pair, each half rounded as the scalar instruction would.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float min3(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Maximum / minimum of 64 raw fp32 scores, four independent chains of 3-input instructions.
+__device__ __forceinline__ float row_max64(const uint32_t* sv) {
+  float m[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) m[k] = fmaxf(__uint_as_float(sv[2 * k]), __uint_as_float(sv[2 * k + 1]));
+#pragma unroll
+  for (int u = 8; u < 64; u += 2)
+    m[(u >> 1) & 3] = max3(m[(u >> 1) & 3], __uint_as_float(sv[u]), __uint_as_float(sv[u + 1]));
+  return max3(fmaxf(m[0], m[1]), m[2], m[3]);
+}
+__device__ __forceinline__ float row_min64(const uint32_t* sv) {
+  float m[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) m[k] = fminf(__uint_as_float(sv[2 * k]), __uint_as_float(sv[2 * k + 1]));
+#pragma unroll
+  for (int u = 8; u < 64; u += 2)
+    m[(u >> 1) & 3] = min3(m[(u >> 1) & 3], __uint_as_float(sv[u]), __uint_as_float(sv[u + 1]));
+  return min3(fminf(m[0], m[1]), m[2], m[3]);
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -458,6 +510,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t t_o = tmem + lane_off + TM_O + grp * 128u;
     float2* xch = reinterpret_cast<float2*>(gbase + SM_XCH);  // [item parity][group][row] (m, l)
     uint32_t pc = 0, bc = 0, itc = 0;  // kv-block pairs; this group's kv blocks; items
+    bool p_zero = false;               // the warp's lanes of P buffer grp hold zeros
     for (uint32_t k = 0;; ++k) {
       int w;
       if (!warp_take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, lane, &w)) {
@@ -497,8 +550,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           return true;
         }
         tc_fence_after_sync();
+        // Warp-uniform: the warp's 32 rows belong to one q tile.
         const bool mine = valid && ((own[j >> 5] >> (j & 31)) & 1u);
         const int vb = mine ? clamp_vbs(p.vbs[j]) : 0;  // visible columns of the row
+        if (vb == 0) {
+          // Nothing of this kv tile is visible to the warp's rows (the other q tile of the pair
+          // selected it, or the tile is empty): S is not read, m and l stay, and P is zero,
+          // which the buffer may already hold from the group's previous block.
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(S_FREE));
+          if (!warp_wait(bar(P_FREE0 + grp), (bc & 1u) ^ 1u, abort, lane)) return false;
+          if (!p_zero) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int u = 0; u < 32; ++u) pk[u] = 0u;
+            tmem_st_32x32b_x32(t_p, pk);
+            tmem_wait_st();
+            p_zero = true;
+          }
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(P_READY0 + grp));
+          ++bc;
+          first = false;
+          return true;
+        }
         uint32_t sv[64];
         tmem_ld_32x32b_x32(t_s, sv);
         tmem_ld_32x32b_x32(t_s + 32u, sv + 32);
@@ -506,10 +583,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(S_FREE));
-        float mb = -INFINITY;  // the row's maximum over this kv block
+        // The row's maximum of s over this kv tile: the extremum of the raw scores, scaled once
+        // (c1 > 0: max; c1 < 0: min), in 3-input max/min instructions.  Few ALU instructions per
+        // element keep this warp from crowding out the UMMA and TMA warps that share its
+        // scheduler.
+        // Columns past the tile's valid count are masked by setting their raw score to the
+        // value that scales to -inf (so they neither win the maximum nor contribute to P); with
+        // c1 = 0 that does not work and the per-column path below masks instead.
+        const bool fast = c1 != 0.f;
+        if (fast && vb < BLOCK) {
+          const uint32_t pad = c1 > 0.f ? 0xff800000u : 0x7f800000u;  // -inf : +inf
 #pragma unroll
-        for (int u = 0; u < 64; ++u)
-          if (u < vb) mb = fmaxf(mb, __uint_as_float(sv[u]) * c1);
+          for (int u = 0; u < 64; ++u)
+            if (u >= vb) sv[u] = pad;
+        }
+        float mb;
+        if (fast) {
+          mb = c1 * (c1 > 0.f ? row_max64(sv) : row_min64(sv));
+        } else {
+          mb = -INFINITY;
+#pragma unroll
+          for (int u = 0; u < 64; ++u)
+            if (u < vb) mb = fmaxf(mb, __uint_as_float(sv[u]) * c1);
+        }
         const bool need = mb > m + RESCALE;
         // P buffer grp is free once the group's previous P.V has completed, and then O_grp
         // holds every block of the group so far.
@@ -534,17 +630,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         const float off = static_cast<float>(KPF) - m;
         uint32_t pk[32];
-        float acc = 0.f;
+        if (fast) {
+          // Two columns per packed fp32x2 FMA and add.
+          const uint64_t c2 = f2_pack(c1, c1), o2 = f2_pack(off, off);
+          uint64_t acc2 = f2_pack(0.f, 0.f);
 #pragma unroll
-        for (int u = 0; u < 64; u += 2) {
-          const float p0 = (u < vb) ? ex2(fmaf(__uint_as_float(sv[u]), c1, off)) : 0.f;
-          const float p1 = (u + 1 < vb) ? ex2(fmaf(__uint_as_float(sv[u + 1]), c1, off)) : 0.f;
-          acc += p0 + p1;
-          pk[u >> 1] = pack_half2(p0, p1);
+          for (int u = 0; u < 64; u += 2) {
+            float a0, a1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[u]), __uint_as_float(sv[u + 1])), c2, o2),
+                      a0, a1);
+            const float p0 = ex2(a0), p1 = ex2(a1);
+            acc2 = f2_add(acc2, f2_pack(p0, p1));
+            pk[u >> 1] = pack_half2(p0, p1);
+          }
+          float s0, s1;
+          f2_unpack(acc2, s0, s1);
+          l += s0 + s1;
+        } else {
+          float acc = 0.f;
+#pragma unroll
+          for (int u = 0; u < 64; u += 2) {
+            const float p0 = (u < vb) ? ex2(fmaf(__uint_as_float(sv[u]), c1, off)) : 0.f;
+            const float p1 = (u + 1 < vb) ? ex2(fmaf(__uint_as_float(sv[u + 1]), c1, off)) : 0.f;
+            acc += p0 + p1;
+            pk[u >> 1] = pack_half2(p0, p1);
+          }
+          l += acc;
         }
-        l += acc;
         tmem_st_32x32b_x32(t_p, pk);
         tmem_wait_st();
+        p_zero = false;
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(P_READY0 + grp));
