@@ -26,11 +26,18 @@
 //
 // Roles (352 threads): warps 0-3 softmax group 0 and warps 4-7 group 1 -- warp w owns TMEM lane
 // quarter w % 4 (query rows 32(w%4) .. +31), one full row of S per thread; warp 8 work claimer,
-// TMEM owner and TMA producer of Q and K pairs; warp 9 UMMA issuer, which issues S of the next
-// pair as soon as both groups have read S of the current one; warp 10 TMA producer of V.  K and
-// V have rings of their own: a K stage is free once S has been computed, before P.V frees the V
-// stages of the same tiles, so the K loads run further ahead.
-// TMEM (512 columns allocated): O x2 [0,256), S [256,384), P x2 [384,448).
+// TMEM owner and TMA producer of Q and K pairs; warp 9 UMMA issuer; warp 10 TMA producer of V.
+// S is double-buffered in TMEM: pair p uses buffer p & 1, and each group writes its P (fp16
+// pairs, 32 columns) over the first half of its own 64 S columns once it holds them in
+// registers, so P.V reads its A operand from there.  The tensor pipe runs
+//   S(p+1)  P.V(p) (group 0, then group 1)  S(p+2)  P.V(p+1) ...
+// S(p+2) waits until both P.V of pair p have completed (the buffer is free again), so while the
+// softmax works on pair p+1 the tensor pipe already has S(p+2) to do.  K and V have rings of
+// their own: a K stage is free once S has been computed, before P.V frees the V stages of the
+// same tiles, so the K loads run further ahead.
+// Every softmax warp takes part in every pair (a group without a tile in a pair only signals
+// that it has none), so no barrier can complete two phases while a waiter looks at it.
+// TMEM (512 columns allocated): O x2 [0,256), S x2 [256,512).
 #include "ptx.cuh"
 #include "queue.cuh"
 #include "vsa_internal.cuh"
@@ -44,7 +51,7 @@ constexpr int SOFTMAX_WARPS = 8;
 constexpr int TMA_WARP = 8;
 constexpr int MMA_WARP = 9;
 constexpr int V_WARP = 10;
-constexpr int K_STAGES = 2;  // stages of a PAIR of kv blocks (32 KB each)
+constexpr int K_STAGES = 2;  // stages of a PAIR of kv blocks (32 KB each), one per S buffer
 constexpr int V_STAGES = 5;
 constexpr int KPF = 7;               // P is carried as P * 2^KPF: below 2^(RESCALE + KPF) = 2^15
 constexpr float RESCALE = 8.0f;      // log2 units the block maximum may exceed m by before a rescale
@@ -59,14 +66,14 @@ enum Bar : uint32_t {
   Q_FULL0 = 0,
   Q_EMPTY0 = Q_FULL0 + 2,
   K_FULL0 = Q_EMPTY0 + 2,
-  K_EMPTY0 = K_FULL0 + K_STAGES,
-  V_FULL0 = K_EMPTY0 + K_STAGES,
+  V_FULL0 = K_FULL0 + K_STAGES,
   V_EMPTY0 = V_FULL0 + V_STAGES,
-  S_FULL = V_EMPTY0 + V_STAGES,  // S of a kv-block pair is in TMEM
-  S_FREE,                        // ... and has been read by both groups
-  P_READY0,
-  P_FREE0 = P_READY0 + 2,
-  O_FULL = P_FREE0 + 2,
+  S_FULL0 = V_EMPTY0 + V_STAGES,  // S(p) is in TMEM buffer p & 1 (and K stage p & 1 is free)
+  BUF_FREE0 = S_FULL0 + 2,        // both P.V of pair p have completed: buffer p & 1 is free
+  // Per group and pair parity: P of the pair is in TMEM (or the group has none).  Alternating
+  // barriers keep a warp that runs ahead to pair p + 1 from arriving in pair p's phase.
+  P_READY0 = BUF_FREE0 + 2,
+  O_FULL = P_READY0 + 4,
   O_EMPTY,
   DRAIN,
   XCH0,  // one per lane quarter: both groups' warps have published (m, l) of the item
@@ -83,7 +90,8 @@ constexpr uint32_t SM_QUEUE = SM_ABORT + 4;
 constexpr uint32_t SMEM_BYTES = SM_QUEUE + 4 * ITEM_SLOTS + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-constexpr uint32_t TM_O = 0, TM_S = 256, TM_P = 384;  // O, P x2: group g at + g * width
+static_assert(K_STAGES == 2, "K stages pair up with the two S buffers");
+constexpr uint32_t TM_O = 0, TM_S = 256;  // O_g at TM_O + 128 g; S buffer b at TM_S + 128 b
 constexpr uint32_t IDESC_S = idesc_f16_f32acc(128, 128, false, false);
 constexpr uint32_t IDESC_PV = idesc_f16_f32acc(128, 128, false, true);
 
@@ -241,19 +249,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(Q_FULL0 + s), 1);
       mbar_init(bar(Q_EMPTY0 + s), 1);
-      mbar_init(bar(P_READY0 + s), GROUP_WARPS);
-      mbar_init(bar(P_FREE0 + s), 1);
+      mbar_init(bar(S_FULL0 + s), 1);
+      mbar_init(bar(BUF_FREE0 + s), 1);
+      mbar_init(bar(P_READY0 + 2 * s), GROUP_WARPS);
+      mbar_init(bar(P_READY0 + 2 * s + 1), GROUP_WARPS);
     }
-    for (int s = 0; s < K_STAGES; ++s) {
-      mbar_init(bar(K_FULL0 + s), 1);
-      mbar_init(bar(K_EMPTY0 + s), 1);
-    }
+    for (int s = 0; s < K_STAGES; ++s) mbar_init(bar(K_FULL0 + s), 1);
     for (int s = 0; s < V_STAGES; ++s) {
       mbar_init(bar(V_FULL0 + s), 1);
       mbar_init(bar(V_EMPTY0 + s), 1);
     }
-    mbar_init(bar(S_FULL), 1);
-    mbar_init(bar(S_FREE), SOFTMAX_WARPS);
     mbar_init(bar(O_FULL), 1);
     mbar_init(bar(O_EMPTY), SOFTMAX_WARPS);
     mbar_init(bar(DRAIN), 1);
@@ -317,7 +322,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int ja = -1, e = 0;
       auto load_pair = [&](int j0, int j1) -> bool {
         const uint32_t st = lg % K_STAGES;
-        if (!mbar_wait_warp(bar(K_EMPTY0 + st), ((lg / K_STAGES) & 1u) ^ 1u, abort,
+        if (!mbar_wait_warp(bar(S_FULL0 + st), ((lg / K_STAGES) & 1u) ^ 1u, abort,
                             WAIT_LIMIT_NS))
           return false;
         if (lane == 0) mbar_arrive_expect_tx(bar(K_FULL0 + st), j1 >= 0 ? 32768u : 16384u);
@@ -399,23 +404,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------------ UMMA issuer
     // The whole warp runs this role in lockstep; every lane polls the barriers and one elected
     // lane issues each UMMA and commit.
-    uint32_t pc = 0, vc = 0, itc = 0;  // kv-block pairs (S), kv blocks (P.V), items
-    uint32_t bc[2] = {0, 0};           // kv blocks of each softmax group
+    uint32_t pc = 0, vc = 0, itc = 0;  // kv-tile pairs (S), kv tiles (P.V), items
     bool ok = true, issued = false;
     const uint64_t q_kmaj = sdesc_sw128(base + SM_Q, 16, 1024);
     const uint64_t k_kmaj = sdesc_sw128(base + SM_K, 16, 1024);   // K pair of stage 0
     const uint64_t v_mn = sdesc_sw128(base + SM_V, 8192, 1024);   // V of stage 0
-    // S = Q_p [K_a; K_b]^T of kv-block pair pb (N = 128: columns 0-63 block a, 64-127 block b);
-    // Q from stage qs.
+    // S(pb) = Q_p [K_a; K_b]^T (N = 128: columns 0-63 tile a, 64-127 tile b) into TMEM buffer
+    // pb & 1, once K stage pb & 1 is loaded and both P.V of pair pb - 2 (which read their P from
+    // that buffer) have completed.  Q from stage qs.
     auto issue_s = [&](uint32_t pb, uint32_t qs) -> bool {
-      const uint32_t st = pb % K_STAGES;
-      if (!mbar_wait_warp(bar(K_FULL0 + st), (pb / K_STAGES) & 1u, abort, WAIT_LIMIT_NS))
+      const uint32_t b = pb & 1u;
+      if (!mbar_wait2_warp(bar(K_FULL0 + b), (pb >> 1) & 1u, bar(BUF_FREE0 + b),
+                           ((pb >> 1) & 1u) ^ 1u, abort, WAIT_LIMIT_NS))
         return false;
-      if (!mbar_wait_warp(bar(S_FREE), (pb & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) return false;
       tc_fence_after_sync();
       const uint64_t qa = sdesc_advance(q_kmaj, qs * 32768u);
-      const uint64_t kd = sdesc_advance(k_kmaj, st * 32768u);
-      const uint32_t ts = tmem + TM_S;
+      const uint64_t kd = sdesc_advance(k_kmaj, b * 32768u);
+      const uint32_t ts = tmem + TM_S + b * 128u;
       umma_ss_elect<false>(ts, qa, kd, IDESC_S);
 #pragma unroll
       for (int kk = 1; kk < 8; ++kk) {
@@ -423,24 +428,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         umma_ss_elect<true>(ts, sdesc_advance(qa, (kk >> 2) * 16384u + off),
                             sdesc_advance(kd, (kk >> 2) * 16384u + off), IDESC_S);
       }
-      umma_commit_elect(bar(S_FULL));
-      umma_commit_elect(bar(K_EMPTY0 + st));
+      // One commit: it tells the softmax that S is ready and the K producer that the stage is
+      // free (a commit issued behind a pending one holds this warp until the first completes).
+      umma_commit_elect(bar(S_FULL0 + b));
       issued = true;
       return true;
     };
-    // O_g += P V_j of the group's next kv block (V stage from the global block count): A = P
-    // buffer g in TMEM (8 columns per 16 kv), B = V_j.  `fresh`: the group's first block of the
-    // item overwrites O_g; `first`: the item's first P.V waits until the previous item's O
-    // buffers have been read.
-    auto issue_pv = [&](uint32_t g, bool fresh, bool first) -> bool {
+    // O_g += P_g V_j for group g's kv tile of pair pb (V stage from the global tile count): A =
+    // P_g in TMEM (columns 64 g .. 64 g + 31 of buffer pb & 1, 8 columns per 16 kv), B = V_j.
+    // `fresh`: the group's first tile of the item overwrites O_g.  Waits for V and for the
+    // group's P of the pair.
+    auto issue_pv = [&](uint32_t pb, uint32_t g, bool fresh) -> bool {
       const uint32_t st = vc % V_STAGES;
-      if (!mbar_wait_warp(bar(V_FULL0 + st), (vc / V_STAGES) & 1u, abort, WAIT_LIMIT_NS))
-        return false;
-      if (!mbar_wait_warp(bar(P_READY0 + g), bc[g] & 1u, abort, WAIT_LIMIT_NS)) return false;
-      if (first && !mbar_wait_warp(bar(O_EMPTY), (itc & 1u) ^ 1u, abort, WAIT_LIMIT_NS))
+      if (!mbar_wait2_warp(bar(V_FULL0 + st), (vc / V_STAGES) & 1u,
+                           bar(P_READY0 + 2 * g + (pb & 1u)), (pb >> 1) & 1u, abort,
+                           WAIT_LIMIT_NS))
         return false;
       tc_fence_after_sync();
-      const uint32_t pa = tmem + TM_P + g * 32u, to = tmem + TM_O + g * 128u;
+      const uint32_t pa = tmem + TM_S + (pb & 1u) * 128u + g * 64u, to = tmem + TM_O + g * 128u;
       const uint64_t vb = sdesc_advance(v_mn, st * 16384u);
       if (fresh)
         umma_ts_elect<false>(to, pa, vb, IDESC_PV);
@@ -449,10 +454,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
       for (int kk = 1; kk < 4; ++kk)
         umma_ts_elect<true>(to, pa + kk * 8u, sdesc_advance(vb, kk * 2048u), IDESC_PV);
-      umma_commit_elect(bar(P_FREE0 + g));
       umma_commit_elect(bar(V_EMPTY0 + st));
       ++vc;
-      ++bc[g];
       return true;
     };
     for (uint32_t k = 0;; ++k) {
@@ -471,21 +474,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ok = false;
         break;
       }
-      // S of pair p+1 goes in as soon as both groups have read S of pair p, ahead of the two
-      // P.V of pair p (group 0: block 2p, group 1: block 2p+1).
       const uint32_t p0 = pc;
       ok = issue_s(p0, qs);
       for (int pr = 0; pr < npr && ok; ++pr) {
+        const uint32_t pb = p0 + pr;
         if (pr + 1 < npr) {
-          if (!issue_s(p0 + pr + 1, qs)) {
+          if (!issue_s(pb + 1, qs)) {
             ok = false;
             break;
           }
         } else {
           umma_commit_elect(bar(Q_EMPTY0 + qs));  // every S of the item has been issued
         }
-        ok = issue_pv(0, pr == 0, pr == 0);
-        if (ok && 2 * pr + 1 < nu) ok = issue_pv(1, pr == 0, false);
+        // Group 0 always has a tile; the item's first P.V also waits until the previous item's
+        // O buffers have been read.  Group 1 signals every pair, also when the union's odd last
+        // tile leaves it none.
+        ok = (pr != 0 || mbar_wait_warp(bar(O_EMPTY), (itc & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) &&
+             issue_pv(pb, 0, pr == 0);
+        if (ok)
+          ok = (2 * pr + 1 < nu)
+                   ? issue_pv(pb, 1, pr == 0)
+                   : mbar_wait_warp(bar(P_READY0 + 2 + (pb & 1u)), (pb >> 1) & 1u, abort,
+                                    WAIT_LIMIT_NS);
+        if (ok) umma_commit_elect(bar(BUF_FREE0 + (pb & 1u)));
       }
       if (!ok) break;
       umma_commit_elect(bar(O_FULL));
@@ -505,12 +516,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int quarter = warp & 3, grp = warp >> 2;  // TMEM lane quarter; softmax group
     const int r = quarter * 32 + lane;              // query row of the pair == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t t_s = tmem + lane_off + TM_S + grp * 64u;
-    const uint32_t t_p = tmem + lane_off + TM_P + grp * 32u;
     const uint32_t t_o = tmem + lane_off + TM_O + grp * 128u;
     float2* xch = reinterpret_cast<float2*>(gbase + SM_XCH);  // [item parity][group][row] (m, l)
-    uint32_t pc = 0, bc = 0, itc = 0;  // kv-block pairs; this group's kv blocks; items
-    bool p_zero = false;               // the warp's lanes of P buffer grp hold zeros
+    uint32_t pc = 0, itc = 0;  // kv-tile pairs; items
     for (uint32_t k = 0;; ++k) {
       int w;
       if (!warp_take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, lane, &w)) {
@@ -539,40 +547,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const float c1 = p.sm_scale * LOG2E_F * exp2i(eq + ek);  // S' -> s (log2 units)
       float m = -INFINITY, l = 0.f;  // this group's reference maximum and sum of P * 2^KPF
       bool first = true;             // no block of this group in the item yet
-      // The union's kv blocks in pairs (block 2p for group 0, 2p+1 for group 1).
+      // The union's kv tiles in pairs (tile 2p for group 0, 2p+1 for group 1); j < 0: the
+      // group has no tile in this pair (the union's odd last tile goes to group 0).
       auto do_pair = [&](int j) -> bool {
-        if (!warp_wait(bar(S_FULL), pc & 1u, abort, lane)) return false;
-        ++pc;
-        if (j < 0) {  // odd tail: group 1 has no block, but S is free as far as it is concerned
+        const uint32_t pb = pc++;
+        const uint32_t b = pb & 1u;
+        if (!warp_wait(bar(S_FULL0 + b), (pb >> 1) & 1u, abort, lane)) return false;
+        tc_fence_after_sync();
+        // S of this group's tile, then its P over the first 32 of those columns.
+        const uint32_t t_s = tmem + lane_off + TM_S + b * 128u + grp * 64u;
+        // Both P.V of the previous pair have completed: O_grp holds every tile so far (needed
+        // before a rescale only).  The barrier cannot be a phase behind (S(pb) was issued after
+        // the UMMA warp had seen pair pb - 3 complete) nor a phase ahead (pair pb + 1 needs this
+        // warp's P), so skipping the wait when nothing is rescaled is safe.
+        auto wait_prev = [&]() -> bool {
+          return pb == 0 ||
+                 warp_wait(bar(BUF_FREE0 + ((pb - 1) & 1u)), ((pb - 1) >> 1) & 1u, abort, lane);
+        };
+        auto ready = [&]() {
           tc_fence_before_sync();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar(S_FREE));
+          if (lane == 0) mbar_arrive(bar(P_READY0 + 2 * grp + b));
+        };
+        if (j < 0) {
+          ready();
           return true;
         }
-        tc_fence_after_sync();
         // Warp-uniform: the warp's 32 rows belong to one q tile.
         const bool mine = valid && ((own[j >> 5] >> (j & 31)) & 1u);
         const int vb = mine ? clamp_vbs(p.vbs[j]) : 0;  // visible columns of the row
+        uint32_t pk[32];
         if (vb == 0) {
           // Nothing of this kv tile is visible to the warp's rows (the other q tile of the pair
-          // selected it, or the tile is empty): S is not read, m and l stay, and P is zero,
-          // which the buffer may already hold from the group's previous block.
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(S_FREE));
-          if (!warp_wait(bar(P_FREE0 + grp), (bc & 1u) ^ 1u, abort, lane)) return false;
-          if (!p_zero) {
-            uint32_t pk[32];
+          // selected it, or the tile is empty): S is not read, m and l stay, and P is zero.
 #pragma unroll
-            for (int u = 0; u < 32; ++u) pk[u] = 0u;
-            tmem_st_32x32b_x32(t_p, pk);
-            tmem_wait_st();
-            p_zero = true;
-          }
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(P_READY0 + grp));
-          ++bc;
+          for (int u = 0; u < 32; ++u) pk[u] = 0u;
+          tmem_st_32x32b_x32(t_s, pk);
+          tmem_wait_st();
+          ready();
           first = false;
           return true;
         }
@@ -580,13 +592,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_ld_32x32b_x32(t_s, sv);
         tmem_ld_32x32b_x32(t_s + 32u, sv + 32);
         tmem_wait_ld();
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(S_FREE));
-        // The row's maximum of s over this kv tile: the extremum of the raw scores, scaled once
-        // (c1 > 0: max; c1 < 0: min), in 3-input max/min instructions.  Few ALU instructions per
-        // element keep this warp from crowding out the UMMA and TMA warps that share its
-        // scheduler.
         // Columns past the tile's valid count are masked by setting their raw score to the
         // value that scales to -inf (so they neither win the maximum nor contribute to P); with
         // c1 = 0 that does not work and the per-column path below masks instead.
@@ -597,6 +602,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int u = 0; u < 64; ++u)
             if (u >= vb) sv[u] = pad;
         }
+        // The row's maximum of s over this kv tile: the extremum of the raw scores, scaled once
+        // (c1 > 0: max; c1 < 0: min), in 3-input max/min instructions.  Few ALU instructions per
+        // element keep this warp from crowding out the UMMA and TMA warps that share its
+        // scheduler.
         float mb;
         if (fast) {
           mb = c1 * (c1 > 0.f ? row_max64(sv) : row_min64(sv));
@@ -607,29 +616,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (u < vb) mb = fmaxf(mb, __uint_as_float(sv[u]) * c1);
         }
         const bool need = mb > m + RESCALE;
-        // P buffer grp is free once the group's previous P.V has completed, and then O_grp
-        // holds every block of the group so far.
-        if (!warp_wait(bar(P_FREE0 + grp), (bc & 1u) ^ 1u, abort, lane)) return false;
-        if (__any_sync(0xffffffffu, need)) {
-          const float f = need ? ex2(m - mb) : 1.f;  // m = -inf: f = 0 (nothing accumulated)
-          if (!first) {
-            tc_fence_after_sync();
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-              uint32_t ov[32];
-              tmem_ld_32x32b_x32(t_o + c * 32u, ov);
-              tmem_wait_ld();
-#pragma unroll
-              for (int u = 0; u < 32; ++u) ov[u] = __float_as_uint(__uint_as_float(ov[u]) * f);
-              tmem_st_32x32b_x32(t_o + c * 32u, ov);
-            }
-            tmem_wait_st();
-          }
+        const bool any_need = __any_sync(0xffffffffu, need);
+        float f = 1.f;  // factor for O_grp and l (m = -inf: f = 0, nothing accumulated yet)
+        if (any_need) {
+          f = need ? ex2(m - mb) : 1.f;
           l *= f;
           if (need) m = mb;
         }
         const float off = static_cast<float>(KPF) - m;
-        uint32_t pk[32];
         if (fast) {
           // Two columns per packed fp32x2 FMA and add.
           const uint64_t c2 = f2_pack(c1, c1), o2 = f2_pack(off, off);
@@ -657,13 +651,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           l += acc;
         }
-        tmem_st_32x32b_x32(t_p, pk);
+        if (any_need && !first) {
+          if (!wait_prev()) return false;
+          tc_fence_after_sync();
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t ov[32];
+            tmem_ld_32x32b_x32(t_o + c * 32u, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 32; ++u) ov[u] = __float_as_uint(__uint_as_float(ov[u]) * f);
+            tmem_st_32x32b_x32(t_o + c * 32u, ov);
+          }
+        }
+        tmem_st_32x32b_x32(t_s, pk);
         tmem_wait_st();
-        p_zero = false;
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(P_READY0 + grp));
-        ++bc;
+        ready();
         first = false;
         return true;
       };

@@ -77,6 +77,29 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, vo
   return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abort, limit_ns));
 }
 
+// mbar_wait_warp on two barriers at once: both first probes go out back to back, so the two
+// round trips overlap (a probe of a completed barrier still costs tens of cycles).
+__device__ __forceinline__ bool mbar_wait2_warp(uint32_t bar_a, uint32_t parity_a, uint32_t bar_b,
+                                                uint32_t parity_b, volatile int* abort,
+                                                uint64_t limit_ns) {
+  bool da = mbar_try_wait(bar_a, parity_a);
+  bool db = mbar_try_wait(bar_b, parity_b);
+  bool ok = true;
+  if (!(da && db)) {
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+      if (!da) da = mbar_try_wait(bar_a, parity_a);
+      if (!db) db = mbar_try_wait(bar_b, parity_b);
+      if (da && db) break;
+      if (*abort || globaltimer_ns() - t0 > limit_ns) {
+        ok = false;
+        break;
+      }
+    }
+  }
+  return __all_sync(0xffffffffu, ok);
+}
+
 // ------------------------------------------------------------------------------ proxy fences
 
 // Generic-proxy writes to shared memory become visible to the async proxy (UMMA, TMA).
