@@ -29,8 +29,9 @@
 //              an 8 KB per-warp box ([64 query rows x 32 head dims] fp32) and adds it into the
 //              fp32 accumulator with one TMA bulk tensor reduction; at the end of an item writes
 //              dK, dV (bf16, zeros for padded rows; whole zero blocks for unselected kv tiles).
-//   warp 12    TMA producer and work claimer (K_j, V_j once per item; Q and dO of each pair into
-//              a 2-stage ring, each tile issued from its own lane); also allocates TMEM.
+//   warp 12    TMA producer and work claimer (K_j, V_j once per item, one copy each; Q and dO of
+//              each pair into a 2-stage ring: one 128-row copy each when the pair's q tiles are
+//              adjacent, else one 64-row column-half box per lane); also allocates TMEM.
 //   warp 13    UMMA issuer, warp-wide (all lanes poll, one elected lane issues).  Per step g the
 //              tensor pipe runs dV^T(g), S(g+1), dK^T(g), dP(g+1), dQ^T(g): dV^T waits for P,
 //              dK^T for dS, so the softmax of step g+1 overlaps dK^T, dP and dQ^T of step g, and
@@ -199,9 +200,10 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v,
+    bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_q2,
+                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_do2,
                     const __grid_constant__ CUtensorMap tm_dq, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -245,9 +247,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   if (warp == TMA_WARP && lane == 0) {
     tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_q2);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_do2);
     tma_prefetch_desc(&tm_dq);
   }
   tc_fence_before_sync();
@@ -295,9 +299,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int row_kv = it.bh * S + it.j * BLOCK;
       if (lane == 0) mbar_arrive_expect_tx(bar(KV_FULL), 32768);
       __syncwarp();
-      if (lane < 4)  // lanes 0, 1: K chunks; 2, 3: V chunks
-        tma_load_2d(base + ((lane < 2) ? SM_K : SM_V) + (lane & 1) * 8192u,
-                    (lane < 2) ? &tm_k : &tm_v, bar(KV_FULL), (lane & 1) * 64, row_kv);
+      if (lane < 2)  // lane 0: K, lane 1: V, both column halves of the tile in one copy each
+        tma_load_3d(base + (lane == 0 ? SM_K : SM_V), lane == 0 ? &tm_k : &tm_v, bar(KV_FULL),
+                    0, row_kv, 0);
       ++kv_loads;
       const int np = it.np;
       for (int pp = 0; pp < np; ++pp, ++g) {
@@ -311,7 +315,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int r0 = it.bh * S + i0 * BLOCK, r1 = it.bh * S + i1 * BLOCK;
         if (lane == 0) mbar_arrive_expect_tx(bar(QDO_FULL0 + s), 65536);
         __syncwarp();
-        if (lane < 8) {
+        if (i1 == i0 + 1) {
+          // Adjacent q tiles (always with 128-token blocks): rows r0 .. r0 + 127 of Q and of dO
+          // in one copy each, the same layout as the four boxes below.
+          if (lane < 2)
+            tma_load_3d(base + (lane == 0 ? SM_Q : SM_DO) + s * 32768u, lane == 0 ? &tm_q2 : &tm_do2,
+                        bar(QDO_FULL0 + s), 0, r0, 0);
+        } else if (lane < 8) {
           // Lanes 0-3: Q, 4-7: dO.  Tile t = lane & 3 sits at byte t * 8192 of the stage:
           // (cols 0-63, block i0), (cols 0-63, i1), (cols 64-127, i0), (cols 64-127, i1).
           const uint32_t t = static_cast<uint32_t>(lane & 3);
@@ -794,15 +804,35 @@ cudaError_t make_tmap_rows128_f16(CUtensorMap* map, const void* ptr, long rows) 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t make_tmap_rows128_f16_halves(CUtensorMap* map, const void* ptr, long rows,
+                                         int box_rows) {
+  auto encode = tensor_map_encoder();
+  if (!encode) return cudaErrorNotSupported;
+  const cuuint64_t gdim[3] = {64u, static_cast<cuuint64_t>(rows), 2u};
+  const cuuint64_t gstride[2] = {static_cast<cuuint64_t>(HEAD_DIM) * sizeof(__half),
+                                 64u * sizeof(__half)};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 2u};
+  const cuuint32_t estride[3] = {1u, 1u, 1u};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(ptr), gdim,
+                      gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t launch_bwd_main(const BwdMainArgs& a, cudaStream_t stream) {
   const long rows = static_cast<long>(a.B) * a.H * a.S;
-  CUtensorMap tq, tk, tv, tdo, tdq;
+  // Q and dO: 64-row boxes per column half (q tiles anywhere) and 128-row two-half boxes
+  // (adjacent q tiles); K and V: one 64-row two-half box per tile.
+  CUtensorMap tq, tq2, tk, tv, tdo, tdo2, tdq;
   cudaError_t e;
   if ((e = make_tmap_rows128_f32(&tdq, a.dqacc, rows)) != cudaSuccess) return e;
   if ((e = make_tmap_rows128_f16(&tq, a.q16, rows)) != cudaSuccess) return e;
-  if ((e = make_tmap_rows128_f16(&tk, a.k16, rows)) != cudaSuccess) return e;
-  if ((e = make_tmap_rows128_f16(&tv, a.v16, rows)) != cudaSuccess) return e;
   if ((e = make_tmap_rows128_f16(&tdo, a.do16, rows)) != cudaSuccess) return e;
+  if ((e = make_tmap_rows128_f16_halves(&tq2, a.q16, rows, 128)) != cudaSuccess) return e;
+  if ((e = make_tmap_rows128_f16_halves(&tdo2, a.do16, rows, 128)) != cudaSuccess) return e;
+  if ((e = make_tmap_rows128_f16_halves(&tk, a.k16, rows, 64)) != cudaSuccess) return e;
+  if ((e = make_tmap_rows128_f16_halves(&tv, a.v16, rows, 64)) != cudaSuccess) return e;
   static bool attr_set = false;
   if (!attr_set) {
     e = cudaFuncSetAttribute(bwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -832,7 +862,7 @@ cudaError_t launch_bwd_main(const BwdMainArgs& a, cudaStream_t stream) {
   p.sm_scale = a.sm_scale;
   const int sms = device_sm_count();
   const int grid = p.total < sms ? p.total : sms;
-  bwd_main_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tq, tk, tv, tdo, tdq, p);
+  bwd_main_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tq, tq2, tk, tv, tdo, tdo2, tdq, p);
   return cudaGetLastError();
 }
 

@@ -231,7 +231,8 @@ __device__ __forceinline__ uint32_t pack_bf162(float lo, float hi) {
 }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    fwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    fwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_q2,
+                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_k2,
                     const __grid_constant__ CUtensorMap tm_v, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -275,7 +276,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   if (warp == TMA_WARP && lane == 0) {
     tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_q2);
     tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_k2);
     tma_prefetch_desc(&tm_v);
   }
   tc_fence_before_sync();
@@ -313,9 +316,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int r1 = q.bh * S + (q.i1 >= 0 ? q.i1 : q.i0) * BLOCK;
       if (lane == 0) mbar_arrive_expect_tx(bar(Q_FULL0 + qs), 32768);
       __syncwarp();
-      if (lane < 4)  // tile t = lane at byte t * 8192: (cols 0-63, i0), (0-63, i1), (64-127, i0), ...
+      if (q.i1 >= 0) {  // the two q tiles are adjacent: both column halves of 128 rows, one copy
+        if (lane == 0) tma_load_3d(base + SM_Q + qs * 32768u, &tm_q2, bar(Q_FULL0 + qs), 0, r0, 0);
+      } else if (lane < 4) {  // tile t = lane at byte t * 8192: (cols 0-63, i0), (0-63, i1), ...
         tma_load_2d(base + SM_Q + qs * 32768u + static_cast<uint32_t>(lane) * 8192u, &tm_q,
                     bar(Q_FULL0 + qs), (lane & 2) ? 64 : 0, (lane & 1) ? r1 : r0);
+      }
       last_q[qs] = itc;
       // K of the union's kv blocks two at a time: block 2p in rows 0-63 of pair stage p, block
       // 2p+1 (if any) in rows 64-127, each as (cols 0-63) and (cols 64-127) chunks of 16 KB.
@@ -327,11 +333,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           return false;
         if (lane == 0) mbar_arrive_expect_tx(bar(K_FULL0 + st), j1 >= 0 ? 32768u : 16384u);
         __syncwarp();
-        if (lane < 4 && (lane < 2 || j1 >= 0))  // lane: (block b = lane >> 1, chunk c = lane & 1)
+        if (j1 == j0 + 1) {  // adjacent kv tiles: 128 rows, both column halves, one copy
+          if (lane == 0)
+            tma_load_3d(base + SM_K + st * 32768u, &tm_k2, bar(K_FULL0 + st), 0,
+                        q.bh * S + j0 * BLOCK, 0);
+        } else if (lane < 4 && (lane < 2 || j1 >= 0)) {  // lane: (block lane >> 1, chunk lane & 1)
           tma_load_2d(base + SM_K + st * 32768u + static_cast<uint32_t>(lane & 1) * 16384u +
                           static_cast<uint32_t>(lane >> 1) * 8192u,
                       &tm_k, bar(K_FULL0 + st), (lane & 1) * 64,
                       q.bh * S + ((lane >> 1) ? j1 : j0) * BLOCK);
+        }
         last_lg[st] = lg;
         ++lg;
         return true;
@@ -382,9 +393,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           return false;
         if (lane == 0) mbar_arrive_expect_tx(bar(V_FULL0 + st), 16384u);
         __syncwarp();
-        if (lane < 2)
-          tma_load_2d(base + SM_V + st * 16384u + static_cast<uint32_t>(lane) * 8192u, &tm_v,
-                      bar(V_FULL0 + st), lane * 64, q.bh * S + j * BLOCK);
+        if (lane == 0)  // both column halves of the tile in one copy
+          tma_load_3d(base + SM_V + st * 16384u, &tm_v, bar(V_FULL0 + st), 0, q.bh * S + j * BLOCK,
+                      0);
         last_lg[st] = lg;
         ++lg;
         return true;
@@ -754,11 +765,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 cudaError_t launch_fwd_main(const FwdMainArgs& a, cudaStream_t stream) {
   const long rows = static_cast<long>(a.B) * a.H * a.S;
-  CUtensorMap tq, tk, tv;
+  // 64-row boxes per column half for tiles anywhere, two-half boxes for adjacent tile pairs
+  // (128 rows) and single V tiles (64 rows).
+  CUtensorMap tq, tq2, tk, tk2, tv;
   cudaError_t e;
   if ((e = make_tmap_rows128_f16(&tq, a.q16, rows)) != cudaSuccess) return e;
   if ((e = make_tmap_rows128_f16(&tk, a.k16, rows)) != cudaSuccess) return e;
-  if ((e = make_tmap_rows128_f16(&tv, a.v16, rows)) != cudaSuccess) return e;
+  if ((e = make_tmap_rows128_f16_halves(&tv, a.v16, rows, 64)) != cudaSuccess) return e;
+  if ((e = make_tmap_rows128_f16_halves(&tq2, a.q16, rows, 128)) != cudaSuccess) return e;
+  if ((e = make_tmap_rows128_f16_halves(&tk2, a.k16, rows, 128)) != cudaSuccess) return e;
   static bool attr_set = false;
   if (!attr_set) {
     e = cudaFuncSetAttribute(fwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -782,7 +797,7 @@ cudaError_t launch_fwd_main(const FwdMainArgs& a, cudaStream_t stream) {
   p.sm_scale = a.sm_scale;
   const int sms = device_sm_count();
   const int grid = p.total < sms ? p.total : sms;
-  fwd_main_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tq, tk, tv, p);
+  fwd_main_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tq, tq2, tk, tk2, tv, p);
   return cudaGetLastError();
 }
 

@@ -191,6 +191,12 @@ cudaError_t launch_fwd_main(const FwdMainArgs& a, cudaStream_t stream);
 
 // Tensor map of a [rows, 128] fp16 matrix, box 64 columns x 64 rows, 128-byte swizzle.
 cudaError_t make_tmap_rows128_f16(CUtensorMap* map, const void* base, long rows);
+// The same matrix seen as [2 column halves][rows][64 columns] (coordinates: column within the
+// half, row, half), box 64 columns x `box_rows` rows x both halves, 128-byte swizzle.  One copy
+// lands both 64-column halves of `box_rows` consecutive rows in shared memory half after half,
+// the layout two 2-D boxes per half would give, in one request instead of two or four.
+cudaError_t make_tmap_rows128_f16_halves(CUtensorMap* map, const void* base, long rows,
+                                         int box_rows);
 
 int device_sm_count();
 
