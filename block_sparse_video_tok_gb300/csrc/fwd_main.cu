@@ -447,15 +447,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     };
     // O_g += P_g V_j for group g's kv tile of pair pb (V stage from the global tile count): A =
     // P_g in TMEM (columns 64 g .. 64 g + 31 of buffer pb & 1, 8 columns per 16 kv), B = V_j.
-    // `fresh`: the group's first tile of the item overwrites O_g.  Waits for V and for the
-    // group's P of the pair.
-    auto issue_pv = [&](uint32_t pb, uint32_t g, bool fresh) -> bool {
+    // `fresh`: the group's first tile of the item overwrites O_g.  The caller has waited for V
+    // and for the group's P.
+    auto issue_pv = [&](uint32_t pb, uint32_t g, bool fresh) {
       const uint32_t st = vc % V_STAGES;
-      if (!mbar_wait2_warp(bar(V_FULL0 + st), (vc / V_STAGES) & 1u,
-                           bar(P_READY0 + 2 * g + (pb & 1u)), (pb >> 1) & 1u, abort,
-                           WAIT_LIMIT_NS))
-        return false;
-      tc_fence_after_sync();
       const uint32_t pa = tmem + TM_S + (pb & 1u) * 128u + g * 64u, to = tmem + TM_O + g * 128u;
       const uint64_t vb = sdesc_advance(v_mn, st * 16384u);
       if (fresh)
@@ -467,7 +462,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         umma_ts_elect<true>(to, pa + kk * 8u, sdesc_advance(vb, kk * 2048u), IDESC_PV);
       umma_commit_elect(bar(V_EMPTY0 + st));
       ++vc;
-      return true;
     };
     for (uint32_t k = 0;; ++k) {
       int w;
@@ -497,17 +491,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         } else {
           umma_commit_elect(bar(Q_EMPTY0 + qs));  // every S of the item has been issued
         }
-        // Group 0 always has a tile; the item's first P.V also waits until the previous item's
-        // O buffers have been read.  Group 1 signals every pair, also when the union's odd last
-        // tile leaves it none.
+        // Group 0 always has a tile; group 1 signals every pair, also when the union's odd last
+        // tile leaves it none.  One wait covers both groups' P and both V tiles (each wait costs
+        // this warp a few hundred cycles while the softmax warps share its scheduler); the
+        // item's first P.V also waits until the previous item's O buffers have been read.
+        const bool two = 2 * pr + 1 < nu;
+        const uint32_t v1 = two ? vc + 1 : vc;
+        const uint32_t wb[4] = {bar(V_FULL0 + vc % V_STAGES), bar(V_FULL0 + v1 % V_STAGES),
+                                bar(P_READY0 + (pb & 1u)), bar(P_READY0 + 2 + (pb & 1u))};
+        const uint32_t wp[4] = {(vc / V_STAGES) & 1u, (v1 / V_STAGES) & 1u, (pb >> 1) & 1u,
+                                (pb >> 1) & 1u};
         ok = (pr != 0 || mbar_wait_warp(bar(O_EMPTY), (itc & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) &&
-             issue_pv(pb, 0, pr == 0);
-        if (ok)
-          ok = (2 * pr + 1 < nu)
-                   ? issue_pv(pb, 1, pr == 0)
-                   : mbar_wait_warp(bar(P_READY0 + 2 + (pb & 1u)), (pb >> 1) & 1u, abort,
-                                    WAIT_LIMIT_NS);
-        if (ok) umma_commit_elect(bar(BUF_FREE0 + (pb & 1u)));
+             mbar_waitn_warp(wb, wp, abort, WAIT_LIMIT_NS);
+        if (!ok) break;
+        tc_fence_after_sync();
+        issue_pv(pb, 0, pr == 0);
+        if (two) issue_pv(pb, 1, pr == 0);
+        umma_commit_elect(bar(BUF_FREE0 + (pb & 1u)));
       }
       if (!ok) break;
       umma_commit_elect(bar(O_FULL));

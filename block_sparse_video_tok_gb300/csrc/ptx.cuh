@@ -100,6 +100,38 @@ __device__ __forceinline__ bool mbar_wait2_warp(uint32_t bar_a, uint32_t parity_
   return __all_sync(0xffffffffu, ok);
 }
 
+// mbar_wait_warp on N barriers at once (the same round-trip overlap as mbar_wait2_warp).
+template <int N>
+__device__ __forceinline__ bool mbar_waitn_warp(const uint32_t (&bars)[N],
+                                                const uint32_t (&parities)[N],
+                                                volatile int* abort, uint64_t limit_ns) {
+  bool done[N];
+  bool all = true;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    done[i] = mbar_try_wait(bars[i], parities[i]);
+    all = all && done[i];
+  }
+  bool ok = true;
+  if (!all) {
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+      all = true;
+#pragma unroll
+      for (int i = 0; i < N; ++i) {
+        if (!done[i]) done[i] = mbar_try_wait(bars[i], parities[i]);
+        all = all && done[i];
+      }
+      if (all) break;
+      if (*abort || globaltimer_ns() - t0 > limit_ns) {
+        ok = false;
+        break;
+      }
+    }
+  }
+  return __all_sync(0xffffffffu, ok);
+}
+
 // ------------------------------------------------------------------------------ proxy fences
 
 // Generic-proxy writes to shared memory become visible to the async proxy (UMMA, TMA).
