@@ -246,9 +246,13 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
   if ((e = vsa::launch_absmax_delta(qb, kb, vb, dob, ob, BH, S, absmax, delta, dqacc, s)) !=
       cudaSuccess)
     return cuda_fail(e);
-  const __nv_bfloat16* src[4] = {qb, kb, vb, dob};
-  __half* dst[4] = {q16, k16, v16, do16};
+  // K and V row-major; Q and dO tile-transposed (one 16 KB copy per 64-row tile in the main
+  // kernel, whatever the distance between the two q tiles of a step).
+  const __nv_bfloat16* src[4] = {nullptr, kb, vb, nullptr};
+  __half* dst[4] = {nullptr, k16, v16, nullptr};
   if ((e = vsa::launch_convert(src, dst, 4, BH, S, absmax, s)) != cudaSuccess) return cuda_fail(e);
+  if ((e = vsa::launch_convert_t(qb, dob, q16, do16, BH, S, absmax, s)) != cudaSuccess)
+    return cuda_fail(e);
   if ((e = vsa::launch_vbs_expand(vbs, nb, blk / vsa::BLOCK, vbs64, err, s)) != cudaSuccess)
     return cuda_fail(e);
   const int32_t* work_order = nullptr;

@@ -102,8 +102,8 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 constexpr uint32_t TM_S = 0, TM_DP = 64, TM_DVT = 128, TM_DKT = 192, TM_DQT = 256;  // dQ^T x2
 
-constexpr uint32_t IDESC_SDP = idesc_f16_f32acc(128, 64, false, false);
-constexpr uint32_t IDESC_DVK = idesc_f16_f32acc(128, 64, true, true);
+constexpr uint32_t IDESC_SDP = idesc_f16_f32acc(128, 64, true, false);  // A = Q_p / dO_p, MN-major
+constexpr uint32_t IDESC_DVK = idesc_f16_f32acc(128, 64, false, true);  // A = Q_p^T / dO_p^T
 constexpr uint32_t IDESC_DQ = idesc_f16_f32acc(128, 128, true, false);
 
 struct Params {
@@ -312,22 +312,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         int i0, i1;
         step_tiles(p, it, pp, &i0, &i1);
-        const int r0 = it.bh * S + i0 * BLOCK, r1 = it.bh * S + i1 * BLOCK;
         if (lane == 0) mbar_arrive_expect_tx(bar(QDO_FULL0 + s), 65536);
         __syncwarp();
-        if (i1 == i0 + 1) {
-          // Adjacent q tiles (always with 128-token blocks): rows r0 .. r0 + 127 of Q and of dO
-          // in one copy each, the same layout as the four boxes below.
+        // Q and dO are stored tile-transposed: 64-token tile i of the head is 128 rows (head
+        // dims) of 64 queries from row (bh * S / 64 + i) * 128 on, 16 KB.  Stage layout: tile i0
+        // at byte 0, tile i1 at 16384, for Q and for dO.
+        const int tile0 = it.bh * (S / BLOCK);
+        const int t0 = (tile0 + i0) * HEAD_DIM, t1 = (tile0 + i1) * HEAD_DIM;
+        if (i1 == i0 + 1) {  // adjacent q tiles (always with 128-token blocks): one 32 KB copy
           if (lane < 2)
-            tma_load_3d(base + (lane == 0 ? SM_Q : SM_DO) + s * 32768u, lane == 0 ? &tm_q2 : &tm_do2,
-                        bar(QDO_FULL0 + s), 0, r0, 0);
-        } else if (lane < 8) {
-          // Lanes 0-3: Q, 4-7: dO.  Tile t = lane & 3 sits at byte t * 8192 of the stage:
-          // (cols 0-63, block i0), (cols 0-63, i1), (cols 64-127, i0), (cols 64-127, i1).
-          const uint32_t t = static_cast<uint32_t>(lane & 3);
-          tma_load_2d(base + ((lane < 4) ? SM_Q : SM_DO) + s * 32768u + t * 8192u,
-                      (lane < 4) ? &tm_q : &tm_do, bar(QDO_FULL0 + s), (t & 2u) ? 64 : 0,
-                      (t & 1u) ? r1 : r0);
+            tma_load_2d(base + (lane == 0 ? SM_Q : SM_DO) + s * 32768u, lane == 0 ? &tm_q2 : &tm_do2,
+                        bar(QDO_FULL0 + s), 0, t0);
+        } else if (lane < 4) {  // lanes 0, 1: Q tiles i0, i1; lanes 2, 3: dO tiles
+          tma_load_2d(base + ((lane < 2) ? SM_Q : SM_DO) + s * 32768u + (lane & 1) * 16384u,
+                      (lane < 2) ? &tm_q : &tm_do, bar(QDO_FULL0 + s), 0, (lane & 1) ? t1 : t0);
         }
         last_g[s] = g;
       }
@@ -353,8 +351,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t g = 0, itc = 0;
     bool ok = true, issued = false;
     // Operand descriptors, built once; each UMMA only adds a constant byte offset to them.
-    //   K-major (S, dP; dQ^T's B): 32 B per k-step inside a 128-B row, 64-element chunks apart.
-    //   MN-major (dV^T, dK^T, dQ^T's A): 2048 B (16 rows) per k-step.
+    //   K-major: 32 B per k-step inside a 128-B row, 64-element chunks (K/V column halves, or
+    //   the two transposed q tiles of Q_p^T / dO_p^T) 8 or 16 KB apart.
+    //   MN-major: 2048 B (16 rows) per k-step; Q_p and dO_p as A of S and dP take their two
+    //   64-query chunks from the two transposed tiles (LBO 16 KB).
     const uint64_t k_kmaj = sdesc_sw128(base + SM_K, 16, 1024);
     const uint64_t v_kmaj = sdesc_sw128(base + SM_V, 16, 1024);
     const uint64_t k_mn = sdesc_sw128(base + SM_K, 8192, 1024);
@@ -367,28 +367,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint64_t ds_kmaj = sdesc_sw128(base + SM_DS, 16, 1024);
     const uint32_t t_s = tmem + TM_S, t_dp = tmem + TM_DP, t_dv = tmem + TM_DVT,
                    t_dk = tmem + TM_DKT;
-    // S = Q_p K_j^T of step gs (stage gs & 1).
+    // S = Q_p K_j^T of step gs (stage gs & 1).  A = Q_p read MN-major from the two transposed
+    // q tiles (64 queries per 128-byte row, one tile per 64-query chunk), 16 head dims (rows)
+    // per k-step.
     auto issue_s = [&](uint32_t gs) {
-      const uint64_t qa = sdesc_advance(q_kmaj, (gs & 1u) * 32768u);
+      const uint64_t qa = sdesc_advance(q_mn, (gs & 1u) * 32768u);
       umma_ss_elect<false>(t_s, qa, k_kmaj, IDESC_SDP);
 #pragma unroll
-      for (int kk = 1; kk < 8; ++kk) {
-        const uint32_t off = (kk >> 2) * 16384u + (kk & 3) * 32u;
-        umma_ss_elect<true>(t_s, sdesc_advance(qa, off),
+      for (int kk = 1; kk < 8; ++kk)
+        umma_ss_elect<true>(t_s, sdesc_advance(qa, kk * 2048u),
                             sdesc_advance(k_kmaj, (kk >> 2) * 8192u + (kk & 3) * 32u), IDESC_SDP);
-      }
       umma_commit_elect(bar(S_FULL));
     };
     // dP = dO_p V_j^T of step gs.
     auto issue_dp = [&](uint32_t gs) {
-      const uint64_t da = sdesc_advance(do_kmaj, (gs & 1u) * 32768u);
+      const uint64_t da = sdesc_advance(do_mn, (gs & 1u) * 32768u);
       umma_ss_elect<false>(t_dp, da, v_kmaj, IDESC_SDP);
 #pragma unroll
-      for (int kk = 1; kk < 8; ++kk) {
-        const uint32_t off = (kk >> 2) * 16384u + (kk & 3) * 32u;
-        umma_ss_elect<true>(t_dp, sdesc_advance(da, off),
+      for (int kk = 1; kk < 8; ++kk)
+        umma_ss_elect<true>(t_dp, sdesc_advance(da, kk * 2048u),
                             sdesc_advance(v_kmaj, (kk >> 2) * 8192u + (kk & 3) * 32u), IDESC_SDP);
-      }
       umma_commit_elect(bar(DP_FULL));
     };
     // dQ^T = K_j^T dS^T of step gs into TMEM buffer gs & 1; then the dS buffer is free.
@@ -408,21 +406,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       umma_commit_elect(bar(DS_FREE));
       return true;
     };
-    // dV^T += dO_p^T P of step gs; the first step of an item overwrites.
+    // dV^T += dO_p^T P of step gs; the first step of an item overwrites.  A = dO_p^T read K-major
+    // from the transposed tiles: 128 head-dim rows, 16 queries per k-step (tile kk >> 2).
     auto issue_dv = [&](uint32_t gs, bool first) {
-      const uint64_t da = sdesc_advance(do_mn, (gs & 1u) * 32768u);
+      const uint64_t da = sdesc_advance(do_kmaj, (gs & 1u) * 32768u);
       if (first)
         umma_ss_elect<false>(t_dv, da, p_mn, IDESC_DVK);
       else
         umma_ss_elect<true>(t_dv, da, p_mn, IDESC_DVK);
 #pragma unroll
       for (int kk = 1; kk < 8; ++kk)
-        umma_ss_elect<true>(t_dv, sdesc_advance(da, kk * 2048u), sdesc_advance(p_mn, kk * 2048u),
-                         IDESC_DVK);
+        umma_ss_elect<true>(t_dv, sdesc_advance(da, (kk >> 2) * 16384u + (kk & 3) * 32u),
+                            sdesc_advance(p_mn, kk * 2048u), IDESC_DVK);
     };
     // dK^T += Q_p^T dS of step gs; the first step of an item overwrites.
     auto issue_dk = [&](uint32_t gs, bool first) {
-      const uint64_t qa = sdesc_advance(q_mn, (gs & 1u) * 32768u);
+      const uint64_t qa = sdesc_advance(q_kmaj, (gs & 1u) * 32768u);
       const uint64_t dsb = ds_mn;
       if (first)
         umma_ss_elect<false>(t_dk, qa, dsb, IDESC_DVK);
@@ -430,8 +429,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         umma_ss_elect<true>(t_dk, qa, dsb, IDESC_DVK);
 #pragma unroll
       for (int kk = 1; kk < 8; ++kk)
-        umma_ss_elect<true>(t_dk, sdesc_advance(qa, kk * 2048u), sdesc_advance(dsb, kk * 2048u),
-                         IDESC_DVK);
+        umma_ss_elect<true>(t_dk, sdesc_advance(qa, (kk >> 2) * 16384u + (kk & 3) * 32u),
+                            sdesc_advance(dsb, kk * 2048u), IDESC_DVK);
     };
     for (uint32_t k = 0;; ++k) {
       int w;
@@ -774,6 +773,22 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // [rows, 128] fp32 (the dQ accumulator), box 32 columns x 64 rows, no swizzle.
+// Tile-transposed fp16 operand (launch_convert_t): `rows` token rows give rows * 2 rows of 64
+// halves; box 64 columns x 128 * `tiles` rows, 128-byte swizzle.
+cudaError_t make_tmap_tiles_t(CUtensorMap* map, const void* ptr, long rows, int tiles) {
+  auto encode = tensor_map_encoder();
+  if (!encode) return cudaErrorNotSupported;
+  const cuuint64_t gdim[2] = {64u, static_cast<cuuint64_t>(rows) * 2u};
+  const cuuint64_t gstride[1] = {64u * sizeof(__half)};
+  const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(HEAD_DIM * tiles)};
+  const cuuint32_t estride[2] = {1u, 1u};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), gdim,
+                      gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t make_tmap_rows128_f32(CUtensorMap* map, const void* ptr, long rows) {
   auto encode = tensor_map_encoder();
   if (!encode) return cudaErrorNotSupported;
@@ -822,15 +837,15 @@ cudaError_t make_tmap_rows128_f16_halves(CUtensorMap* map, const void* ptr, long
 
 cudaError_t launch_bwd_main(const BwdMainArgs& a, cudaStream_t stream) {
   const long rows = static_cast<long>(a.B) * a.H * a.S;
-  // Q and dO: 64-row boxes per column half (q tiles anywhere) and 128-row two-half boxes
-  // (adjacent q tiles); K and V: one 64-row two-half box per tile.
+  // Q and dO (tile-transposed): one tile (128 rows of 64) or two adjacent tiles per box; K and
+  // V: one 64-row two-half box per tile.
   CUtensorMap tq, tq2, tk, tv, tdo, tdo2, tdq;
   cudaError_t e;
   if ((e = make_tmap_rows128_f32(&tdq, a.dqacc, rows)) != cudaSuccess) return e;
-  if ((e = make_tmap_rows128_f16(&tq, a.q16, rows)) != cudaSuccess) return e;
-  if ((e = make_tmap_rows128_f16(&tdo, a.do16, rows)) != cudaSuccess) return e;
-  if ((e = make_tmap_rows128_f16_halves(&tq2, a.q16, rows, 128)) != cudaSuccess) return e;
-  if ((e = make_tmap_rows128_f16_halves(&tdo2, a.do16, rows, 128)) != cudaSuccess) return e;
+  if ((e = make_tmap_tiles_t(&tq, a.q16, rows, 1)) != cudaSuccess) return e;
+  if ((e = make_tmap_tiles_t(&tdo, a.do16, rows, 1)) != cudaSuccess) return e;
+  if ((e = make_tmap_tiles_t(&tq2, a.q16, rows, 2)) != cudaSuccess) return e;
+  if ((e = make_tmap_tiles_t(&tdo2, a.do16, rows, 2)) != cudaSuccess) return e;
   if ((e = make_tmap_rows128_f16_halves(&tk, a.k16, rows, 64)) != cudaSuccess) return e;
   if ((e = make_tmap_rows128_f16_halves(&tv, a.v16, rows, 64)) != cudaSuccess) return e;
   static bool attr_set = false;

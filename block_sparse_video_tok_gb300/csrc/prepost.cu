@@ -4,6 +4,8 @@
 //                 "fp32 rowsum(bf16(o) * dout), written by the preprocess"); zeroing of the fp32
 //                 dQ accumulator ("preprocess zeroes, main reduce-adds, postprocess reads").
 //   convert       scaled fp16 copies of the bf16 operands for the tensor cores.
+//   convert_t     the same for Q and dO of the backward, each 64-row tile stored transposed
+//                 ([128 head dims][64 rows]), so one 16 KB copy brings a whole tile.
 //   order         work order: (b, h) segments, items sorted by descending k2q list length,
 //                 stable (the commit message's "a device kernel sorts by list length from 1024 kv
 //                 blocks per sequence on").
@@ -117,6 +119,47 @@ __global__ void __launch_bounds__(256) convert_kernel(ConvertPack pk, size_t chu
       out[i] = *reinterpret_cast<const uint32_t*>(&h);
     }
     dst[c] = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+}
+
+// Grid (S / 64, BH, count): one 64-row tile of one tensor per CTA, read as rows of 128 bf16,
+// scaled, and written as 128 rows (head dims) of 64 fp16 (the tile's rows).  The shared tile has
+// rows of 130 halves (65 words), so the column gathers of the write phase hit distinct banks.
+struct ConvertTPack {
+  const uint4* src[2];
+  __half* dst[2];
+  int slot[2];  // operand index in the per-head maxima (Q 0, dO 3)
+};
+
+__global__ void __launch_bounds__(256) convert_t_kernel(ConvertTPack pk, int S,
+                                                        const uint32_t* __restrict__ absmax) {
+  constexpr int LD = 130;
+  __shared__ __half tl[BLOCK * LD];
+  const int t = blockIdx.z, bh = blockIdx.y, tile = blockIdx.x, nt = gridDim.x;
+  const uint4* __restrict__ src = t == 0 ? pk.src[0] : pk.src[1];
+  __half* __restrict__ dst = t == 0 ? pk.dst[0] : pk.dst[1];
+  const float sc = exp2i(-operand_exponent(absmax[bh * 4 + (t == 0 ? pk.slot[0] : pk.slot[1])]));
+  const size_t row0 = static_cast<size_t>(bh) * S + static_cast<size_t>(tile) * BLOCK;
+  for (int c = threadIdx.x; c < BLOCK * 16; c += blockDim.x) {
+    const int r = c >> 4, ch = c & 15;
+    const uint4 x = src[(row0 + r) * 16 + ch];
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    __half2* d2 = reinterpret_cast<__half2*>(tl + r * LD + ch * 8);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d2[i] = __floats2half2_rn(bf16lo(w[i]) * sc, bf16hi(w[i]) * sc);
+  }
+  __syncthreads();
+  uint4* out = reinterpret_cast<uint4*>(dst + (static_cast<size_t>(bh) * nt + tile) * HEAD_DIM *
+                                                  BLOCK);
+  for (int c = threadIdx.x; c < HEAD_DIM * 8; c += blockDim.x) {
+    const int d = c >> 3, rc = c & 7;
+    uint32_t v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 h = __halves2half2(tl[(rc * 8 + 2 * i) * LD + d], tl[(rc * 8 + 2 * i + 1) * LD + d]);
+      v[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    out[d * 8 + rc] = make_uint4(v[0], v[1], v[2], v[3]);
   }
 }
 
@@ -248,6 +291,21 @@ cudaError_t launch_convert(const __nv_bfloat16* const* src, __half* const* dst, 
   const size_t total = per_head * BH;
   dim3 grid(static_cast<unsigned>(grid_for(total, 256, 8)), static_cast<unsigned>(count));
   convert_kernel<<<grid, 256, 0, stream>>>(pk, per_head, total, absmax);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_convert_t(const __nv_bfloat16* q, const __nv_bfloat16* dout, __half* q16t,
+                             __half* do16t, int BH, int S, const uint32_t* absmax,
+                             cudaStream_t stream) {
+  ConvertTPack pk{};
+  pk.src[0] = reinterpret_cast<const uint4*>(q);
+  pk.src[1] = reinterpret_cast<const uint4*>(dout);
+  pk.dst[0] = q16t;
+  pk.dst[1] = do16t;
+  pk.slot[0] = 0;
+  pk.slot[1] = 3;
+  dim3 grid(static_cast<unsigned>(S / BLOCK), static_cast<unsigned>(BH), 2u);
+  convert_t_kernel<<<grid, 256, 0, stream>>>(pk, S, absmax);
   return cudaGetLastError();
 }
 

@@ -134,6 +134,12 @@ cudaError_t launch_absmax_delta(const __nv_bfloat16* q, const __nv_bfloat16* k,
 // fp16 copies X' = X * 2^-e(head) of up to four [BH, S, 128] bf16 tensors (null entries skipped).
 cudaError_t launch_convert(const __nv_bfloat16* const* src, __half* const* dst, int count, int BH,
                            int S, const uint32_t* absmax, cudaStream_t stream);
+// Q and dO of the backward as tile-transposed fp16: tile i of head bh is stored at
+// ((bh * S/64 + i) * 128 + d) * 64 + r for row r of the tile and head dim d, scaled like
+// launch_convert (operand slots 0 and 3 of the per-head maxima).
+cudaError_t launch_convert_t(const __nv_bfloat16* q, const __nv_bfloat16* dout, __half* q16t,
+                             __half* do16t, int BH, int S, const uint32_t* absmax,
+                             cudaStream_t stream);
 
 cudaError_t launch_order(const int32_t* k2q_num, int BH, int nb, int max_q, int32_t* order,
                          cudaStream_t stream);
