@@ -16,7 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libvsa.so")
-SOURCES = ["api.cu", "invert.cu", "prepost.cu", "bwd_main.cu", "fwd_main.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "invert.cu", "prepost.cu", "tmap.cu", "bwd_main.cu", "fwd_main.cu",
+           "noalloc.cu"]
 HEADERS = ["ptx.cuh", "queue.cuh", "vsa_internal.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

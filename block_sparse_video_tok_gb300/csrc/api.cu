@@ -152,20 +152,20 @@ vsa_status vsa_fwd(const void* q, const void* k, const void* v, const int32_t* q
   uint32_t* absmax = ws_at<uint32_t>(workspace, L.absmax);
   uint32_t* bitmap = ws_at<uint32_t>(workspace, L.bitmap);
   int32_t* vbs64 = ws_at<int32_t>(workspace, L.vbs64);
-  __half* q16 = ws_at<__half>(workspace, L.q16);
-  __half* k16 = ws_at<__half>(workspace, L.k16);
   __half* v16 = ws_at<__half>(workspace, L.v16);
   const auto* qb = static_cast<const __nv_bfloat16*>(q);
   const auto* kb = static_cast<const __nv_bfloat16*>(k);
   const auto* vb = static_cast<const __nv_bfloat16*>(v);
 
-  cudaError_t e = cudaMemsetAsync(workspace, 0, L.q16, s);  // header, maxima, bitmap
+  cudaError_t e = cudaMemsetAsync(workspace, 0, L.v16, s);  // header, maxima, bitmap
   if (e != cudaSuccess) return cuda_fail(e);
-  if ((e = vsa::launch_absmax_delta(qb, kb, vb, nullptr, nullptr, BH, S, absmax, nullptr, nullptr,
-                                    s)) != cudaSuccess)
+  // S = Q K^T takes the bf16 Q and K as given; only V needs the scaled fp16 copy that P.V (fp16
+  // P) takes, so only V's maximum is scanned.
+  if ((e = vsa::launch_absmax_delta(nullptr, nullptr, vb, nullptr, nullptr, BH, S, absmax, nullptr,
+                                    nullptr, s)) != cudaSuccess)
     return cuda_fail(e);
-  const __nv_bfloat16* src[3] = {qb, kb, vb};
-  __half* dst[3] = {q16, k16, v16};
+  const __nv_bfloat16* src[3] = {nullptr, nullptr, vb};
+  __half* dst[3] = {nullptr, nullptr, v16};
   if ((e = vsa::launch_convert(src, dst, 3, BH, S, absmax, s)) != cudaSuccess) return cuda_fail(e);
   if ((e = vsa::launch_vbs_expand(vbs, nb, blk / vsa::BLOCK, vbs64, err, s)) != cudaSuccess)
     return cuda_fail(e);
@@ -173,8 +173,8 @@ vsa_status vsa_fwd(const void* q, const void* k, const void* v, const int32_t* q
                                   s)) != cudaSuccess)
     return cuda_fail(e);
   vsa::FwdMainArgs a{};
-  a.q16 = q16;
-  a.k16 = k16;
+  a.q = qb;
+  a.k = kb;
   a.v16 = v16;
   a.bitmap = bitmap;
   a.vbs = vbs64;

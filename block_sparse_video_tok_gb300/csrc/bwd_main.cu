@@ -41,7 +41,6 @@
 // the tensor pipe runs in issue order, so S(g) completing means dV^T(g-1) has read P(g-1), and
 // the softmax writes dS(g) only after dQ^T(g-1) has read dS(g-1), a barrier it waits on); dQ
 // staging.
-#include <cudaTypedefs.h>
 
 #include "ptx.cuh"
 #include "queue.cuh"
@@ -756,84 +755,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 }  // namespace
-
-namespace {
-
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  if (!encode) {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                     cudaEnableDefault, &q);
-    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return nullptr;
-    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  }
-  return encode;
-}
-
-// [rows, 128] fp32 (the dQ accumulator), box 32 columns x 64 rows, no swizzle.
-// Tile-transposed fp16 operand (launch_convert_t): `rows` token rows give rows * 2 rows of 64
-// halves; box 64 columns x 128 * `tiles` rows, 128-byte swizzle.
-cudaError_t make_tmap_tiles_t(CUtensorMap* map, const void* ptr, long rows, int tiles) {
-  auto encode = tensor_map_encoder();
-  if (!encode) return cudaErrorNotSupported;
-  const cuuint64_t gdim[2] = {64u, static_cast<cuuint64_t>(rows) * 2u};
-  const cuuint64_t gstride[1] = {64u * sizeof(__half)};
-  const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(HEAD_DIM * tiles)};
-  const cuuint32_t estride[2] = {1u, 1u};
-  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), gdim,
-                      gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
-cudaError_t make_tmap_rows128_f32(CUtensorMap* map, const void* ptr, long rows) {
-  auto encode = tensor_map_encoder();
-  if (!encode) return cudaErrorNotSupported;
-  const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(HEAD_DIM), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(HEAD_DIM) * sizeof(float)};
-  const cuuint32_t box[2] = {32u, 64u};
-  const cuuint32_t estride[2] = {1u, 1u};
-  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), gdim,
-                      gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
-}  // namespace
-
-cudaError_t make_tmap_rows128_f16(CUtensorMap* map, const void* ptr, long rows) {
-  auto encode = tensor_map_encoder();
-  if (!encode) return cudaErrorNotSupported;
-  const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(HEAD_DIM), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(HEAD_DIM) * sizeof(__half)};
-  const cuuint32_t box[2] = {64u, 64u};
-  const cuuint32_t estride[2] = {1u, 1u};
-  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), gdim,
-                      gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
-cudaError_t make_tmap_rows128_f16_halves(CUtensorMap* map, const void* ptr, long rows,
-                                         int box_rows) {
-  auto encode = tensor_map_encoder();
-  if (!encode) return cudaErrorNotSupported;
-  const cuuint64_t gdim[3] = {64u, static_cast<cuuint64_t>(rows), 2u};
-  const cuuint64_t gstride[2] = {static_cast<cuuint64_t>(HEAD_DIM) * sizeof(__half),
-                                 64u * sizeof(__half)};
-  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 2u};
-  const cuuint32_t estride[3] = {1u, 1u, 1u};
-  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(ptr), gdim,
-                      gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
 
 cudaError_t launch_bwd_main(const BwdMainArgs& a, cudaStream_t stream) {
   const long rows = static_cast<long>(a.B) * a.H * a.S;

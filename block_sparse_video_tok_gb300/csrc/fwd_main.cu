@@ -7,14 +7,15 @@
 // blocks are 128 tokens) -- so the UMMA M dimension is 128 and row m of every accumulator is TMEM
 // lane m.  The item walks the UNION of the two tiles' selected kv tiles (ascending); for each
 // row, kv tiles its own q tile did not select are masked.  The union is taken two kv tiles at a
-// time: S = Q_p [K_a; K_b]^T is one set of 128x128x16 UMMAs (both operands in shared memory,
-// fp32 accumulator in TMEM), and softmax group 0 takes tile a, group 1 tile b.  Per group and kv
-// tile, an online softmax:
+// time: S = Q_p [K_a; K_b]^T is one set of 128x128x16 UMMAs (the caller's bf16 Q and K, both in
+// shared memory, fp32 accumulator in TMEM), and softmax group 0 takes tile a, group 1 tile b.
+// Per group and kv tile, an online softmax:
 //   the row maximum of the tile; if it exceeds the row's reference maximum m by more than
 //   RESCALE (log2 units), m moves up to it and the group's O row and running sum are scaled by
 //   2^(m_old - m_new) first (otherwise m stays, so P stays below 2^(RESCALE + KPF));
 //   P = 2^(s - m + KPF) in fp16, written to TMEM, where it is the A operand of
-//   O_g += P V_j (B = V_j from shared memory, MN-major).
+//   O_g += P V_j (B = V_j from shared memory, MN-major; kind::f16 takes one type for A and B,
+//   so V comes from the preprocess's fp16 copy, scaled by 2^-e_v).
 // P never passes through shared memory, so per kv tile the tensor pipe reads Q_p, K_j and V_j
 // only.
 //
@@ -92,7 +93,7 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 static_assert(K_STAGES == 2, "K stages pair up with the two S buffers");
 constexpr uint32_t TM_O = 0, TM_S = 256;  // O_g at TM_O + 128 g; S buffer b at TM_S + 128 b
-constexpr uint32_t IDESC_S = idesc_f16_f32acc(128, 128, false, false);
+constexpr uint32_t IDESC_S = idesc_f16_f32acc(128, 128, false, false, true);  // bf16 Q, K
 constexpr uint32_t IDESC_PV = idesc_f16_f32acc(128, 128, false, true);
 
 struct Params {
@@ -553,9 +554,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         continue;
       }
       const uint32_t* am = p.absmax + q.bh * 4;
-      const int eq = operand_exponent(am[0]), ek = operand_exponent(am[1]);
       const int ev = operand_exponent(am[2]);
-      const float c1 = p.sm_scale * LOG2E_F * exp2i(eq + ek);  // S' -> s (log2 units)
+      const float c1 = p.sm_scale * LOG2E_F;  // S -> s (log2 units); Q and K are unscaled bf16
       float m = -INFINITY, l = 0.f;  // this group's reference maximum and sum of P * 2^KPF
       bool first = true;             // no block of this group in the item yet
       // The union's kv tiles in pairs (tile 2p for group 0, 2p+1 for group 1); j < 0: the
@@ -769,11 +769,11 @@ cudaError_t launch_fwd_main(const FwdMainArgs& a, cudaStream_t stream) {
   // (128 rows) and single V tiles (64 rows).
   CUtensorMap tq, tq2, tk, tk2, tv;
   cudaError_t e;
-  if ((e = make_tmap_rows128_f16(&tq, a.q16, rows)) != cudaSuccess) return e;
-  if ((e = make_tmap_rows128_f16(&tk, a.k16, rows)) != cudaSuccess) return e;
+  if ((e = make_tmap_rows128_f16(&tq, a.q, rows, true)) != cudaSuccess) return e;
+  if ((e = make_tmap_rows128_f16(&tk, a.k, rows, true)) != cudaSuccess) return e;
   if ((e = make_tmap_rows128_f16_halves(&tv, a.v16, rows, 64)) != cudaSuccess) return e;
-  if ((e = make_tmap_rows128_f16_halves(&tq2, a.q16, rows, 128)) != cudaSuccess) return e;
-  if ((e = make_tmap_rows128_f16_halves(&tk2, a.k16, rows, 128)) != cudaSuccess) return e;
+  if ((e = make_tmap_rows128_f16_halves(&tq2, a.q, rows, 128, true)) != cudaSuccess) return e;
+  if ((e = make_tmap_rows128_f16_halves(&tk2, a.k, rows, 128, true)) != cudaSuccess) return e;
   static bool attr_set = false;
   if (!attr_set) {
     e = cudaFuncSetAttribute(fwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -54,9 +54,9 @@ __global__ void __launch_bounds__(PRE_THREADS) absmax_delta_kernel(
   for (int rr = half; rr < BLOCK; rr += PRE_THREADS / 16) {
     const size_t row = static_cast<size_t>(bh) * S + static_cast<size_t>(blockIdx.x) * BLOCK + rr;
     const size_t at = row * 16 + sub;
-    mq = max(mq, absmax_bits8(q[at]));
-    mk = max(mk, absmax_bits8(k[at]));
-    mv = max(mv, absmax_bits8(v[at]));
+    if (q) mq = max(mq, absmax_bits8(q[at]));  // a null operand is not scanned (its max stays 0)
+    if (k) mk = max(mk, absmax_bits8(k[at]));
+    if (v) mv = max(mv, absmax_bits8(v[at]));
     if (bwd) {
       const uint4 a = dout[at], b = o[at];
       mdo = max(mdo, absmax_bits8(a));

@@ -412,13 +412,15 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
-// Instruction descriptor for kind::f16 with fp16 A and B and an fp32 accumulator.
-// Bits: [4,6) D format (1 = F32), [7,10) A format (0 = F16), [10,13) B format (0 = F16),
-// 15 A major (1 = MN), 16 B major (1 = MN), [17,23) N >> 3, [24,29) M >> 4.
-__host__ __device__ constexpr uint32_t idesc_f16_f32acc(int M, int N, bool a_mn, bool b_mn) {
-  return (1u << 4) | (0u << 7) | (0u << 10) | ((a_mn ? 1u : 0u) << 15) |
-         ((b_mn ? 1u : 0u) << 16) | ((static_cast<uint32_t>(N) >> 3) << 17) |
-         ((static_cast<uint32_t>(M) >> 4) << 24);
+// Instruction descriptor for kind::f16 with an fp32 accumulator; A and B are both fp16, or both
+// bf16 when `bf16` is set (kind::f16 takes one type for both).
+// Bits: [4,6) D format (1 = F32), [7,10) A format (0 = F16, 1 = BF16), [10,13) B format (same
+// codes), 15 A major (1 = MN), 16 B major (1 = MN), [17,23) N >> 3, [24,29) M >> 4.
+__host__ __device__ constexpr uint32_t idesc_f16_f32acc(int M, int N, bool a_mn, bool b_mn,
+                                                        bool bf16 = false) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+         ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((static_cast<uint32_t>(N) >> 3) << 17) | ((static_cast<uint32_t>(M) >> 4) << 24);
 }
 
 }  // namespace vsa

@@ -32,7 +32,7 @@ struct BwdLayout {
   size_t err, sched, absmax, delta, order, vbs64, dqacc, q16, k16, v16, do16, total;
 };
 struct FwdLayout {
-  size_t err, sched, absmax, bitmap, vbs64, q16, k16, v16, total;
+  size_t err, sched, absmax, bitmap, vbs64, v16, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -80,10 +80,6 @@ inline FwdLayout fwd_layout(long B, long H, long S) {
   off = align_up(off + bh * nb * words * sizeof(uint32_t), 1024);
   L.vbs64 = off;
   off = align_up(off + nb * sizeof(int32_t), 1024);
-  L.q16 = off;
-  off = align_up(off + rows * HEAD_DIM * sizeof(__half), 1024);
-  L.k16 = off;
-  off = align_up(off + rows * HEAD_DIM * sizeof(__half), 1024);
   L.v16 = off;
   off = align_up(off + rows * HEAD_DIM * sizeof(__half), 1024);
   L.total = off;
@@ -182,7 +178,8 @@ cudaError_t launch_vbs_expand(const int32_t* vbs, int nb, int tiles, int32_t* vb
                               uint32_t* err, cudaStream_t stream);
 
 struct FwdMainArgs {
-  const __half *q16, *k16, *v16;
+  const __nv_bfloat16 *q, *k;  // the caller's bf16 Q and K (the S = Q K^T operands)
+  const __half* v16;           // V in fp16, scaled by 2^-e_v (the B operand of P.V)
   const uint32_t* bitmap;  // [BH, nb, words] selection bits
   const int32_t* vbs;
   const uint32_t* absmax;
@@ -195,14 +192,22 @@ struct FwdMainArgs {
 };
 cudaError_t launch_fwd_main(const FwdMainArgs& a, cudaStream_t stream);
 
-// Tensor map of a [rows, 128] fp16 matrix, box 64 columns x 64 rows, 128-byte swizzle.
-cudaError_t make_tmap_rows128_f16(CUtensorMap* map, const void* base, long rows);
+// Tensor maps (tmap.cu).
+// [rows, 128] fp32 (the dQ accumulator), box 32 columns x 64 rows, no swizzle.
+cudaError_t make_tmap_rows128_f32(CUtensorMap* map, const void* base, long rows);
+// Tile-transposed fp16 operand (launch_convert_t): `rows` token rows give rows * 2 rows of 64
+// halves; box 64 columns x 128 * `tiles` rows, 128-byte swizzle.
+cudaError_t make_tmap_tiles_t(CUtensorMap* map, const void* base, long rows, int tiles);
+// Tensor map of a [rows, 128] fp16 (bf16 with `bf16`) matrix, box 64 columns x 64 rows,
+// 128-byte swizzle.
+cudaError_t make_tmap_rows128_f16(CUtensorMap* map, const void* base, long rows,
+                                  bool bf16 = false);
 // The same matrix seen as [2 column halves][rows][64 columns] (coordinates: column within the
 // half, row, half), box 64 columns x `box_rows` rows x both halves, 128-byte swizzle.  One copy
 // lands both 64-column halves of `box_rows` consecutive rows in shared memory half after half,
 // the layout two 2-D boxes per half would give, in one request instead of two or four.
 cudaError_t make_tmap_rows128_f16_halves(CUtensorMap* map, const void* base, long rows,
-                                         int box_rows);
+                                         int box_rows, bool bf16 = false);
 
 int device_sm_count();
 

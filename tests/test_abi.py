@@ -52,7 +52,8 @@ def test_workspace_sizes(vsa):
     fwd = vsa.vsa_fwd_workspace_bytes(B, H, S)
     # dQ accumulator (fp32) + four fp16 operand copies dominate the backward workspace.
     assert bwd >= rows * 128 * 4 + 4 * rows * 128 * 2 + rows * 4
-    assert fwd >= 3 * rows * 128 * 2
+    # The forward copies only V to fp16 (S = Q K^T takes the bf16 Q and K as given).
+    assert rows * 128 * 2 <= fwd < 2 * rows * 128 * 2
     assert vsa.vsa_bwd_workspace_bytes(B, H, 100) == 0      # S not a multiple of 64
     assert vsa.vsa_bwd_workspace_bytes(B, H, S, 64) == 0    # head_dim 64
     assert vsa.vsa_fwd_workspace_bytes(0, H, S) == 0
