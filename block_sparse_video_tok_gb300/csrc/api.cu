@@ -241,7 +241,8 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
 
   cudaError_t e = record(events ? events->start : nullptr, s);
   if (e != cudaSuccess) return cuda_fail(e);
-  if ((e = cudaMemsetAsync(workspace, 0, L.delta, s)) != cudaSuccess)  // header, counter, maxima
+  // Header, work counter, maxima and the split items' counters and sums.
+  if ((e = cudaMemsetAsync(workspace, 0, L.delta, s)) != cudaSuccess)
     return cuda_fail(e);
   if ((e = vsa::launch_absmax_delta(qb, kb, vb, dob, ob, BH, S, absmax, delta, dqacc, s)) !=
       cudaSuccess)
@@ -278,6 +279,8 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
   a.dv = static_cast<__nv_bfloat16*>(dv);
   a.err = err;
   a.sched = ws_at<int32_t>(workspace, L.sched);
+  a.split_acc = ws_at<float>(workspace, L.split_acc);
+  a.split_row = ws_at<int32_t>(workspace, L.split_row);
   a.B = shape.batch;
   a.H = shape.heads;
   a.S = S;
@@ -290,7 +293,8 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
   if ((e = vsa::launch_bwd_main(a, s)) != cudaSuccess) return cuda_fail(e);
   if ((e = record(events ? events->after_main : nullptr, s)) != cudaSuccess) return cuda_fail(e);
   if ((e = vsa::launch_postprocess(dqacc, absmax, BH, S, sm_scale,
-                                   static_cast<__nv_bfloat16*>(dq), s)) != cudaSuccess)
+                                   static_cast<__nv_bfloat16*>(dq), a.split_acc, a.split_row,
+                                   vsa::bwd_split_items(BH * a.nb), a.dk, a.dv, s)) != cudaSuccess)
     return cuda_fail(e);
   if ((e = record(events ? events->end : nullptr, s)) != cudaSuccess) return cuda_fail(e);
   return VSA_OK;

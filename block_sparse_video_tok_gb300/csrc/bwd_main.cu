@@ -19,7 +19,10 @@
 // contiguous bytes of one query row.
 //
 // Work items are claimed dynamically (queue.cuh).  With 128-token blocks an item is one of the
-// two 64-token kv tiles of a block, and each k2q entry supplies a whole q tile pair.
+// two 64-token kv tiles of a block, and each k2q entry supplies a whole q tile pair.  The last
+// items of the claim order (one per CTA) are handed out as two halves of their step lists, so
+// the grid's end is spread over half an item; a half adds its fp32 dK, dV rows into a zeroed
+// workspace slot, which the postprocess turns into bf16.
 //
 // Roles (448 threads):
 //   warps 0-7  softmax: warps w and w+4 share TMEM lane quarter w (query rows 32w..32w+31 of the
@@ -122,7 +125,16 @@ struct Params {
   int nb;     // 64-token tiles per sequence; work items are (b, h, kv tile)
   int nsel;   // sparse blocks per sequence (k2q rows per head)
   int tiles;  // 64-token tiles per sparse block: 1, or 2 for 128-token blocks
-  int max_q, total;
+  int max_q;
+  // The last `nsplit` items (claim positions split0 ..) are each taken as two halves of their
+  // step list, so that the grid's last claims are half as long.  A half adds its dK, dV rows
+  // (fp32, scaled) into split_acc[slot] ([dV, dK][64 kv rows][128]), zeroed before the launch,
+  // and records the item's first output row in split_row[slot]; the postprocess writes the
+  // bf16 rows once both halves are in.
+  int split0, nsplit;
+  float* split_acc;
+  int32_t* split_row;
+  int total;  // claim positions: split0 + 2 * nsplit
   float sm_scale;
 };
 
@@ -130,11 +142,19 @@ struct Params {
 // processes a pair of 64-token q tiles: two consecutive list entries (64-token blocks; an odd
 // tail repeats the last one), or the two tiles of one 128-token entry.
 struct Item {
-  int bh, j, sel, n, np;
+  int bh, j, sel, n;
+  int first, np;  // this claim's steps: first .. first + np - 1 of the item's list
+  int slot;       // split slot, or -1 for a whole item
   const int32_t* list;
 };
 
-__device__ __forceinline__ Item decode_item(const Params& p, int w) {
+__device__ __forceinline__ Item decode_item(const Params& p, int u) {
+  int w = u, part = -1, slot = -1;
+  if (u >= p.split0) {  // one half of a split item
+    slot = (u - p.split0) >> 1;
+    part = (u - p.split0) & 1;
+    w = p.split0 + slot;
+  }
   int half = 0, ws = w;
   if (p.tiles == 2) {
     half = w & 1;
@@ -147,7 +167,11 @@ __device__ __forceinline__ Item decode_item(const Params& p, int w) {
   it.sel = sel;
   const int n = p.k2q_num[sel];
   it.n = n < 0 ? 0 : (n > p.max_q ? p.max_q : n);
-  it.np = p.tiles == 2 ? it.n : (it.n + 1) >> 1;
+  const int np = p.tiles == 2 ? it.n : (it.n + 1) >> 1;
+  const int h = (np + 1) >> 1;  // steps of the first half (the second may have none)
+  it.first = part == 1 ? h : 0;
+  it.np = part < 0 ? np : (part == 0 ? h : np - h);
+  it.slot = slot;
   it.list = p.k2q_idx + static_cast<size_t>(sel) * p.max_q;
   return it;
 }
@@ -157,18 +181,19 @@ __device__ __forceinline__ int q_block(const Item& it, int x, int nq) {
   return (i < 0 || i >= nq) ? 0 : i;
 }
 
-// The two 64-token q tiles of step pp; false if the second one only repeats the first (odd
-// tail of a 64-token list).
+// The two 64-token q tiles of the claim's step pp; false if the second one only repeats the
+// first (odd tail of a 64-token list).
 __device__ __forceinline__ bool step_tiles(const Params& p, const Item& it, int pp, int* i0,
                                            int* i1) {
+  const int ps = it.first + pp;
   if (p.tiles == 2) {
-    *i0 = 2 * q_block(it, pp, p.nsel);
+    *i0 = 2 * q_block(it, ps, p.nsel);
     *i1 = *i0 + 1;
     return true;
   }
-  *i0 = q_block(it, 2 * pp, p.nsel);
-  const bool has2 = 2 * pp + 1 < it.n;
-  *i1 = has2 ? q_block(it, 2 * pp + 1, p.nsel) : *i0;
+  *i0 = q_block(it, 2 * ps, p.nsel);
+  const bool has2 = 2 * ps + 1 < it.n;
+  *i1 = has2 ? q_block(it, 2 * ps + 1, p.nsel) : *i0;
   return has2;
 }
 
@@ -290,7 +315,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       bad = __reduce_or_sync(0xffffffffu, bad);
       if (bad && lane == 0) atomicOr(p.err, bad);
-      if (it.n == 0) continue;
+      if (it.np == 0) continue;  // nothing to compute (an unselected block, or an empty half)
       if (!mbar_wait_warp(bar(KV_EMPTY), (itc & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) {
         ok = false;
         break;
@@ -320,8 +345,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int t0 = (tile0 + i0) * HEAD_DIM, t1 = (tile0 + i1) * HEAD_DIM;
         if (i1 == i0 + 1) {  // adjacent q tiles (always with 128-token blocks): one 32 KB copy
           if (lane < 2)
-            tma_load_2d(base + (lane == 0 ? SM_Q : SM_DO) + s * 32768u, lane == 0 ? &tm_q2 : &tm_do2,
-                        bar(QDO_FULL0 + s), 0, t0);
+            tma_load_2d(base + (lane == 0 ? SM_Q : SM_DO) + s * 32768u,
+                        lane == 0 ? &tm_q2 : &tm_do2, bar(QDO_FULL0 + s), 0, t0);
         } else if (lane < 4) {  // lanes 0, 1: Q tiles i0, i1; lanes 2, 3: dO tiles
           tma_load_2d(base + ((lane < 2) ? SM_Q : SM_DO) + s * 32768u + (lane & 1) * 16384u,
                       (lane < 2) ? &tm_q : &tm_do, bar(QDO_FULL0 + s), 0, (lane & 1) ? t1 : t0);
@@ -439,7 +464,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if (w >= p.total) break;
       const Item it = decode_item(p, w);
-      if (it.n == 0) continue;
+      if (it.np == 0) continue;  // nothing to compute (an unselected block, or an empty half)
       const int np = it.np;
       if (!mbar_wait_warp(bar(KV_FULL), itc & 1u, abort, WAIT_LIMIT_NS)) {
         ok = false;
@@ -524,7 +549,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if (w >= p.total) break;
       const Item it = decode_item(p, w);
-      if (it.n == 0) continue;
+      if (it.np == 0) continue;  // nothing to compute (an unselected block, or an empty half)
       const int vb = clamp_vbs(p.vbs[it.j]);
       const uint32_t* am = p.absmax + it.bh * 4;
       const int eq = operand_exponent(am[0]), ek = operand_exponent(am[1]);
@@ -637,7 +662,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const size_t row_kv = static_cast<size_t>(it.bh) * S + static_cast<size_t>(it.j) * BLOCK;
       __nv_bfloat16* dk_out = p.dk + row_kv * HEAD_DIM + d;
       __nv_bfloat16* dv_out = p.dv + row_kv * HEAD_DIM + d;
-      if (it.n == 0) {
+      if (it.slot < 0 && it.n == 0) {
         // No q block selects this kv block: exact-zero dK/dV rows.
         const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
         for (int t = 0; t < BLOCK; ++t) {
@@ -715,33 +740,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) raise_abort(abort, p.err);
         break;
       }
-      if (!warp_wait(bar(ACC_FULL), itc & 1u, abort, lane)) {
-        if (lane == 0) raise_abort(abort, p.err);
-        break;
-      }
-      tc_fence_after_sync();
-      // dV^T and dK^T rows (head dim d, kv rows 0..63) in 32-column chunks; masked kv rows get
-      // an explicit +0.0.
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        const bool is_dk = c >= 2;
-        const uint32_t col = (is_dk ? TM_DKT : TM_DVT) + (c & 1) * 32u;
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem + lane_off + col, v);
-        tmem_wait_ld();
-        if (c == 3) {
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(ACC_EMPTY));
+      // A split item's rows of this warp's 32 head dims: [dV, dK][64 kv rows][128] fp32.
+      float* acc = nullptr;
+      if (it.slot >= 0)
+        acc = p.split_acc + static_cast<size_t>(it.slot) * (2 * BLOCK * HEAD_DIM) + d;
+      if (np > 0) {
+        if (!warp_wait(bar(ACC_FULL), itc & 1u, abort, lane)) {
+          if (lane == 0) raise_abort(abort, p.err);
+          break;
         }
-        __nv_bfloat16* out = (is_dk ? dk_out : dv_out) + (c & 1) * 32 * HEAD_DIM;
-        const float sc = is_dk ? sk_scale : sv_scale;
+        tc_fence_after_sync();
+        // dV^T and dK^T rows (head dim d, kv rows 0..63) in 32-column chunks; masked kv rows get
+        // an explicit +0.0.  A half of a split item adds its scaled rows into the split
+        // accumulator instead (masked rows are left at zero).
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          const bool is_dk = c >= 2;
+          const uint32_t col = (is_dk ? TM_DKT : TM_DVT) + (c & 1) * 32u;
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + col, v);
+          tmem_wait_ld();
+          if (c == 3) {
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(ACC_EMPTY));
+          }
+          const float sc = is_dk ? sk_scale : sv_scale;
+          if (acc) {  // both halves add into zeroed memory: the sums do not depend on order
+            float* a = acc + ((is_dk ? BLOCK : 0) + (c & 1) * 32) * HEAD_DIM;
 #pragma unroll
-        for (int t = 0; t < 32; ++t)
-          out[t * HEAD_DIM] =
-              __float2bfloat16_rn((c & 1) * 32 + t < vb ? __uint_as_float(v[t]) * sc : 0.f);
+            for (int t = 0; t < 32; ++t)
+              if ((c & 1) * 32 + t < vb) atomicAdd(a + t * HEAD_DIM, __uint_as_float(v[t]) * sc);
+          } else {
+            __nv_bfloat16* out = (is_dk ? dk_out : dv_out) + (c & 1) * 32 * HEAD_DIM;
+#pragma unroll
+            for (int t = 0; t < 32; ++t)
+              out[t * HEAD_DIM] =
+                  __float2bfloat16_rn((c & 1) * 32 + t < vb ? __uint_as_float(v[t]) * sc : 0.f);
+          }
+        }
+        ++itc;
       }
-      ++itc;
+      if (acc && wq == 0 && lane == 0) p.split_row[it.slot] = static_cast<int32_t>(row_kv);
     }
     // Every reduction this warp issued has landed before the CTA retires.
     if (lane == 0) bulk_wait_all();
@@ -755,6 +795,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 }  // namespace
+
+int bwd_split_items(int items) {
+  // One split item per CTA: the grid's last claims are then half items.
+  const int sms = device_sm_count();
+  const int grid = items < sms ? items : sms;
+  const int cap = split_capacity(items);
+  return grid < cap ? grid : cap;
+}
 
 cudaError_t launch_bwd_main(const BwdMainArgs& a, cudaStream_t stream) {
   const long rows = static_cast<long>(a.B) * a.H * a.S;
@@ -794,10 +842,15 @@ cudaError_t launch_bwd_main(const BwdMainArgs& a, cudaStream_t stream) {
   p.nsel = a.nsel;
   p.tiles = a.tiles;
   p.max_q = a.max_q;
-  p.total = a.B * a.H * a.nb;
   p.sm_scale = a.sm_scale;
+  const int items = a.B * a.H * a.nb;
   const int sms = device_sm_count();
-  const int grid = p.total < sms ? p.total : sms;
+  const int grid = items < sms ? items : sms;
+  p.nsplit = bwd_split_items(items);
+  p.split0 = items - p.nsplit;
+  p.total = items + p.nsplit;
+  p.split_acc = a.split_acc;
+  p.split_row = a.split_row;
   bwd_main_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tq, tq2, tk, tv, tdo, tdo2, tdq, p);
   return cudaGetLastError();
 }

@@ -186,11 +186,11 @@ __global__ void __launch_bounds__(256) order_kernel(const int32_t* __restrict__ 
   order[static_cast<size_t>(bh) * nb + pos] = bh * nb + x;
 }
 
-__global__ void __launch_bounds__(256) postprocess_kernel(const float4* __restrict__ dqacc,
-                                                          const uint32_t* __restrict__ absmax,
-                                                          size_t chunks_per_head,
-                                                          size_t total_chunks, float sm_scale,
-                                                          uint4* __restrict__ dq) {
+__global__ void __launch_bounds__(256) postprocess_kernel(
+    const float4* __restrict__ dqacc, const uint32_t* __restrict__ absmax, size_t chunks_per_head,
+    size_t total_chunks, float sm_scale, uint4* __restrict__ dq,
+    const float4* __restrict__ split_acc, const int32_t* __restrict__ split_row, int split_chunks,
+    uint4* __restrict__ dk, uint4* __restrict__ dv) {
   for (size_t c = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; c < total_chunks;
        c += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const int bh = static_cast<int>(c / chunks_per_head);
@@ -206,6 +206,24 @@ __global__ void __launch_bounds__(256) postprocess_kernel(const float4* __restri
                        *reinterpret_cast<const uint32_t*>(&r1),
                        *reinterpret_cast<const uint32_t*>(&r2),
                        *reinterpret_cast<const uint32_t*>(&r3));
+  }
+  // Split items of the main kernel: slot s holds [dV, dK][64 kv rows][128] fp32, already scaled
+  // (rows past the block's valid size hold zeros); 16 chunks of 8 per row.
+  for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < split_chunks;
+       c += gridDim.x * blockDim.x) {
+    const int slot = c / (2 * BLOCK * 16), rem = c % (2 * BLOCK * 16);
+    const bool is_dk = rem >= BLOCK * 16;
+    const int t = (rem / 16) % BLOCK, d8 = rem % 16;
+    const float4 a = split_acc[2 * c], b = split_acc[2 * c + 1];
+    const __nv_bfloat162 r0 = __floats2bfloat162_rn(a.x, a.y);
+    const __nv_bfloat162 r1 = __floats2bfloat162_rn(a.z, a.w);
+    const __nv_bfloat162 r2 = __floats2bfloat162_rn(b.x, b.y);
+    const __nv_bfloat162 r3 = __floats2bfloat162_rn(b.z, b.w);
+    const size_t at = (static_cast<size_t>(split_row[slot]) + t) * 16 + d8;
+    (is_dk ? dk : dv)[at] = make_uint4(*reinterpret_cast<const uint32_t*>(&r0),
+                                       *reinterpret_cast<const uint32_t*>(&r1),
+                                       *reinterpret_cast<const uint32_t*>(&r2),
+                                       *reinterpret_cast<const uint32_t*>(&r3));
   }
 }
 
@@ -323,12 +341,16 @@ cudaError_t launch_order(const int32_t* k2q_num, int BH, int nb, int max_q, int3
 }
 
 cudaError_t launch_postprocess(const float* dqacc, const uint32_t* absmax, int BH, int S,
-                               float sm_scale, __nv_bfloat16* dq, cudaStream_t stream) {
+                               float sm_scale, __nv_bfloat16* dq, const float* split_acc,
+                               const int32_t* split_row, int nsplit, __nv_bfloat16* dk,
+                               __nv_bfloat16* dv, cudaStream_t stream) {
   const size_t per_head = static_cast<size_t>(S) * HEAD_DIM / 8;
   const size_t total = per_head * BH;
+  const int split_chunks = nsplit * 2 * BLOCK * (HEAD_DIM / 8);
   postprocess_kernel<<<grid_for(total, 256, 8), 256, 0, stream>>>(
       reinterpret_cast<const float4*>(dqacc), absmax, per_head, total, sm_scale,
-      reinterpret_cast<uint4*>(dq));
+      reinterpret_cast<uint4*>(dq), reinterpret_cast<const float4*>(split_acc), split_row,
+      split_chunks, reinterpret_cast<uint4*>(dk), reinterpret_cast<uint4*>(dv));
   return cudaGetLastError();
 }
 

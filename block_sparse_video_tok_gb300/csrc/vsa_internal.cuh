@@ -29,8 +29,16 @@ constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;   // in-flight copies after an
 // dO), then 1024-byte aligned arrays.
 
 struct BwdLayout {
-  size_t err, sched, absmax, delta, order, vbs64, dqacc, q16, k16, v16, do16, total;
+  size_t err, sched, absmax, split_row, split_acc, delta, order, vbs64, dqacc, q16, k16, v16, do16,
+      total;
 };
+
+// Items of the backward's main kernel that are split in two at the end of the grid (at most one
+// per CTA, a quarter of the items and SPLIT_MAX): W = B * H * S / 64 items.
+constexpr int SPLIT_MAX = 256;
+inline int split_capacity(long W) {
+  return static_cast<int>(W / 4 < SPLIT_MAX ? W / 4 : SPLIT_MAX);
+}
 struct FwdLayout {
   size_t err, sched, absmax, bitmap, vbs64, v16, total;
 };
@@ -46,6 +54,13 @@ inline BwdLayout bwd_layout(long B, long H, long S) {
   off += 256;
   L.absmax = off;
   off = align_up(off + bh * 4 * sizeof(uint32_t), 1024);
+  // Split items: the first output row and [dV, dK][64][128] fp32 sums each.  Zeroed with the
+  // header and the maxima on every call.
+  const size_t nsplit = static_cast<size_t>(split_capacity(static_cast<long>(bh * nb)));
+  L.split_row = off;
+  off = align_up(off + nsplit * sizeof(int32_t), 1024);
+  L.split_acc = off;
+  off = align_up(off + nsplit * 2 * BLOCK * HEAD_DIM * sizeof(float), 1024);
   L.delta = off;
   off = align_up(off + rows * sizeof(float), 1024);
   L.order = off;
@@ -140,8 +155,12 @@ cudaError_t launch_convert_t(const __nv_bfloat16* q, const __nv_bfloat16* dout, 
 cudaError_t launch_order(const int32_t* k2q_num, int BH, int nb, int max_q, int32_t* order,
                          cudaStream_t stream);
 
+// dQ = bf16(dqacc * scale); then the bf16 dV, dK rows of the main kernel's `nsplit` split items
+// from their fp32 sums.
 cudaError_t launch_postprocess(const float* dqacc, const uint32_t* absmax, int BH, int S,
-                               float sm_scale, __nv_bfloat16* dq, cudaStream_t stream);
+                               float sm_scale, __nv_bfloat16* dq, const float* split_acc,
+                               const int32_t* split_row, int nsplit, __nv_bfloat16* dk,
+                               __nv_bfloat16* dv, cudaStream_t stream);
 
 struct BwdMainArgs {
   const __half *q16, *k16, *v16, *do16;
@@ -157,6 +176,8 @@ struct BwdMainArgs {
   __nv_bfloat16* dv;
   uint32_t* err;
   int32_t* sched;  // zeroed work counter
+  float* split_acc;    // zeroed, split_capacity(B * H * nb) slots of [2][64][128]
+  int32_t* split_row;  // [split_capacity]
   int B, H, S;
   int nb;     // 64-token tiles per sequence (kv items per head = nb)
   int nsel;   // sparse blocks per sequence (rows of k2q per head); nb = nsel * tiles
@@ -165,6 +186,8 @@ struct BwdMainArgs {
   float sm_scale;
 };
 cudaError_t launch_bwd_main(const BwdMainArgs& a, cudaStream_t stream);
+// Items the main kernel splits in two for `items` work items on this device.
+int bwd_split_items(int items);
 
 // Selection bitmap of the forward at 64-token granularity: [BH, nb * tiles, ceil(nb * tiles / 32)]
 // bits from q2k rows that count blocks of `tiles` 64-token tiles (1 or 2).
