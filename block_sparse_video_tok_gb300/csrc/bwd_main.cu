@@ -514,15 +514,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after_sync();
         issue_dk(g, pp == 0);
-        umma_commit_elect(bar(QDO_EMPTY0 + (g & 1u)));  // Q_p and dO_p of step g are no longer read
-        if (more) issue_dp(g + 1);
+        if (more) {
+          umma_commit_elect(bar(QDO_EMPTY0 + (g & 1u)));  // Q_p, dO_p of step g are no longer read
+          issue_dp(g + 1);
+        } else {
+          // dV^T and dK^T of the item are complete with dK^T(g): the drain warps read them out
+          // while dQ^T(g) runs, and the next item's dV^T can start that much earlier.
+          umma_commit_elect(bar(ACC_FULL));
+        }
         if (!issue_dq(g)) {
           ok = false;
           break;
         }
+        if (!more) umma_commit_elect(bar(QDO_EMPTY0 + (g & 1u)));
       }
       if (!ok) break;
-      umma_commit_elect(bar(ACC_FULL));
       umma_commit_elect(bar(KV_EMPTY));
       ++itc;
     }
@@ -679,7 +685,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int vb = clamp_vbs(p.vbs[it.j]);
       const int np = it.np;
       bool ok = true;
+      // A split item's rows of this warp's 32 head dims: [dV, dK][64 kv rows][128] fp32.
+      float* acc = nullptr;
+      if (it.slot >= 0)
+        acc = p.split_acc + static_cast<size_t>(it.slot) * (2 * BLOCK * HEAD_DIM) + d;
+      // The item's dV^T and dK^T, complete once its last dK^T is (before its last dQ^T): read
+      // out before the last step's dQ^T is drained, so that the next item's dV^T can start.
+      auto read_acc = [&]() -> bool {
+        if (!warp_wait(bar(ACC_FULL), itc & 1u, abort, lane)) return false;
+        tc_fence_after_sync();
+        // dV^T and dK^T rows (head dim d, kv rows 0..63) in 32-column chunks; masked kv rows get
+        // an explicit +0.0.  A half of a split item adds its scaled rows into the split
+        // accumulator instead (masked rows are left at zero).
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          const bool is_dk = c >= 2;
+          const uint32_t col = (is_dk ? TM_DKT : TM_DVT) + (c & 1) * 32u;
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + col, v);
+          tmem_wait_ld();
+          if (c == 3) {
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(ACC_EMPTY));
+          }
+          const float sc = is_dk ? sk_scale : sv_scale;
+          if (acc) {  // both halves add into zeroed memory: the sums do not depend on order
+            float* a = acc + ((is_dk ? BLOCK : 0) + (c & 1) * 32) * HEAD_DIM;
+#pragma unroll
+            for (int t = 0; t < 32; ++t)
+              if ((c & 1) * 32 + t < vb) atomicAdd(a + t * HEAD_DIM, __uint_as_float(v[t]) * sc);
+          } else {
+            __nv_bfloat16* out = (is_dk ? dk_out : dv_out) + (c & 1) * 32 * HEAD_DIM;
+#pragma unroll
+            for (int t = 0; t < 32; ++t)
+              out[t * HEAD_DIM] =
+                  __float2bfloat16_rn((c & 1) * 32 + t < vb ? __uint_as_float(v[t]) * sc : 0.f);
+          }
+        }
+        ++itc;
+        return true;
+      };
       for (int pp = 0; pp < np; ++pp, ++g) {
+        if (pp == np - 1 && !read_acc()) {
+          ok = false;
+          break;
+        }
         int i0, i1;
         const bool has2 = step_tiles(p, it, pp, &i0, &i1);
         const uint32_t buf = g & 1u;
@@ -739,47 +790,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) {
         if (lane == 0) raise_abort(abort, p.err);
         break;
-      }
-      // A split item's rows of this warp's 32 head dims: [dV, dK][64 kv rows][128] fp32.
-      float* acc = nullptr;
-      if (it.slot >= 0)
-        acc = p.split_acc + static_cast<size_t>(it.slot) * (2 * BLOCK * HEAD_DIM) + d;
-      if (np > 0) {
-        if (!warp_wait(bar(ACC_FULL), itc & 1u, abort, lane)) {
-          if (lane == 0) raise_abort(abort, p.err);
-          break;
-        }
-        tc_fence_after_sync();
-        // dV^T and dK^T rows (head dim d, kv rows 0..63) in 32-column chunks; masked kv rows get
-        // an explicit +0.0.  A half of a split item adds its scaled rows into the split
-        // accumulator instead (masked rows are left at zero).
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          const bool is_dk = c >= 2;
-          const uint32_t col = (is_dk ? TM_DKT : TM_DVT) + (c & 1) * 32u;
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem + lane_off + col, v);
-          tmem_wait_ld();
-          if (c == 3) {
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(ACC_EMPTY));
-          }
-          const float sc = is_dk ? sk_scale : sv_scale;
-          if (acc) {  // both halves add into zeroed memory: the sums do not depend on order
-            float* a = acc + ((is_dk ? BLOCK : 0) + (c & 1) * 32) * HEAD_DIM;
-#pragma unroll
-            for (int t = 0; t < 32; ++t)
-              if ((c & 1) * 32 + t < vb) atomicAdd(a + t * HEAD_DIM, __uint_as_float(v[t]) * sc);
-          } else {
-            __nv_bfloat16* out = (is_dk ? dk_out : dv_out) + (c & 1) * 32 * HEAD_DIM;
-#pragma unroll
-            for (int t = 0; t < 32; ++t)
-              out[t * HEAD_DIM] =
-                  __float2bfloat16_rn((c & 1) * 32 + t < vb ? __uint_as_float(v[t]) * sc : 0.f);
-          }
-        }
-        ++itc;
       }
       if (acc && wq == 0 && lane == 0) p.split_row[it.slot] = static_cast<int32_t>(row_kv);
     }
