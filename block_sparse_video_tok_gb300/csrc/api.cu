@@ -161,14 +161,18 @@ vsa_status vsa_fwd(const void* q, const void* k, const void* v, const int32_t* q
   if (e != cudaSuccess) return cuda_fail(e);
   // S = Q K^T takes the bf16 Q and K as given; only V needs the scaled fp16 copy that P.V (fp16
   // P) takes, so only V's maximum is scanned.
+  vsa::PreExtras x{};
+  x.vbs = vbs;
+  x.nb = nb;
+  x.tiles = blk / vsa::BLOCK;
+  x.vbs64 = vbs64;
+  x.err = err;
   if ((e = vsa::launch_absmax_delta(nullptr, nullptr, vb, nullptr, nullptr, BH, S, absmax, nullptr,
-                                    nullptr, s)) != cudaSuccess)
+                                    nullptr, x, s)) != cudaSuccess)
     return cuda_fail(e);
   const __nv_bfloat16* src[3] = {nullptr, nullptr, vb};
   __half* dst[3] = {nullptr, nullptr, v16};
   if ((e = vsa::launch_convert(src, dst, 3, BH, S, absmax, s)) != cudaSuccess) return cuda_fail(e);
-  if ((e = vsa::launch_vbs_expand(vbs, nb, blk / vsa::BLOCK, vbs64, err, s)) != cudaSuccess)
-    return cuda_fail(e);
   if ((e = vsa::launch_fwd_bitmap(q2k_idx, q2k_num, topk, BH, nb, blk / vsa::BLOCK, bitmap, err,
                                   s)) != cudaSuccess)
     return cuda_fail(e);
@@ -241,10 +245,19 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
 
   cudaError_t e = record(events ? events->start : nullptr, s);
   if (e != cudaSuccess) return cuda_fail(e);
-  // Header, work counter, maxima and the split items' counters and sums.
-  if ((e = cudaMemsetAsync(workspace, 0, L.delta, s)) != cudaSuccess)
-    return cuda_fail(e);
-  if ((e = vsa::launch_absmax_delta(qb, kb, vb, dob, ob, BH, S, absmax, delta, dqacc, s)) !=
+  // Header, work counter, maxima and the split items' rows; their sums are zeroed by the
+  // preprocess kernel.
+  if ((e = cudaMemsetAsync(workspace, 0, L.split_acc, s)) != cudaSuccess) return cuda_fail(e);
+  vsa::PreExtras x{};
+  x.vbs = vbs;
+  x.nb = nb;
+  x.tiles = blk / vsa::BLOCK;
+  x.vbs64 = vbs64;
+  x.err = err;
+  x.zero = ws_at<float4>(workspace, L.split_acc);
+  x.zero_n = static_cast<size_t>(vsa::bwd_split_items(BH * (S / vsa::BLOCK))) * 2 * vsa::BLOCK *
+             vsa::HEAD_DIM / 4;
+  if ((e = vsa::launch_absmax_delta(qb, kb, vb, dob, ob, BH, S, absmax, delta, dqacc, x, s)) !=
       cudaSuccess)
     return cuda_fail(e);
   // K and V row-major; Q and dO tile-transposed (one 16 KB copy per 64-row tile in the main
@@ -253,8 +266,6 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
   __half* dst[4] = {nullptr, k16, v16, nullptr};
   if ((e = vsa::launch_convert(src, dst, 4, BH, S, absmax, s)) != cudaSuccess) return cuda_fail(e);
   if ((e = vsa::launch_convert_t(qb, dob, q16, do16, BH, S, absmax, s)) != cudaSuccess)
-    return cuda_fail(e);
-  if ((e = vsa::launch_vbs_expand(vbs, nb, blk / vsa::BLOCK, vbs64, err, s)) != cudaSuccess)
     return cuda_fail(e);
   const int32_t* work_order = nullptr;
   if (S / vsa::BLOCK >= vsa::ORDER_MIN_KV_BLOCKS) {

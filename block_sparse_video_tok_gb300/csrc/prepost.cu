@@ -45,7 +45,24 @@ constexpr int PRE_THREADS = 256;
 __global__ void __launch_bounds__(PRE_THREADS) absmax_delta_kernel(
     const uint4* __restrict__ q, const uint4* __restrict__ k, const uint4* __restrict__ v,
     const uint4* __restrict__ dout, const uint4* __restrict__ o, int S, uint32_t* absmax,
-    float* __restrict__ delta, float4* __restrict__ dqacc) {
+    float* __restrict__ delta, float4* __restrict__ dqacc, PreExtras x) {
+  // The small jobs, spread over the whole grid: the clamped valid size of every 64-token kv
+  // tile (64-token tile t of block t / tiles), and zeroing of a scratch range.
+  {
+    const size_t gt =
+        (static_cast<size_t>(blockIdx.y) * gridDim.x + blockIdx.x) * PRE_THREADS + threadIdx.x;
+    const size_t gn = static_cast<size_t>(gridDim.x) * gridDim.y * PRE_THREADS;
+    const int lim = BLOCK * x.tiles;
+    uint32_t badv = 0;
+    for (size_t t = gt; t < static_cast<size_t>(x.nb) * x.tiles; t += gn) {
+      const int vv = x.vbs[t / x.tiles];
+      if (vv < 0 || vv > lim) badv |= VSA_DEVERR_VBS;
+      const int w = (vv < 0 ? 0 : (vv > lim ? lim : vv)) - BLOCK * static_cast<int>(t % x.tiles);
+      x.vbs64[t] = w < 0 ? 0 : (w > BLOCK ? BLOCK : w);
+    }
+    if (badv && x.err) atomicOr(x.err, badv);
+    for (size_t i = gt; i < x.zero_n; i += gn) x.zero[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   const int bh = blockIdx.y;
   const int half = threadIdx.x >> 4;  // which of the 16 rows-in-flight
   const int sub = threadIdx.x & 15;   // 16-byte chunk of the row
@@ -140,10 +157,18 @@ __global__ void __launch_bounds__(256) convert_t_kernel(ConvertTPack pk, int S,
   __half* __restrict__ dst = t == 0 ? pk.dst[0] : pk.dst[1];
   const float sc = exp2i(-operand_exponent(absmax[bh * 4 + (t == 0 ? pk.slot[0] : pk.slot[1])]));
   const size_t row0 = static_cast<size_t>(bh) * S + static_cast<size_t>(tile) * BLOCK;
-  for (int c = threadIdx.x; c < BLOCK * 16; c += blockDim.x) {
-    const int r = c >> 4, ch = c & 15;
-    const uint4 x = src[(row0 + r) * 16 + ch];
-    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  // The tile's 1024 16-byte chunks, four per thread, all loads in flight before any is used.
+  constexpr int PER = BLOCK * 16 / 256;
+  uint4 xs[PER];
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int c = threadIdx.x + u * 256;
+    xs[u] = src[(row0 + (c >> 4)) * 16 + (c & 15)];
+  }
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int c = threadIdx.x + u * 256, r = c >> 4, ch = c & 15;
+    const uint32_t w[4] = {xs[u].x, xs[u].y, xs[u].z, xs[u].w};
     __half2* d2 = reinterpret_cast<__half2*>(tl + r * LD + ch * 8);
 #pragma unroll
     for (int i = 0; i < 4; ++i) d2[i] = __floats2half2_rn(bf16lo(w[i]) * sc, bf16hi(w[i]) * sc);
@@ -263,21 +288,6 @@ __global__ void __launch_bounds__(256) fwd_bitmap_kernel(const int32_t* __restri
   if (bad && err) atomicOr(err, bad);
 }
 
-__global__ void __launch_bounds__(256) vbs_expand_kernel(const int32_t* __restrict__ vbs, int nb,
-                                                         int tiles, int32_t* __restrict__ vbs64,
-                                                         uint32_t* err) {
-  const int lim = BLOCK * tiles;
-  uint32_t bad = 0;
-  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < nb * tiles;
-       t += gridDim.x * blockDim.x) {
-    const int v = vbs[t / tiles];
-    if (v < 0 || v > lim) bad |= VSA_DEVERR_VBS;
-    const int w = (v < 0 ? 0 : (v > lim ? lim : v)) - BLOCK * (t % tiles);
-    vbs64[t] = w < 0 ? 0 : (w > BLOCK ? BLOCK : w);
-  }
-  if (bad && err) atomicOr(err, bad);
-}
-
 int grid_for(size_t work, int threads, int per_sm) {
   const size_t want = (work + threads - 1) / threads;
   const size_t cap = static_cast<size_t>(device_sm_count()) * per_sm;
@@ -289,12 +299,13 @@ int grid_for(size_t work, int threads, int per_sm) {
 cudaError_t launch_absmax_delta(const __nv_bfloat16* q, const __nv_bfloat16* k,
                                 const __nv_bfloat16* v, const __nv_bfloat16* dout,
                                 const __nv_bfloat16* o, int BH, int S, uint32_t* absmax,
-                                float* delta, float* dqacc, cudaStream_t stream) {
+                                float* delta, float* dqacc, const PreExtras& x,
+                                cudaStream_t stream) {
   dim3 grid(static_cast<unsigned>(S / BLOCK), static_cast<unsigned>(BH));
   absmax_delta_kernel<<<grid, PRE_THREADS, 0, stream>>>(
       reinterpret_cast<const uint4*>(q), reinterpret_cast<const uint4*>(k),
       reinterpret_cast<const uint4*>(v), reinterpret_cast<const uint4*>(dout),
-      reinterpret_cast<const uint4*>(o), S, absmax, delta, reinterpret_cast<float4*>(dqacc));
+      reinterpret_cast<const uint4*>(o), S, absmax, delta, reinterpret_cast<float4*>(dqacc), x);
   return cudaGetLastError();
 }
 
@@ -360,13 +371,6 @@ cudaError_t launch_fwd_bitmap(const int32_t* q2k_idx, const int32_t* q2k_num, in
   const size_t entries = static_cast<size_t>(BH) * nb * topk;
   fwd_bitmap_kernel<<<grid_for(entries, 256, 4), 256, 0, stream>>>(q2k_idx, q2k_num, topk, nb,
                                                                     tiles, entries, bitmap, err);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_vbs_expand(const int32_t* vbs, int nb, int tiles, int32_t* vbs64,
-                              uint32_t* err, cudaStream_t stream) {
-  vbs_expand_kernel<<<grid_for(static_cast<size_t>(nb) * tiles, 256, 1), 256, 0, stream>>>(
-      vbs, nb, tiles, vbs64, err);
   return cudaGetLastError();
 }
 

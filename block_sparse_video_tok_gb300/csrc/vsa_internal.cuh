@@ -137,10 +137,22 @@ cudaError_t launch_invert(const int32_t* q2k_idx, const int32_t* q2k_num, int to
 
 // Per-head absolute maxima of the operands; with `o`/`dout` non-null also Delta = rowsum(O*dO)
 // and zeroing of the fp32 dQ accumulator.
+// Jobs too small for a launch of their own, done by the absmax_delta grid: the valid size of
+// every 64-token kv tile, vbs64[t] = clamp(vbs[t / tiles] - 64 (t % tiles), 0, 64) (an entry
+// outside [0, 64 tiles] raises VSA_DEVERR_VBS in *err), and zeroing `zero_n` float4s.
+struct PreExtras {
+  const int32_t* vbs;
+  int nb, tiles;
+  int32_t* vbs64;
+  uint32_t* err;
+  float4* zero;
+  size_t zero_n;
+};
 cudaError_t launch_absmax_delta(const __nv_bfloat16* q, const __nv_bfloat16* k,
                                 const __nv_bfloat16* v, const __nv_bfloat16* dout,
                                 const __nv_bfloat16* o, int BH, int S, uint32_t* absmax,
-                                float* delta, float* dqacc, cudaStream_t stream);
+                                float* delta, float* dqacc, const PreExtras& x,
+                                cudaStream_t stream);
 
 // fp16 copies X' = X * 2^-e(head) of up to four [BH, S, 128] bf16 tensors (null entries skipped).
 cudaError_t launch_convert(const __nv_bfloat16* const* src, __half* const* dst, int count, int BH,
@@ -195,10 +207,6 @@ cudaError_t launch_fwd_bitmap(const int32_t* q2k_idx, const int32_t* q2k_num, in
                               int nb, int tiles, uint32_t* bitmap, uint32_t* err,
                               cudaStream_t stream);
 
-// vbs64[t] = valid tokens of 64-token tile t from the per-block sizes of blocks of `tiles`
-// 64-token tiles (block sizes clamped to [0, 64 * tiles]; VSA_DEVERR_VBS when one is outside).
-cudaError_t launch_vbs_expand(const int32_t* vbs, int nb, int tiles, int32_t* vbs64,
-                              uint32_t* err, cudaStream_t stream);
 
 struct FwdMainArgs {
   const __nv_bfloat16 *q, *k;  // the caller's bf16 Q and K (the S = Q K^T operands)
