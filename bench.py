@@ -346,7 +346,8 @@ def main():
     k2q_num = torch.empty((B, H, nb), dtype=torch.int32, device=device)
     dq, dk, dv = (torch.empty_like(dev["q"]) for _ in range(3))
     ws = torch.empty(vsa.vsa_bwd_workspace_bytes(B, H, S), dtype=torch.uint8, device=device)
-    kernels_per_step = 5 + (1 if nb >= 1024 else 0)  # invert, absmax/delta, convert, [order], main, post
+    # invert, absmax/delta, convert (K, V), convert_t (Q, dO), [order], main, postprocess
+    kernels_per_step = 6 + (1 if nb >= 1024 else 0)
 
     def step(events=None, inv=None):
         if inv is not None:
