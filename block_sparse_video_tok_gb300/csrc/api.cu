@@ -245,8 +245,7 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
 
   cudaError_t e = record(events ? events->start : nullptr, s);
   if (e != cudaSuccess) return cuda_fail(e);
-  // Header, work counter, maxima and the split items' rows; their sums are zeroed by the
-  // preprocess kernel.
+  // Header, work counter, maxima and the split items' rows.
   if ((e = cudaMemsetAsync(workspace, 0, L.split_acc, s)) != cudaSuccess) return cuda_fail(e);
   vsa::PreExtras x{};
   x.vbs = vbs;
@@ -254,9 +253,6 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
   x.tiles = blk / vsa::BLOCK;
   x.vbs64 = vbs64;
   x.err = err;
-  x.zero = ws_at<float4>(workspace, L.split_acc);
-  x.zero_n = static_cast<size_t>(vsa::bwd_split_items(BH * (S / vsa::BLOCK))) * 2 * vsa::BLOCK *
-             vsa::HEAD_DIM / 4;
   if ((e = vsa::launch_absmax_delta(qb, kb, vb, dob, ob, BH, S, absmax, delta, dqacc, x, s)) !=
       cudaSuccess)
     return cuda_fail(e);

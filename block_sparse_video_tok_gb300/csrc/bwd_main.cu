@@ -20,9 +20,9 @@
 //
 // Work items are claimed dynamically (queue.cuh).  With 128-token blocks an item is one of the
 // two 64-token kv tiles of a block, and each k2q entry supplies a whole q tile pair.  The last
-// items of the claim order (one per CTA) are handed out as two halves of their step lists, so
-// the grid's end is spread over half an item; a half adds its fp32 dK, dV rows into a zeroed
-// workspace slot, which the postprocess turns into bf16.
+// items of the claim order (one per two CTAs) are handed out as four claims each, one per
+// quarter of their step lists, so the grid ends on short claims; a part stores its fp32 dK, dV
+// rows in a workspace slot of its own, and the postprocess adds the parts and writes bf16.
 //
 // Roles (448 threads):
 //   warps 0-7  softmax: warps w and w+4 share TMEM lane quarter w (query rows 32w..32w+31 of the
@@ -126,15 +126,15 @@ struct Params {
   int nsel;   // sparse blocks per sequence (k2q rows per head)
   int tiles;  // 64-token tiles per sparse block: 1, or 2 for 128-token blocks
   int max_q;
-  // The last `nsplit` items (claim positions split0 ..) are each taken as two halves of their
-  // step list, so that the grid's last claims are half as long.  A half adds its dK, dV rows
-  // (fp32, scaled) into split_acc[slot] ([dV, dK][64 kv rows][128]), zeroed before the launch,
-  // and records the item's first output row in split_row[slot]; the postprocess writes the
-  // bf16 rows once both halves are in.
+  // The last `nsplit` items (claim positions split0 ..) are each taken as SPLIT_PARTS claims,
+  // one per consecutive share of their step list, so that the grid's last claims are short.
+  // Part x stores its dK, dV rows (fp32, scaled; zeros for masked rows and for a part without
+  // steps) in split_acc[slot][x] ([dV, dK][64 kv rows][128]) and the item's first output row in
+  // split_row[slot]; the postprocess adds the parts in a fixed order and writes the bf16 rows.
   int split0, nsplit;
   float* split_acc;
   int32_t* split_row;
-  int total;  // claim positions: split0 + 2 * nsplit
+  int total;  // claim positions: split0 + SPLIT_PARTS * nsplit
   float sm_scale;
 };
 
@@ -144,15 +144,15 @@ struct Params {
 struct Item {
   int bh, j, sel, n;
   int first, np;  // this claim's steps: first .. first + np - 1 of the item's list
-  int slot;       // split slot, or -1 for a whole item
+  int slot, part;  // split slot and part, or -1 for a whole item
   const int32_t* list;
 };
 
 __device__ __forceinline__ Item decode_item(const Params& p, int u) {
   int w = u, part = -1, slot = -1;
-  if (u >= p.split0) {  // one half of a split item
-    slot = (u - p.split0) >> 1;
-    part = (u - p.split0) & 1;
+  if (u >= p.split0) {  // one part of a split item
+    slot = (u - p.split0) / SPLIT_PARTS;
+    part = (u - p.split0) % SPLIT_PARTS;
     w = p.split0 + slot;
   }
   int half = 0, ws = w;
@@ -168,10 +168,12 @@ __device__ __forceinline__ Item decode_item(const Params& p, int u) {
   const int n = p.k2q_num[sel];
   it.n = n < 0 ? 0 : (n > p.max_q ? p.max_q : n);
   const int np = p.tiles == 2 ? it.n : (it.n + 1) >> 1;
-  const int h = (np + 1) >> 1;  // steps of the first half (the second may have none)
-  it.first = part == 1 ? h : 0;
-  it.np = part < 0 ? np : (part == 0 ? h : np - h);
+  // Part x takes steps [np x / P, np (x + 1) / P): shares differ by at most one, and a part
+  // may have none when the list is short.
+  it.first = part < 0 ? 0 : np * part / SPLIT_PARTS;
+  it.np = part < 0 ? np : np * (part + 1) / SPLIT_PARTS - it.first;
   it.slot = slot;
+  it.part = part;
   it.list = p.k2q_idx + static_cast<size_t>(sel) * p.max_q;
   return it;
 }
@@ -685,18 +687,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int vb = clamp_vbs(p.vbs[it.j]);
       const int np = it.np;
       bool ok = true;
-      // A split item's rows of this warp's 32 head dims: [dV, dK][64 kv rows][128] fp32.
+      // A split part's rows of this warp's 32 head dims: [dV, dK][64 kv rows][128] fp32.
       float* acc = nullptr;
       if (it.slot >= 0)
-        acc = p.split_acc + static_cast<size_t>(it.slot) * (2 * BLOCK * HEAD_DIM) + d;
+        acc = p.split_acc +
+              static_cast<size_t>(it.slot * SPLIT_PARTS + it.part) * (2 * BLOCK * HEAD_DIM) + d;
       // The item's dV^T and dK^T, complete once its last dK^T is (before its last dQ^T): read
       // out before the last step's dQ^T is drained, so that the next item's dV^T can start.
       auto read_acc = [&]() -> bool {
         if (!warp_wait(bar(ACC_FULL), itc & 1u, abort, lane)) return false;
         tc_fence_after_sync();
         // dV^T and dK^T rows (head dim d, kv rows 0..63) in 32-column chunks; masked kv rows get
-        // an explicit +0.0.  A half of a split item adds its scaled rows into the split
-        // accumulator instead (masked rows are left at zero).
+        // an explicit +0.0.  A split part stores its scaled fp32 rows in its own slot instead.
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           const bool is_dk = c >= 2;
@@ -710,11 +712,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (lane == 0) mbar_arrive(bar(ACC_EMPTY));
           }
           const float sc = is_dk ? sk_scale : sv_scale;
-          if (acc) {  // both halves add into zeroed memory: the sums do not depend on order
+          if (acc) {
             float* a = acc + ((is_dk ? BLOCK : 0) + (c & 1) * 32) * HEAD_DIM;
 #pragma unroll
             for (int t = 0; t < 32; ++t)
-              if ((c & 1) * 32 + t < vb) atomicAdd(a + t * HEAD_DIM, __uint_as_float(v[t]) * sc);
+              a[t * HEAD_DIM] = (c & 1) * 32 + t < vb ? __uint_as_float(v[t]) * sc : 0.f;
           } else {
             __nv_bfloat16* out = (is_dk ? dk_out : dv_out) + (c & 1) * 32 * HEAD_DIM;
 #pragma unroll
@@ -791,6 +793,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) raise_abort(abort, p.err);
         break;
       }
+      if (acc && np == 0) {  // a part without steps contributes zeros
+        for (int t = 0; t < 2 * BLOCK; ++t) acc[t * HEAD_DIM] = 0.f;
+      }
       if (acc && wq == 0 && lane == 0) p.split_row[it.slot] = static_cast<int32_t>(row_kv);
     }
     // Every reduction this warp issued has landed before the CTA retires.
@@ -807,11 +812,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }  // namespace
 
 int bwd_split_items(int items) {
-  // One split item per CTA: the grid's last claims are then half items.
+  // SPLIT_CLAIMS split claims per CTA on average: enough short claims at the end of the grid
+  // for the CTAs that finish their whole items early to even out the finishing times.
   const int sms = device_sm_count();
   const int grid = items < sms ? items : sms;
+  const int want =
+      SPLIT_CLAIMS * grid / SPLIT_PARTS > 0 ? SPLIT_CLAIMS * grid / SPLIT_PARTS : 1;
   const int cap = split_capacity(items);
-  return grid < cap ? grid : cap;
+  return want < cap ? want : cap;
 }
 
 cudaError_t launch_bwd_main(const BwdMainArgs& a, cudaStream_t stream) {
@@ -858,7 +866,7 @@ cudaError_t launch_bwd_main(const BwdMainArgs& a, cudaStream_t stream) {
   const int grid = items < sms ? items : sms;
   p.nsplit = bwd_split_items(items);
   p.split0 = items - p.nsplit;
-  p.total = items + p.nsplit;
+  p.total = items + (SPLIT_PARTS - 1) * p.nsplit;
   p.split_acc = a.split_acc;
   p.split_row = a.split_row;
   bwd_main_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tq, tq2, tk, tv, tdo, tdo2, tdq, p);

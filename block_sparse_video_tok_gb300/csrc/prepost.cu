@@ -46,8 +46,8 @@ __global__ void __launch_bounds__(PRE_THREADS) absmax_delta_kernel(
     const uint4* __restrict__ q, const uint4* __restrict__ k, const uint4* __restrict__ v,
     const uint4* __restrict__ dout, const uint4* __restrict__ o, int S, uint32_t* absmax,
     float* __restrict__ delta, float4* __restrict__ dqacc, PreExtras x) {
-  // The small jobs, spread over the whole grid: the clamped valid size of every 64-token kv
-  // tile (64-token tile t of block t / tiles), and zeroing of a scratch range.
+  // A small job spread over the whole grid: the clamped valid size of every 64-token kv tile
+  // (64-token tile t of block t / tiles).
   {
     const size_t gt =
         (static_cast<size_t>(blockIdx.y) * gridDim.x + blockIdx.x) * PRE_THREADS + threadIdx.x;
@@ -61,7 +61,6 @@ __global__ void __launch_bounds__(PRE_THREADS) absmax_delta_kernel(
       x.vbs64[t] = w < 0 ? 0 : (w > BLOCK ? BLOCK : w);
     }
     if (badv && x.err) atomicOr(x.err, badv);
-    for (size_t i = gt; i < x.zero_n; i += gn) x.zero[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   const int bh = blockIdx.y;
   const int half = threadIdx.x >> 4;  // which of the 16 rows-in-flight
@@ -232,14 +231,23 @@ __global__ void __launch_bounds__(256) postprocess_kernel(
                        *reinterpret_cast<const uint32_t*>(&r2),
                        *reinterpret_cast<const uint32_t*>(&r3));
   }
-  // Split items of the main kernel: slot s holds [dV, dK][64 kv rows][128] fp32, already scaled
-  // (rows past the block's valid size hold zeros); 16 chunks of 8 per row.
+  // Split items of the main kernel: part x of slot s holds [dV, dK][64 kv rows][128] fp32,
+  // already scaled (rows past the block's valid size hold zeros); 16 chunks of 8 per row.  The
+  // parts are added in order, so the sums do not depend on which part finished first.
   for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < split_chunks;
        c += gridDim.x * blockDim.x) {
     const int slot = c / (2 * BLOCK * 16), rem = c % (2 * BLOCK * 16);
     const bool is_dk = rem >= BLOCK * 16;
     const int t = (rem / 16) % BLOCK, d8 = rem % 16;
-    const float4 a = split_acc[2 * c], b = split_acc[2 * c + 1];
+    const float4* part =
+        split_acc + (static_cast<size_t>(slot) * SPLIT_PARTS * 2 * BLOCK * 16 + rem) * 2;
+    float4 a = part[0], b = part[1];
+#pragma unroll
+    for (int x = 1; x < SPLIT_PARTS; ++x) {
+      const float4 a2 = part[x * 2 * BLOCK * 16 * 2], b2 = part[x * 2 * BLOCK * 16 * 2 + 1];
+      a = make_float4(a.x + a2.x, a.y + a2.y, a.z + a2.z, a.w + a2.w);
+      b = make_float4(b.x + b2.x, b.y + b2.y, b.z + b2.z, b.w + b2.w);
+    }
     const __nv_bfloat162 r0 = __floats2bfloat162_rn(a.x, a.y);
     const __nv_bfloat162 r1 = __floats2bfloat162_rn(a.z, a.w);
     const __nv_bfloat162 r2 = __floats2bfloat162_rn(b.x, b.y);

@@ -33,11 +33,22 @@ struct BwdLayout {
       total;
 };
 
-// Items of the backward's main kernel that are split in two at the end of the grid (at most one
-// per CTA, a quarter of the items and SPLIT_MAX): W = B * H * S / 64 items.
-constexpr int SPLIT_MAX = 256;
+// The backward's main kernel hands out its last items as SPLIT_PARTS claims each (shares of the
+// item's step list), so that the grid ends on short claims.  split_capacity(W): how many of the
+// W = B * H * S / 64 items the workspace has room to split, SPLIT_PARTS slots of 64 KB each,
+// at most a quarter of W slots in all (about 256 bytes per token row) and SPLIT_MAX_SLOTS.
+#ifndef VSA_SPLIT_PARTS
+#define VSA_SPLIT_PARTS 4
+#endif
+constexpr int SPLIT_PARTS = VSA_SPLIT_PARTS;
+#ifndef VSA_SPLIT_CLAIMS
+#define VSA_SPLIT_CLAIMS 2
+#endif
+constexpr int SPLIT_CLAIMS = VSA_SPLIT_CLAIMS;  // split claims per CTA, on average
+constexpr int SPLIT_MAX_SLOTS = 512;
 inline int split_capacity(long W) {
-  return static_cast<int>(W / 4 < SPLIT_MAX ? W / 4 : SPLIT_MAX);
+  const long slots = W / 4 < SPLIT_MAX_SLOTS ? W / 4 : SPLIT_MAX_SLOTS;
+  return static_cast<int>(slots / SPLIT_PARTS);
 }
 struct FwdLayout {
   size_t err, sched, absmax, bitmap, vbs64, v16, total;
@@ -54,13 +65,12 @@ inline BwdLayout bwd_layout(long B, long H, long S) {
   off += 256;
   L.absmax = off;
   off = align_up(off + bh * 4 * sizeof(uint32_t), 1024);
-  // Split items: the first output row and [dV, dK][64][128] fp32 sums each.  Zeroed with the
-  // header and the maxima on every call.
+  // Split items: the first output row, and [parts][dV, dK][64][128] fp32 rows each.
   const size_t nsplit = static_cast<size_t>(split_capacity(static_cast<long>(bh * nb)));
   L.split_row = off;
   off = align_up(off + nsplit * sizeof(int32_t), 1024);
   L.split_acc = off;
-  off = align_up(off + nsplit * 2 * BLOCK * HEAD_DIM * sizeof(float), 1024);
+  off = align_up(off + nsplit * SPLIT_PARTS * 2 * BLOCK * HEAD_DIM * sizeof(float), 1024);
   L.delta = off;
   off = align_up(off + rows * sizeof(float), 1024);
   L.order = off;
@@ -137,16 +147,14 @@ cudaError_t launch_invert(const int32_t* q2k_idx, const int32_t* q2k_num, int to
 
 // Per-head absolute maxima of the operands; with `o`/`dout` non-null also Delta = rowsum(O*dO)
 // and zeroing of the fp32 dQ accumulator.
-// Jobs too small for a launch of their own, done by the absmax_delta grid: the valid size of
+// A job too small for a launch of its own, done by the absmax_delta grid: the valid size of
 // every 64-token kv tile, vbs64[t] = clamp(vbs[t / tiles] - 64 (t % tiles), 0, 64) (an entry
-// outside [0, 64 tiles] raises VSA_DEVERR_VBS in *err), and zeroing `zero_n` float4s.
+// outside [0, 64 tiles] raises VSA_DEVERR_VBS in *err).
 struct PreExtras {
   const int32_t* vbs;
   int nb, tiles;
   int32_t* vbs64;
   uint32_t* err;
-  float4* zero;
-  size_t zero_n;
 };
 cudaError_t launch_absmax_delta(const __nv_bfloat16* q, const __nv_bfloat16* k,
                                 const __nv_bfloat16* v, const __nv_bfloat16* dout,
@@ -167,8 +175,8 @@ cudaError_t launch_convert_t(const __nv_bfloat16* q, const __nv_bfloat16* dout, 
 cudaError_t launch_order(const int32_t* k2q_num, int BH, int nb, int max_q, int32_t* order,
                          cudaStream_t stream);
 
-// dQ = bf16(dqacc * scale); then the bf16 dV, dK rows of the main kernel's `nsplit` split items
-// from their fp32 sums.
+// dQ = bf16(dqacc * scale); then the bf16 dV, dK rows of the main kernel's `nsplit` split items:
+// the sum of their SPLIT_PARTS fp32 parts, added in part order.
 cudaError_t launch_postprocess(const float* dqacc, const uint32_t* absmax, int BH, int S,
                                float sm_scale, __nv_bfloat16* dq, const float* split_acc,
                                const int32_t* split_row, int nsplit, __nv_bfloat16* dk,
@@ -188,7 +196,7 @@ struct BwdMainArgs {
   __nv_bfloat16* dv;
   uint32_t* err;
   int32_t* sched;  // zeroed work counter
-  float* split_acc;    // zeroed, split_capacity(B * H * nb) slots of [2][64][128]
+  float* split_acc;    // split_capacity(B * H * nb) x SPLIT_PARTS slots of [2][64][128]
   int32_t* split_row;  // [split_capacity]
   int B, H, S;
   int nb;     // 64-token tiles per sequence (kv items per head = nb)

@@ -188,7 +188,7 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
 /* Largest workspace vsa_bwd_no_alloc can serve (32 MiB): the size of the static scratch array
  * that every GPU loading this library holds until the process exits.  A shape needs
  * vsa_bwd_workspace_bytes(shape) of it, about 1800 bytes per (batch, head, token) row on such
- * small shapes (1540 plus the fp32 sums of the main kernel's split items) and a small header: for
+ * small shapes (1540 plus the fp32 parts of the main kernel's split items) and a small header: for
  * example B = 1, H = 4, S = 4096 fits, H = 8 at S = 4096 does not. */
 #define VSA_BWD_NO_ALLOC_MAX_WORKSPACE_BYTES (32u * 1024u * 1024u)
 
