@@ -144,6 +144,13 @@ SMALL_CASES["blk128_odd_nb_topk3"] = lambda: wl.make_case(1, 2, 5, 3, vbs="ragge
 SMALL_CASES["blk128_batch2_zero_kv"] = lambda: wl.make_case(2, 2, 6, 2, vbs="ragged65", seed=33,
                                                            kv_pool=[0, 2, 3, 5], blk=128)
 
+# The backward hands out the last items of its grid in parts (shares of an item's step list).
+# With 16 heads of 16 kv blocks the last 16 items are split; with 3 q blocks per row most items
+# have two steps, so some parts have none, and kv blocks 14 and 15 (selected by no q block) give
+# split items without any step.
+SMALL_CASES["split_parts_short_lists"] = lambda: wl.make_case(1, 16, 16, 3, vbs="ragged32", seed=41,
+                                                             kv_pool=list(range(14)))
+
 SMALL_CASES["growing_scores"] = lambda: _scaled_kv_blocks(
     wl.make_case(1, 2, 16, 8, vbs="ragged32", seed=15), lambda j: 1.0 + j)
 SMALL_CASES["shrinking_scores"] = lambda: _scaled_kv_blocks(
@@ -182,6 +189,15 @@ def test_backward_matches_oracle(vsa, name):
                 lo = blk * j + (0 if k2q_num[b, h, j] == 0 else int(vbs[j]))
                 rows = slice(lo, blk * (j + 1))
                 assert zero_bits(dk[b, h, rows]).all() and zero_bits(dv[b, h, rows]).all(), (b, h, j)
+
+
+def test_split_parts_are_reproducible(vsa):
+    """Split items add their parts in a fixed order: two runs give the same dK and dV bits."""
+    case = SMALL_CASES["split_parts_short_lists"]()
+    _, _, (dq1, dk1, dv1), _ = _run_small(vsa, case)
+    _, _, (dq2, dk2, dv2), _ = _run_small(vsa, case)
+    assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
+    assert (dq1.float() - dq2.float()).abs().max() <= 5e-3 * dq1.float().abs().max()
 
 
 @pytest.mark.parametrize("name", list(SMALL_CASES))
