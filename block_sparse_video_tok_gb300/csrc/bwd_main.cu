@@ -6,17 +6,18 @@
 // has M = 128 (the q pair, or the 128 head-dim rows) and the fp32 accumulator maps row m to TMEM
 // lane m.  Per q pair (p = the pair's 128 query rows, all operands fp16 with per-head power-of-
 // two scales, fp32 accumulation):
-//   S   [128 q  x  64 kv] = Q_p  K_j^T      A = Q_p  (K-major), B = K_j (K-major)
-//   dP  [128 q  x  64 kv] = dO_p V_j^T      A = dO_p (K-major), B = V_j (K-major)
+//   S   [128 q  x  64 kv] = Q_p  K_j^T      A = Q_p    (MN-major), B = K_j (K-major)
+//   dP  [128 q  x  64 kv] = dO_p V_j^T      A = dO_p   (MN-major), B = V_j (K-major)
 //   P   = exp2(S * c - lse), masked (kv row >= vbs[j], or missing second q block) -> fp16 smem
 //   dS  = P * (dP - Delta)                                                          -> fp16 smem
-//   dV^T [128 hd x 64 kv] += dO_p^T P         A = dO_p (MN-major), B = P  (MN-major)
-//   dK^T [128 hd x 64 kv] += Q_p^T  dS        A = Q_p  (MN-major), B = dS (MN-major)
-//   dQ^T [128 hd x 128 q] =  K_j^T  dS^T      A = K_j  (MN-major), B = dS (K-major)
-// The same shared-memory tiles serve as K-major and MN-major operands (128-byte swizzle, 8-row
-// groups 1024 B apart), so no transposed copies of Q or dO are needed.  dQ^T leaves TMEM with
-// head-dim on the lanes, so each warp's fp32 reduction into the dQ accumulator covers 128
-// contiguous bytes of one query row.
+//   dV^T [128 hd x 64 kv] += dO_p^T P         A = dO_p^T (K-major),  B = P  (MN-major)
+//   dK^T [128 hd x 64 kv] += Q_p^T  dS        A = Q_p^T  (K-major),  B = dS (MN-major)
+//   dQ^T [128 hd x 128 q] =  K_j^T  dS^T      A = K_j    (MN-major), B = dS (K-major)
+// Q and dO come from the preprocess tile-transposed (each 64-token tile as [128 head dims][64
+// rows], one 16 KB copy), K and V row-major; each shared-memory tile (128-byte swizzle, 8-row
+// groups 1024 B apart) serves as a K-major operand of one GEMM and an MN-major operand of
+// another.  dQ^T leaves TMEM with head-dim on the lanes, so each warp's fp32 reduction into the
+// dQ accumulator covers 128 contiguous bytes of one query row.
 //
 // Work items are claimed dynamically (queue.cuh).  With 128-token blocks an item is one of the
 // two 64-token kv tiles of a block, and each k2q entry supplies a whole q tile pair.  The last
@@ -30,11 +31,13 @@
 //              soon as S is in TMEM (fp16, swizzled, into shared memory), then dS from dP.
 //   warps 8-11 dQ drain + epilogue: thread d owns head-dim row d; stages dQ^T of each q tile in
 //              an 8 KB per-warp box ([64 query rows x 32 head dims] fp32) and adds it into the
-//              fp32 accumulator with one TMA bulk tensor reduction; at the end of an item writes
-//              dK, dV (bf16, zeros for padded rows; whole zero blocks for unselected kv tiles).
+//              fp32 accumulator with one TMA bulk tensor reduction.  dK^T and dV^T are read out
+//              of TMEM as soon as the item's last dK^T is done (before its last dQ^T is
+//              drained) and written as bf16 dK, dV (zeros for padded rows; whole zero blocks
+//              for unselected kv tiles), or, for a part of a split item, as fp32 rows.
 //   warp 12    TMA producer and work claimer (K_j, V_j once per item, one copy each; Q and dO of
-//              each pair into a 2-stage ring: one 128-row copy each when the pair's q tiles are
-//              adjacent, else one 64-row column-half box per lane); also allocates TMEM.
+//              each pair into a 2-stage ring: one 16 KB copy per transposed q tile, one 32 KB
+//              copy when the pair's tiles are adjacent); also allocates TMEM.
 //   warp 13    UMMA issuer, warp-wide (all lanes poll, one elected lane issues).  Per step g the
 //              tensor pipe runs dV^T(g), S(g+1), dK^T(g), dP(g+1), dQ^T(g): dV^T waits for P,
 //              dK^T for dS, so the softmax of step g+1 overlaps dK^T, dP and dQ^T of step g, and
@@ -317,7 +320,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       bad = __reduce_or_sync(0xffffffffu, bad);
       if (bad && lane == 0) atomicOr(p.err, bad);
-      if (it.np == 0) continue;  // nothing to compute (an unselected block, or an empty half)
+      if (it.np == 0) continue;  // nothing to compute (an unselected block, or an empty part)
       if (!mbar_wait_warp(bar(KV_EMPTY), (itc & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) {
         ok = false;
         break;
@@ -466,7 +469,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if (w >= p.total) break;
       const Item it = decode_item(p, w);
-      if (it.np == 0) continue;  // nothing to compute (an unselected block, or an empty half)
+      if (it.np == 0) continue;  // nothing to compute (an unselected block, or an empty part)
       const int np = it.np;
       if (!mbar_wait_warp(bar(KV_FULL), itc & 1u, abort, WAIT_LIMIT_NS)) {
         ok = false;
@@ -557,7 +560,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if (w >= p.total) break;
       const Item it = decode_item(p, w);
-      if (it.np == 0) continue;  // nothing to compute (an unselected block, or an empty half)
+      if (it.np == 0) continue;  // nothing to compute (an unselected block, or an empty part)
       const int vb = clamp_vbs(p.vbs[it.j]);
       const uint32_t* am = p.absmax + it.bh * 4;
       const int eq = operand_exponent(am[0]), ek = operand_exponent(am[1]);
