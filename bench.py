@@ -57,21 +57,31 @@ def parse():
     return ap.parse_args()
 
 
+def kernel_code_hash(text):
+    """sha256 of a CUDA source with its comments removed and its whitespace collapsed: it changes
+    when the code does, not when only comments do."""
+    import hashlib
+    import re
+    t = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    t = re.sub(r"//[^\n]*", " ", t)
+    t = re.sub(r"\s+", " ", t).strip()
+    return hashlib.sha256(t.encode()).hexdigest()
+
+
 def main_kernel_traffic(config):
     """DRAM bytes per main-kernel launch from the committed ncu summary of this workload, or None
-    when there is none or the kernel source changed since it was captured."""
-    import hashlib
+    when there is none or the kernel's code changed since it was captured."""
     import re
     prof = os.path.join(ROOT, "profiles", "bwd_main_%s.md" % config.split("_")[0])
     src = os.path.join(ROOT, "block_sparse_video_tok_gb300", "csrc", "bwd_main.cu")
     if not os.path.exists(prof):
         return None
     text = open(prof).read()
-    m_sha = re.search(r"sha256 at capture: `([0-9a-f]{64})`", text)
+    m_code = re.search(r"code sha256 at capture: `([0-9a-f]{64})`", text)
     m_tr = re.search(r"traffic_bytes_per_launch \| (\d+)", text)
-    if not (m_sha and m_tr):
+    if not (m_code and m_tr):
         return None
-    if hashlib.sha256(open(src, "rb").read()).hexdigest() != m_sha.group(1):
+    if kernel_code_hash(open(src).read()) != m_code.group(1):
         return None
     return int(m_tr.group(1))
 

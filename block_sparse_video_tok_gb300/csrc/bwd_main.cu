@@ -1,11 +1,11 @@
 // bwd_main.cu -- the main kernel of the block-sparse attention backward on sm_103a.
 //
-// Work unit: one (b, h, kv block j) item, as in FastVideo's sm_100a backward (commit message:
-// "one warp-specialized tcgen05 kernel per (batch, head, kv64 block) computing dK, dV and the dQ
-// partials").  The item's k2q list of q blocks is walked two q blocks at a time, so every UMMA
-// has M = 128 (the q pair, or the 128 head-dim rows) and the fp32 accumulator maps row m to TMEM
-// lane m.  Per q pair (p = the pair's 128 query rows, all operands fp16 with per-head power-of-
-// two scales, fp32 accumulation):
+// Work unit: one (b, h, kv block j) item, as in FastVideo's sm_100a backward (its commit message:
+// one warp-specialized tcgen05 kernel whose work item is a (batch, head, 64-token kv block) and
+// which produces dK, dV and the dQ partials).  The item's k2q list of q blocks is walked two q
+// blocks at a time, so every UMMA has M = 128 (the q pair, or the 128 head-dim rows) and the
+// fp32 accumulator maps row m to TMEM lane m.  Per q pair (p = the pair's 128 query rows, all
+// operands fp16 with per-head power-of-two scales, fp32 accumulation):
 //   S   [128 q  x  64 kv] = Q_p  K_j^T      A = Q_p    (MN-major), B = K_j (K-major)
 //   dP  [128 q  x  64 kv] = dO_p V_j^T      A = dO_p   (MN-major), B = V_j (K-major)
 //   P   = exp2(S * c - lse), masked (kv row >= vbs[j], or missing second q block) -> fp16 smem

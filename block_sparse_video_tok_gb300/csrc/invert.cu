@@ -1,6 +1,6 @@
 // invert.cu -- q2k -> k2q inversion of the block selection (FastVideo block_sparse_attn_bwd_sm100a.py,
-// block_sparse_attn_backward_sm100a: "k2q_idx, k2q_num = invert_indices(...)"; the row order is
-// ascending as in the compare page's tests, invert_indices_torch).
+// block_sparse_attn_backward_sm100a, which inverts the selection before the backward kernels; the
+// row order is ascending as in the compare page's tests, invert_indices_torch).
 //
 // One CTA per (head, slice of kv-block columns).  Phase 1 scans the head's q2k rows and sets
 // bit i of column j in a shared-memory bitmap (column-major: one run of nq bits per kv block), so

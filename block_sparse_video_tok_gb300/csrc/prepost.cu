@@ -1,15 +1,18 @@
 // prepost.cu -- the memory-bound kernels around the tensor-core kernels:
-//   absmax_delta  per-head max|X| of the operands; Delta = rowsum(bf16(O) * dO) (FastVideo compare
-//                 main...vsa_bwd_fix, block_sparse_bwd_launch_sm100a.cuh, BlockSparseVsaBwdArgs:
-//                 "fp32 rowsum(bf16(o) * dout), written by the preprocess"); zeroing of the fp32
-//                 dQ accumulator ("preprocess zeroes, main reduce-adds, postprocess reads").
+//   absmax_delta  per-head max|X| of the operands; Delta = rowsum(bf16(O) * dO) in fp32, from
+//                 the O the backward receives (FastVideo compare main...vsa_bwd_fix,
+//                 block_sparse_bwd_launch_sm100a.cuh, BlockSparseVsaBwdArgs: the preprocess
+//                 writes Delta); zeroing of the fp32 dQ accumulator, which the main kernel
+//                 reduces into and the postprocess reads (same struct); the valid size of every
+//                 64-token kv tile.
 //   convert       scaled fp16 copies of the bf16 operands for the tensor cores.
 //   convert_t     the same for Q and dO of the backward, each 64-row tile stored transposed
 //                 ([128 head dims][64 rows]), so one 16 KB copy brings a whole tile.
 //   order         work order: (b, h) segments, items sorted by descending k2q list length,
-//                 stable (the commit message's "a device kernel sorts by list length from 1024 kv
-//                 blocks per sequence on").
-//   postprocess   dQ = bf16(dqacc * sm_scale * 2^scale) ("postprocess (dQ ... + sm_scale)").
+//                 stable (the commit message: sorted on the device, from 1024 kv blocks per
+//                 sequence on).
+//   postprocess   dQ = bf16(dqacc * sm_scale * 2^scale) (the commit message's postprocess step
+//                 applies sm_scale to dQ); the dV, dK rows of the main kernel's split items.
 //   fwd_bitmap    per-q-block selection bitmaps for the forward.
 // All are HBM-bound; each thread moves 16-byte vectors, grids cover the data once.
 #include "vsa_internal.cuh"

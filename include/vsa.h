@@ -24,8 +24,8 @@
  * Conventions shared by every entry point:
  *   - Layout: activations are contiguous [B, H, S, 128] bf16 (B batch, H heads, S tokens,
  *     head_dim 128), S = block * nb with nb the number of sparse blocks of `block` tokens (64 or
- *     128, vsa_shape.block; [FV-diff] BlockSparseVsaBwdArgs with VSA_BHSD; the torch binding's
- *     "FastVideo pads the sequence up to whole blocks"; [FV-fwd]).  Any nb >= 1 is accepted (no
+ *     128, vsa_shape.block; [FV-diff] BlockSparseVsaBwdArgs with VSA_BHSD; the torch binding
+ *     expects sequences already padded to whole blocks; [FV-fwd]).  Any nb >= 1 is accepted (no
  *     even-nb rule).  Block ids, q2k/k2q rows and variable_block_sizes all count blocks of
  *     `block` tokens.
  *   - Pointers: every buffer is device memory owned and allocated by the caller; activation
@@ -36,8 +36,8 @@
  *     before the GPU finishes.
  *   - Errors: problems visible on the host (null pointer, bad size, misalignment, too small a
  *     workspace, non-finite sm_scale, wrong device) return a status before anything is
- *     enqueued ("report an unsupported regime loudly rather than returning plausible-looking
- *     wrong values", [FV-diff] block_sparse_bwd_sm100a.cu).  Problems only visible on the
+ *     enqueued (an unsupported configuration is an error, never a silently wrong result:
+ *     [FV-diff] block_sparse_bwd_sm100a.cu).  Problems only visible on the
  *     device never trap: an out-of-range block id is skipped, a count is clamped to its row
  *     width, a block size is clamped to [0, block] ([cuDNN] Summary: a slot participates only
  *     inside the bounded active prefix with its index in [0, nb)), and a bit is set in the
@@ -87,8 +87,8 @@ int vsa_last_cuda_error(void);
 
 /*
  * vsa_invert_indices -- k2q from q2k.
- * Defined by [FV-bwd] block_sparse_attn_backward_sm100a ("k2q_idx, k2q_num =
- * invert_indices(idx, num, num_kv_blocks)") and [FV-diff] invert_indices_torch: for every
+ * Defined by [FV-bwd] block_sparse_attn_backward_sm100a (the backward first inverts the
+ * selection into per-kv-block lists) and [FV-diff] invert_indices_torch: for every
  * (b, h, kv block j), the q blocks i whose active q2k slots contain j, each once, in ASCENDING
  * order of i, and their count.
  *   q2k_idx  [B, H, nb, topk] int32: kv block ids selected by each q block (read: the first
