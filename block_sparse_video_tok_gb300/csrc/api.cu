@@ -11,6 +11,16 @@
 
 namespace vsa {
 
+namespace {
+std::atomic<uint64_t> g_wait_limit_ns{DEFAULT_WAIT_LIMIT_NS};
+}  // namespace
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
+uint64_t set_wait_limit_ns(uint64_t ns) {
+  return g_wait_limit_ns.exchange(ns == 0 ? DEFAULT_WAIT_LIMIT_NS : ns);
+}
+
 int device_sm_count() {
   static int cached[64] = {0};
   int dev = 0;
@@ -101,6 +111,8 @@ const char* vsa_status_string(vsa_status status) {
 
 int vsa_last_cuda_error(void) { return g_last_cuda_error; }
 
+uint64_t vsa_set_wait_limit_ns(uint64_t limit_ns) { return vsa::set_wait_limit_ns(limit_ns); }
+
 vsa_status vsa_invert_indices(const int32_t* q2k_idx, const int32_t* q2k_num, int32_t topk,
                               vsa_shape shape, int32_t* k2q_idx, int32_t* k2q_num,
                               uint32_t* dev_err, void* stream) {
@@ -167,12 +179,15 @@ vsa_status vsa_fwd(const void* q, const void* k, const void* v, const int32_t* q
   x.tiles = blk / vsa::BLOCK;
   x.vbs64 = vbs64;
   x.err = err;
+  x.tstat = nullptr;
   if ((e = vsa::launch_absmax_delta(nullptr, nullptr, vb, nullptr, nullptr, BH, S, absmax, nullptr,
                                     nullptr, x, s)) != cudaSuccess)
     return cuda_fail(e);
+  // V of the forward is scaled per head: P.V accumulates over the kv tiles in one accumulator.
   const __nv_bfloat16* src[3] = {nullptr, nullptr, vb};
   __half* dst[3] = {nullptr, nullptr, v16};
-  if ((e = vsa::launch_convert(src, dst, 3, BH, S, absmax, s)) != cudaSuccess) return cuda_fail(e);
+  if ((e = vsa::launch_convert(src, dst, 3, BH, S, absmax, nullptr, s)) != cudaSuccess)
+    return cuda_fail(e);
   if ((e = vsa::launch_fwd_bitmap(q2k_idx, q2k_num, topk, BH, nb, blk / vsa::BLOCK, bitmap, err,
                                   s)) != cudaSuccess)
     return cuda_fail(e);
@@ -192,6 +207,7 @@ vsa_status vsa_fwd(const void* q, const void* k, const void* v, const int32_t* q
   a.S = S;
   a.nb = S / vsa::BLOCK;
   a.sm_scale = sm_scale;
+  a.wait_ns = vsa::wait_limit_ns();
   if ((e = vsa::launch_fwd_main(a, s)) != cudaSuccess) return cuda_fail(e);
   return VSA_OK;
 }
@@ -229,6 +245,7 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
   const int BH = shape.batch * shape.heads, S = shape.seqlen;
   uint32_t* err = ws_at<uint32_t>(workspace, L.err);
   uint32_t* absmax = ws_at<uint32_t>(workspace, L.absmax);
+  uint32_t* tstat = ws_at<uint32_t>(workspace, L.tstat);
   float* delta = ws_at<float>(workspace, L.delta);
   int32_t* order = ws_at<int32_t>(workspace, L.order);
   int32_t* vbs64 = ws_at<int32_t>(workspace, L.vbs64);
@@ -245,7 +262,7 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
 
   cudaError_t e = record(events ? events->start : nullptr, s);
   if (e != cudaSuccess) return cuda_fail(e);
-  // Header, work counter, maxima and the split items' rows.
+  // Header, work counter, head and tile statistics and the split items' rows.
   if ((e = cudaMemsetAsync(workspace, 0, L.split_acc, s)) != cudaSuccess) return cuda_fail(e);
   vsa::PreExtras x{};
   x.vbs = vbs;
@@ -253,14 +270,17 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
   x.tiles = blk / vsa::BLOCK;
   x.vbs64 = vbs64;
   x.err = err;
+  x.tstat = tstat;
   if ((e = vsa::launch_absmax_delta(qb, kb, vb, dob, ob, BH, S, absmax, delta, dqacc, x, s)) !=
       cudaSuccess)
     return cuda_fail(e);
-  // K and V row-major; Q and dO tile-transposed (one 16 KB copy per 64-row tile in the main
-  // kernel, whatever the distance between the two q tiles of a step).
+  // K and V row-major, scaled per 64-token tile; Q and dO tile-transposed, scaled per head (one
+  // 16 KB copy per 64-row tile in the main kernel, whatever the distance between the two q tiles
+  // of a step).
   const __nv_bfloat16* src[4] = {nullptr, kb, vb, nullptr};
   __half* dst[4] = {nullptr, k16, v16, nullptr};
-  if ((e = vsa::launch_convert(src, dst, 4, BH, S, absmax, s)) != cudaSuccess) return cuda_fail(e);
+  if ((e = vsa::launch_convert(src, dst, 4, BH, S, absmax, tstat, s)) != cudaSuccess)
+    return cuda_fail(e);
   if ((e = vsa::launch_convert_t(qb, dob, q16, do16, BH, S, absmax, s)) != cudaSuccess)
     return cuda_fail(e);
   const int32_t* work_order = nullptr;
@@ -281,6 +301,7 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
   a.lse = lse;
   a.delta = delta;
   a.absmax = absmax;
+  a.tstat = tstat;
   a.dqacc = dqacc;
   a.dk = static_cast<__nv_bfloat16*>(dk);
   a.dv = static_cast<__nv_bfloat16*>(dv);
@@ -296,6 +317,7 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
   a.tiles = blk / vsa::BLOCK;
   a.max_q = max_q_blocks;
   a.sm_scale = sm_scale;
+  a.wait_ns = vsa::wait_limit_ns();
   if ((e = record(events ? events->before_main : nullptr, s)) != cudaSuccess) return cuda_fail(e);
   if ((e = vsa::launch_bwd_main(a, s)) != cudaSuccess) return cuda_fail(e);
   if ((e = record(events ? events->after_main : nullptr, s)) != cudaSuccess) return cuda_fail(e);
@@ -305,6 +327,19 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
     return cuda_fail(e);
   if ((e = record(events ? events->end : nullptr, s)) != cudaSuccess) return cuda_fail(e);
   return VSA_OK;
+}
+
+vsa_status vsa_work_order(const int32_t* k2q_num, int32_t max_q_blocks, vsa_shape shape,
+                          int32_t* order, void* stream) {
+  int nb = 0;
+  vsa_status st = check_shape(shape, &nb);
+  if (st != VSA_OK) return st;
+  if (!k2q_num || !order || max_q_blocks < 1) return VSA_ERR_INVALID_ARG;
+  if (!aligned(k2q_num, 4) || !aligned(order, 4)) return VSA_ERR_INVALID_ARG;
+  if ((st = check_device()) != VSA_OK) return st;
+  const cudaError_t e = vsa::launch_order(k2q_num, shape.batch * shape.heads, nb, max_q_blocks,
+                                          order, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? VSA_OK : cuda_fail(e);
 }
 
 vsa_status vsa_read_device_error(const void* workspace, uint32_t* bits, void* stream) {

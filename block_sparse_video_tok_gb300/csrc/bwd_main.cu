@@ -8,7 +8,8 @@
 // operands fp16 with per-head power-of-two scales, fp32 accumulation):
 //   S   [128 q  x  64 kv] = Q_p  K_j^T      A = Q_p    (MN-major), B = K_j (K-major)
 //   dP  [128 q  x  64 kv] = dO_p V_j^T      A = dO_p   (MN-major), B = V_j (K-major)
-//   P   = exp2(S * c - lse), masked (kv row >= vbs[j], or missing second q block) -> fp16 smem
+//   P   = exp2(S * c - lse), masked (kv row >= vbs[j], missing second q block, or a k2q id
+//         outside [0, nb), which is skipped)                                       -> fp16 smem
 //   dS  = P * (dP - Delta)                                                          -> fp16 smem
 //   dV^T [128 hd x 64 kv] += dO_p^T P         A = dO_p^T (K-major),  B = P  (MN-major)
 //   dK^T [128 hd x 64 kv] += Q_p^T  dS        A = Q_p^T  (K-major),  B = dS (MN-major)
@@ -118,7 +119,8 @@ struct Params {
   const int32_t* vbs;
   const float* lse;
   const float* delta;
-  const uint32_t* absmax;
+  const uint32_t* absmax;  // per-head statistics (HeadStat)
+  const uint32_t* tstat;   // per-kv-tile statistics (TileStat), [B * H * nb]
   float* dqacc;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -139,6 +141,7 @@ struct Params {
   int32_t* split_row;
   int total;  // claim positions: split0 + SPLIT_PARTS * nsplit
   float sm_scale;
+  uint64_t wait_ns;  // limit of each pipeline wait
 };
 
 // A work item: kv tile j of head bh.  Its k2q row `sel` lists selecting q blocks; each step
@@ -181,34 +184,71 @@ __device__ __forceinline__ Item decode_item(const Params& p, int u) {
   return it;
 }
 
+// Entry x of the item's k2q list, or -1 for an id outside [0, nq): such a slot is skipped (its
+// rows are masked and its dQ partial is not written), as an invalid q2k slot is.
 __device__ __forceinline__ int q_block(const Item& it, int x, int nq) {
   const int i = it.list[x];
-  return (i < 0 || i >= nq) ? 0 : i;
+  return (i < 0 || i >= nq) ? -1 : i;
 }
 
-// The two 64-token q tiles of the claim's step pp; false if the second one only repeats the
-// first (odd tail of a 64-token list).
-__device__ __forceinline__ bool step_tiles(const Params& p, const Item& it, int pp, int* i0,
-                                           int* i1) {
+// The two 64-token q tiles of a step.  i0, i1 are always tiles of the head (loaded); v0, v1 say
+// whether the rows of each take part: not for the repeat of the first tile at the odd tail of a
+// 64-token list, nor for a skipped slot (its tile is loaded as tile 0 or as a repeat).
+struct StepTiles {
+  int i0, i1;
+  bool v0, v1;
+};
+
+__device__ __forceinline__ StepTiles step_tiles(const Params& p, const Item& it, int pp) {
   const int ps = it.first + pp;
-  if (p.tiles == 2) {
-    *i0 = 2 * q_block(it, ps, p.nsel);
-    *i1 = *i0 + 1;
-    return true;
+  StepTiles t;
+  if (p.tiles == 2) {  // one 128-token entry: both tiles of its block, or neither
+    const int i = q_block(it, ps, p.nsel);
+    t.v0 = t.v1 = i >= 0;
+    t.i0 = i >= 0 ? 2 * i : 0;
+    t.i1 = t.i0 + 1;
+    return t;
   }
-  *i0 = q_block(it, 2 * ps, p.nsel);
-  const bool has2 = 2 * ps + 1 < it.n;
-  *i1 = has2 ? q_block(it, 2 * ps + 1, p.nsel) : *i0;
-  return has2;
+  const int a = q_block(it, 2 * ps, p.nsel);
+  const int b = 2 * ps + 1 < it.n ? q_block(it, 2 * ps + 1, p.nsel) : -1;
+  t.v0 = a >= 0;
+  t.v1 = b >= 0;
+  t.i0 = a >= 0 ? a : 0;
+  t.i1 = b >= 0 ? b : t.i0;
+  return t;
 }
 
 __device__ __forceinline__ int clamp_vbs(int v) { return v < 0 ? 0 : (v > BLOCK ? BLOCK : v); }
 
+// Scale exponents of an item: Q' = 2^-eq Q and dO' = 2^-eo dO (per head), K' = 2^-ek K and
+// V' = 2^-ev V (per kv tile), dS' = 2^kap P (dP' - Delta') (per kv tile, ds_exponent).  Then
+//   S'   = Q' K'^T   = 2^-(eq+ek) S            dP' = dO' V'^T = 2^-(eo+ev) dP
+//   dV^T accumulates dO'^T (2^KP P)  = 2^(KP-eo) dV^T
+//   dK^T accumulates Q'^T dS'        = 2^(kap-eq-eo-ev) dK^T / sm_scale
+//   dQ^T partial     K'^T dS'^T      = 2^(kap-ek-eo-ev) dQ^T / sm_scale
+// and the drain brings every dQ partial to 2^-eo dQ / sm_scale before adding it.
+struct ItemScales {
+  int eq, eo, ek, ev, kap;
+};
+
+__device__ __forceinline__ ItemScales item_scales(const Params& p, const Item& it) {
+  const uint32_t* hs = p.absmax + it.bh * HEAD_STATS;
+  const uint32_t* ts = p.tstat + (static_cast<size_t>(it.bh) * p.nb + it.j) * TILE_STATS;
+  ItemScales e;
+  e.eq = operand_exponent(hs[HS_Q]);
+  e.eo = operand_exponent(hs[HS_DO]);
+  e.ek = operand_exponent(ts[TS_K]);
+  e.ev = operand_exponent(ts[TS_V]);
+  e.kap = ds_exponent(bits_float(hs[HS_DO_NORM]), bits_float(ts[TS_V_NORM]),
+                      bits_float(hs[HS_DELTA]), e.eo, e.ev);
+  return e;
+}
+
 // One elected lane waits; the result is broadcast so the warp stays converged.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          int lane) {
+                                          uint64_t limit_ns, int lane) {
   int ok = 1;
-  if (lane == 0) ok = mbar_wait_bounded(bar, parity, abort, WAIT_LIMIT_NS) ? 1 : 0;
+  if (lane == 0) ok = mbar_wait_bounded(bar, parity, abort, limit_ns) ? 1 : 0;
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
@@ -303,8 +343,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (uint32_t k = 0;; ++k) {
       int w = 0, okp = 1;
       if (lane == 0)
-        okp = publish_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, p.sched, abort, &w) ? 1
-                                                                                             : 0;
+        okp = publish_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, p.sched, abort, p.wait_ns,
+                           &w)
+                  ? 1
+                  : 0;
       w = __shfl_sync(0xffffffffu, w, 0);
       if (!__shfl_sync(0xffffffffu, okp, 0)) {
         ok = false;
@@ -321,7 +363,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bad = __reduce_or_sync(0xffffffffu, bad);
       if (bad && lane == 0) atomicOr(p.err, bad);
       if (it.np == 0) continue;  // nothing to compute (an unselected block, or an empty part)
-      if (!mbar_wait_warp(bar(KV_EMPTY), (itc & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) {
+      if (!mbar_wait_warp(bar(KV_EMPTY), (itc & 1u) ^ 1u, abort, p.wait_ns)) {
         ok = false;
         break;
       }
@@ -335,12 +377,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int np = it.np;
       for (int pp = 0; pp < np; ++pp, ++g) {
         const uint32_t s = g & 1u;
-        if (!mbar_wait_warp(bar(QDO_EMPTY0 + s), ((g >> 1) & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) {
+        if (!mbar_wait_warp(bar(QDO_EMPTY0 + s), ((g >> 1) & 1u) ^ 1u, abort, p.wait_ns)) {
           ok = false;
           break;
         }
-        int i0, i1;
-        step_tiles(p, it, pp, &i0, &i1);
+        const StepTiles st = step_tiles(p, it, pp);
+        const int i0 = st.i0, i1 = st.i1;
         if (lane == 0) mbar_arrive_expect_tx(bar(QDO_FULL0 + s), 65536);
         __syncwarp();
         // Q and dO are stored tile-transposed: 64-token tile i of the head is 128 rows (head
@@ -421,7 +463,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // dQ^T = K_j^T dS^T of step gs into TMEM buffer gs & 1; then the dS buffer is free.
     auto issue_dq = [&](uint32_t gs) -> bool {
       const uint32_t b = gs & 1u;
-      if (!mbar_wait_warp(bar(DQ_FREE0 + b), ((gs >> 1) & 1u) ^ 1u, abort, WAIT_LIMIT_NS))
+      if (!mbar_wait_warp(bar(DQ_FREE0 + b), ((gs >> 1) & 1u) ^ 1u, abort, p.wait_ns))
         return false;
       tc_fence_after_sync();
       const uint64_t dsb = ds_kmaj;
@@ -463,7 +505,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     };
     for (uint32_t k = 0;; ++k) {
       int w;
-      if (!warp_take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, lane, &w)) {
+      if (!warp_take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, p.wait_ns, lane, &w)) {
         ok = false;
         break;
       }
@@ -471,7 +513,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const Item it = decode_item(p, w);
       if (it.np == 0) continue;  // nothing to compute (an unselected block, or an empty part)
       const int np = it.np;
-      if (!mbar_wait_warp(bar(KV_FULL), itc & 1u, abort, WAIT_LIMIT_NS)) {
+      if (!mbar_wait_warp(bar(KV_FULL), itc & 1u, abort, p.wait_ns)) {
         ok = false;
         break;
       }
@@ -479,7 +521,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // so the softmax of step g+1 (which needs S(g+1), then dP(g+1)) overlaps dK^T, dP and
       // dQ^T of step g.  S and dP of the item's first step go in up front.
       const uint32_t g0 = g;
-      if (!mbar_wait_warp(bar(QDO_FULL0 + (g0 & 1u)), (g0 >> 1) & 1u, abort, WAIT_LIMIT_NS)) {
+      if (!mbar_wait_warp(bar(QDO_FULL0 + (g0 & 1u)), (g0 >> 1) & 1u, abort, p.wait_ns)) {
         ok = false;
         break;
       }
@@ -490,12 +532,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int pp = 0; pp < np; ++pp, ++g) {
         const bool more = pp + 1 < np;
         // The softmax read S(g) before P_READY(g); P(g) is in shared memory.
-        if (!mbar_wait_warp(bar(P_READY), g & 1u, abort, WAIT_LIMIT_NS)) {
+        if (!mbar_wait_warp(bar(P_READY), g & 1u, abort, p.wait_ns)) {
           ok = false;
           break;
         }
         if (pp == 0 &&
-            !mbar_wait_warp(bar(ACC_EMPTY), (itc & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) {
+            !mbar_wait_warp(bar(ACC_EMPTY), (itc & 1u) ^ 1u, abort, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -505,7 +547,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // S(g+1) overwrites S(g), already read.  P(g+1) is written by the softmax only once
           // S(g+1) is done, which in the tensor pipe follows dV^T(g).
           if (!mbar_wait_warp(bar(QDO_FULL0 + ((g + 1) & 1u)), ((g + 1) >> 1) & 1u, abort,
-                              WAIT_LIMIT_NS)) {
+                              p.wait_ns)) {
             ok = false;
             break;
           }
@@ -513,7 +555,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           issue_s(g + 1);
         }
         // The softmax read dP(g) before DS_READY(g); dS(g) is in shared memory.
-        if (!mbar_wait_warp(bar(DS_READY), g & 1u, abort, WAIT_LIMIT_NS)) {
+        if (!mbar_wait_warp(bar(DS_READY), g & 1u, abort, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -554,7 +596,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t sw = static_cast<uint32_t>(r & 7);
     for (uint32_t k = 0;; ++k) {
       int w;
-      if (!warp_take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, lane, &w)) {
+      if (!warp_take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, p.wait_ns, lane, &w)) {
         if (lane == 0) raise_abort(abort, p.err);
         break;
       }
@@ -562,24 +604,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const Item it = decode_item(p, w);
       if (it.np == 0) continue;  // nothing to compute (an unselected block, or an empty part)
       const int vb = clamp_vbs(p.vbs[it.j]);
-      const uint32_t* am = p.absmax + it.bh * 4;
-      const int eq = operand_exponent(am[0]), ek = operand_exponent(am[1]);
-      const int ev = operand_exponent(am[2]), eo = operand_exponent(am[3]);
-      const float c1 = p.sm_scale * LOG2E_F * exp2i(eq + ek);
-      const float dscale = exp2i(-(eo + ev));
+      const ItemScales es = item_scales(p, it);
+      const float c1 = p.sm_scale * LOG2E_F * exp2i(es.eq + es.ek);
+      // dS' = P 2^KP (dP' m - Delta' m) with m = 2^(kap - KP): Delta' in the units of dP'.
+      const float dsm = exp2i(es.kap - KP);
+      const float dscale = exp2i(-(es.eo + es.ev)) * dsm;
       const int np = it.np;
       bool ok = true;
       for (int pp = 0; pp < np; ++pp, ++g) {
-        int i0, i1;
-        const bool has2 = step_tiles(p, it, pp, &i0, &i1);
-        const bool valid = (r < 64) || has2;
-        const int qb = (r >= 64) ? i1 : i0;
+        const StepTiles st = step_tiles(p, it, pp);
+        const bool valid = (r < 64) ? st.v0 : st.v1;
+        const int qb = (r >= 64) ? st.i1 : st.i0;
         const size_t grow = static_cast<size_t>(it.bh) * S + static_cast<size_t>(qb) * BLOCK + (r & 63);
         const float nlse = static_cast<float>(KP) - p.lse[grow];
-        const float dl = p.delta[grow] * dscale;  // Delta in the units of dP' = dO'.V'
+        const float dl = p.delta[grow] * dscale;  // Delta' m
         const bool full = valid && (vb == BLOCK);
         // Phase 1: P from S, as soon as S is in TMEM (dP and dQ^T(g-1) are still running).
-        if (!warp_wait(bar(S_FULL), g & 1u, abort, lane)) {
+        if (!warp_wait(bar(S_FULL), g & 1u, abort, p.wait_ns, lane)) {
           ok = false;
           break;
         }
@@ -617,7 +658,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(P_READY));
         // Phase 2: dS = P (dP - Delta) while dV^T(g) runs.
-        if (!warp_wait(bar(DP_FULL), g & 1u, abort, lane)) {
+        if (!warp_wait(bar(DP_FULL), g & 1u, abort, p.wait_ns, lane)) {
           ok = false;
           break;
         }
@@ -626,13 +667,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint32_t dpv[32];
           tmem_ld_32x32b_x32(tmem + lane_off + TM_DP + h * 32u, dpv);
           tmem_wait_ld();
-          uint32_t dk[16];  // dS, fp16 pairs (masked columns have P = 0, so dS = 0 exactly)
+          uint32_t dk[16];  // dS', fp16 pairs (masked columns have P = 0, so dS' = 0 exactly)
 #pragma unroll
           for (int c = 0; c < 32; c += 2)
-            dk[c >> 1] = pack_half2(pv[c] * (__uint_as_float(dpv[c]) - dl),
-                                    pv[c + 1] * (__uint_as_float(dpv[c + 1]) - dl));
+            dk[c >> 1] = pack_half2(pv[c] * fmaf(__uint_as_float(dpv[c]), dsm, -dl),
+                                    pv[c + 1] * fmaf(__uint_as_float(dpv[c + 1]), dsm, -dl));
           // The buffer's previous contents (step g-1) must have been consumed by dQ^T(g-1).
-          if (!warp_wait(bar(DS_FREE), (g & 1u) ^ 1u, abort, lane)) {
+          if (!warp_wait(bar(DS_FREE), (g & 1u) ^ 1u, abort, p.wait_ns, lane)) {
             ok = false;
             break;
           }
@@ -664,7 +705,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t g = 0, itc = 0;
     for (uint32_t k = 0;; ++k) {
       int w;
-      if (!warp_take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, lane, &w)) {
+      if (!warp_take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, p.wait_ns, lane, &w)) {
         if (lane == 0) raise_abort(abort, p.err);
         break;
       }
@@ -682,11 +723,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         continue;
       }
-      const uint32_t* am = p.absmax + it.bh * 4;
-      const int eq = operand_exponent(am[0]);
-      const int ev = operand_exponent(am[2]), eo = operand_exponent(am[3]);
-      const float sv_scale = exp2i(eo - KP);
-      const float sk_scale = p.sm_scale * exp2i(eq + eo + ev - KP);
+      const ItemScales es = item_scales(p, it);
+      const float sv_scale = exp2i(es.eo - KP);
+      const float sk_scale =
+          p.sm_scale * exp2i(es.eq + es.eo) * exp2i(clamp_exponent(es.ev - es.kap, 126));
+      // dQ^T partial -> 2^-eo dQ^T / sm_scale, the accumulator's scale for every item.
+      const float dq_scale = exp2i(clamp_exponent(es.ek + es.ev - es.kap, 126));
       const int vb = clamp_vbs(p.vbs[it.j]);
       const int np = it.np;
       bool ok = true;
@@ -698,7 +740,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // The item's dV^T and dK^T, complete once its last dK^T is (before its last dQ^T): read
       // out before the last step's dQ^T is drained, so that the next item's dV^T can start.
       auto read_acc = [&]() -> bool {
-        if (!warp_wait(bar(ACC_FULL), itc & 1u, abort, lane)) return false;
+        if (!warp_wait(bar(ACC_FULL), itc & 1u, abort, p.wait_ns, lane)) return false;
         tc_fence_after_sync();
         // dV^T and dK^T rows (head dim d, kv rows 0..63) in 32-column chunks; masked kv rows get
         // an explicit +0.0.  A split part stores its scaled fp32 rows in its own slot instead.
@@ -736,10 +778,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ok = false;
           break;
         }
-        int i0, i1;
-        const bool has2 = step_tiles(p, it, pp, &i0, &i1);
+        const StepTiles st = step_tiles(p, it, pp);
         const uint32_t buf = g & 1u;
-        if (!warp_wait(bar(DQ_FULL0 + buf), (g >> 1) & 1u, abort, lane)) {
+        if (!warp_wait(bar(DQ_FULL0 + buf), (g >> 1) & 1u, abort, p.wait_ns, lane)) {
           ok = false;
           break;
         }
@@ -751,8 +792,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // one TMA reduce adds into the accumulator: a thread's bulk requests are processed one
         // after another, so few large requests move more than many small ones.  The load of
         // chunk c+1 is in flight while chunk c is staged.
+        // A tile whose rows do not take part (odd tail, skipped slot) has no partial to add.
         auto stage = [&](const uint32_t* v, int c) {
-          if (c >= 2 && !has2) return;
+          if (!(c < 2 ? st.v0 : st.v1)) return;
           const uint32_t rows = stg + static_cast<uint32_t>(c & 1) * 4096u;
           if ((c & 1) == 0) {
             if (lane == 0) bulk_wait_read<0>();  // the previous reduce has read the box
@@ -760,15 +802,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
 #pragma unroll
           for (int q = 0; q < 32; ++q)
-            asm volatile("st.shared.b32 [%0], %1;" ::"r"(rows + static_cast<uint32_t>(q) * 128u +
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(rows + static_cast<uint32_t>(q) * 128u +
                                                           static_cast<uint32_t>(lane) * 4u),
-                         "r"(v[q])
+                         "f"(__uint_as_float(v[q]) * dq_scale)
                          : "memory");
           if (c & 1) {
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_reduce_add_2d(&tm_dq, stg, wq * 32, it.bh * S + ((c < 2) ? i0 : i1) * BLOCK);
+              tma_reduce_add_2d(&tm_dq, stg, wq * 32,
+                                it.bh * S + ((c < 2) ? st.i0 : st.i1) * BLOCK);
               bulk_commit_group();
             }
           }
@@ -838,13 +881,10 @@ cudaError_t launch_bwd_main(const BwdMainArgs& a, cudaStream_t stream) {
   if ((e = make_tmap_tiles_t(&tdo2, a.do16, rows, 2)) != cudaSuccess) return e;
   if ((e = make_tmap_rows128_f16_halves(&tk, a.k16, rows, 64)) != cudaSuccess) return e;
   if ((e = make_tmap_rows128_f16_halves(&tv, a.v16, rows, 64)) != cudaSuccess) return e;
-  static bool attr_set = false;
-  if (!attr_set) {
-    e = cudaFuncSetAttribute(bwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(SMEM_BYTES));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  if ((e = ensure_smem_limit(bwd_main_kernel, static_cast<int>(SMEM_BYTES), smem_set)) !=
+      cudaSuccess)
+    return e;
   Params p{};
   p.k2q_idx = a.k2q_idx;
   p.k2q_num = a.k2q_num;
@@ -853,6 +893,7 @@ cudaError_t launch_bwd_main(const BwdMainArgs& a, cudaStream_t stream) {
   p.lse = a.lse;
   p.delta = a.delta;
   p.absmax = a.absmax;
+  p.tstat = a.tstat;
   p.dqacc = a.dqacc;
   p.dk = a.dk;
   p.dv = a.dv;
@@ -864,6 +905,7 @@ cudaError_t launch_bwd_main(const BwdMainArgs& a, cudaStream_t stream) {
   p.tiles = a.tiles;
   p.max_q = a.max_q;
   p.sm_scale = a.sm_scale;
+  p.wait_ns = a.wait_ns;
   const int items = a.B * a.H * a.nb;
   const int sms = device_sm_count();
   const int grid = items < sms ? items : sms;

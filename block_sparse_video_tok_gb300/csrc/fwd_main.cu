@@ -106,6 +106,7 @@ struct Params {
   int32_t* sched;
   int S, nb, words, npairs, total;
   float sm_scale;
+  uint64_t wait_ns;  // limit of each pipeline wait
 };
 
 struct Pair {
@@ -152,9 +153,9 @@ __device__ __forceinline__ bool for_union(const Params& p, const Pair& q, F f) {
 __device__ __forceinline__ int clamp_vbs(int v) { return v < 0 ? 0 : (v > BLOCK ? BLOCK : v); }
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          int lane) {
+                                          uint64_t limit_ns, int lane) {
   int ok = 1;
-  if (lane == 0) ok = mbar_wait_bounded(bar, parity, abort, WAIT_LIMIT_NS) ? 1 : 0;
+  if (lane == 0) ok = mbar_wait_bounded(bar, parity, abort, limit_ns) ? 1 : 0;
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
@@ -298,8 +299,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (uint32_t k = 0;; ++k) {
       int w = 0, okp = 1;
       if (lane == 0)
-        okp = publish_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, p.sched, abort, &w) ? 1
-                                                                                             : 0;
+        okp = publish_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, p.sched, abort, p.wait_ns,
+                           &w)
+                  ? 1
+                  : 0;
       w = __shfl_sync(0xffffffffu, w, 0);
       if (!__shfl_sync(0xffffffffu, okp, 0)) {
         ok = false;
@@ -309,7 +312,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const Pair q = decode_pair(p, w);
       if (union_size(p, q) == 0) continue;
       const uint32_t qs = itc & 1u;
-      if (!mbar_wait_warp(bar(Q_EMPTY0 + qs), ((itc >> 1) & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) {
+      if (!mbar_wait_warp(bar(Q_EMPTY0 + qs), ((itc >> 1) & 1u) ^ 1u, abort, p.wait_ns)) {
         ok = false;
         break;
       }
@@ -330,7 +333,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       auto load_pair = [&](int j0, int j1) -> bool {
         const uint32_t st = lg % K_STAGES;
         if (!mbar_wait_warp(bar(S_FULL0 + st), ((lg / K_STAGES) & 1u) ^ 1u, abort,
-                            WAIT_LIMIT_NS))
+                            p.wait_ns))
           return false;
         if (lane == 0) mbar_arrive_expect_tx(bar(K_FULL0 + st), j1 >= 0 ? 32768u : 16384u);
         __syncwarp();
@@ -381,7 +384,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     for (uint32_t k = 0;; ++k) {
       int w;
-      if (!warp_take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, lane, &w)) {
+      if (!warp_take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, p.wait_ns, lane, &w)) {
         ok = false;
         break;
       }
@@ -390,7 +393,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ok = for_union(p, q, [&](int j) {
         const uint32_t st = lg % V_STAGES;
         if (!mbar_wait_warp(bar(V_EMPTY0 + st), ((lg / V_STAGES) & 1u) ^ 1u, abort,
-                            WAIT_LIMIT_NS))
+                            p.wait_ns))
           return false;
         if (lane == 0) mbar_arrive_expect_tx(bar(V_FULL0 + st), 16384u);
         __syncwarp();
@@ -427,7 +430,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto issue_s = [&](uint32_t pb, uint32_t qs) -> bool {
       const uint32_t b = pb & 1u;
       if (!mbar_wait2_warp(bar(K_FULL0 + b), (pb >> 1) & 1u, bar(BUF_FREE0 + b),
-                           ((pb >> 1) & 1u) ^ 1u, abort, WAIT_LIMIT_NS))
+                           ((pb >> 1) & 1u) ^ 1u, abort, p.wait_ns))
         return false;
       tc_fence_after_sync();
       const uint64_t qa = sdesc_advance(q_kmaj, qs * 32768u);
@@ -466,7 +469,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     };
     for (uint32_t k = 0;; ++k) {
       int w;
-      if (!warp_take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, lane, &w)) {
+      if (!warp_take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, p.wait_ns, lane, &w)) {
         ok = false;
         break;
       }
@@ -476,7 +479,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (nu == 0) continue;
       const int npr = (nu + 1) >> 1;
       const uint32_t qs = itc & 1u;
-      if (!mbar_wait_warp(bar(Q_FULL0 + qs), (itc >> 1) & 1u, abort, WAIT_LIMIT_NS)) {
+      if (!mbar_wait_warp(bar(Q_FULL0 + qs), (itc >> 1) & 1u, abort, p.wait_ns)) {
         ok = false;
         break;
       }
@@ -502,8 +505,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 bar(P_READY0 + (pb & 1u)), bar(P_READY0 + 2 + (pb & 1u))};
         const uint32_t wp[4] = {(vc / V_STAGES) & 1u, (v1 / V_STAGES) & 1u, (pb >> 1) & 1u,
                                 (pb >> 1) & 1u};
-        ok = (pr != 0 || mbar_wait_warp(bar(O_EMPTY), (itc & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) &&
-             mbar_waitn_warp(wb, wp, abort, WAIT_LIMIT_NS);
+        ok = (pr != 0 || mbar_wait_warp(bar(O_EMPTY), (itc & 1u) ^ 1u, abort, p.wait_ns)) &&
+             mbar_waitn_warp(wb, wp, abort, p.wait_ns);
         if (!ok) break;
         tc_fence_after_sync();
         issue_pv(pb, 0, pr == 0);
@@ -533,7 +536,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t pc = 0, itc = 0;  // kv-tile pairs; items
     for (uint32_t k = 0;; ++k) {
       int w;
-      if (!warp_take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, lane, &w)) {
+      if (!warp_take_item(bar(ITEM_FULL0), bar(ITEM_EMPTY0), queue, k, abort, p.wait_ns, lane, &w)) {
         if (lane == 0) raise_abort(abort, p.err);
         break;
       }
@@ -553,8 +556,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         continue;
       }
-      const uint32_t* am = p.absmax + q.bh * 4;
-      const int ev = operand_exponent(am[2]);
+      const int ev = operand_exponent(p.absmax[q.bh * HEAD_STATS + HS_V]);
       const float c1 = p.sm_scale * LOG2E_F;  // S -> s (log2 units); Q and K are unscaled bf16
       float m = -INFINITY, l = 0.f;  // this group's reference maximum and sum of P * 2^KPF
       bool first = true;             // no block of this group in the item yet
@@ -563,7 +565,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       auto do_pair = [&](int j) -> bool {
         const uint32_t pb = pc++;
         const uint32_t b = pb & 1u;
-        if (!warp_wait(bar(S_FULL0 + b), (pb >> 1) & 1u, abort, lane)) return false;
+        if (!warp_wait(bar(S_FULL0 + b), (pb >> 1) & 1u, abort, p.wait_ns, lane)) return false;
         tc_fence_after_sync();
         // S of this group's tile, then its P over the first 32 of those columns.
         const uint32_t t_s = tmem + lane_off + TM_S + b * 128u + grp * 64u;
@@ -573,7 +575,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // warp's P), so skipping the wait when nothing is rescaled is safe.
         auto wait_prev = [&]() -> bool {
           return pb == 0 ||
-                 warp_wait(bar(BUF_FREE0 + ((pb - 1) & 1u)), ((pb - 1) >> 1) & 1u, abort, lane);
+                 warp_wait(bar(BUF_FREE0 + ((pb - 1) & 1u)), ((pb - 1) >> 1) & 1u, abort,
+                           p.wait_ns, lane);
         };
         auto ready = [&]() {
           tc_fence_before_sync();
@@ -701,13 +704,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       slot[grp * 128 + r] = make_float2(m, l);
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(XCH0 + quarter));
-      if (!warp_wait(bar(XCH0 + quarter), itc & 1u, abort, lane)) {
+      if (!warp_wait(bar(XCH0 + quarter), itc & 1u, abort, p.wait_ns, lane)) {
         if (lane == 0) raise_abort(abort, p.err);
         break;
       }
       __syncwarp();
       const float2 mo = slot[(1 - grp) * 128 + r];
-      if (!warp_wait(bar(O_FULL), itc & 1u, abort, lane)) {
+      if (!warp_wait(bar(O_FULL), itc & 1u, abort, p.wait_ns, lane)) {
         if (lane == 0) raise_abort(abort, p.err);
         break;
       }
@@ -774,13 +777,10 @@ cudaError_t launch_fwd_main(const FwdMainArgs& a, cudaStream_t stream) {
   if ((e = make_tmap_rows128_f16_halves(&tv, a.v16, rows, 64)) != cudaSuccess) return e;
   if ((e = make_tmap_rows128_f16_halves(&tq2, a.q, rows, 128, true)) != cudaSuccess) return e;
   if ((e = make_tmap_rows128_f16_halves(&tk2, a.k, rows, 128, true)) != cudaSuccess) return e;
-  static bool attr_set = false;
-  if (!attr_set) {
-    e = cudaFuncSetAttribute(fwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(SMEM_BYTES));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  if ((e = ensure_smem_limit(fwd_main_kernel, static_cast<int>(SMEM_BYTES), smem_set)) !=
+      cudaSuccess)
+    return e;
   Params p{};
   p.bitmap = a.bitmap;
   p.vbs = a.vbs;
@@ -795,6 +795,7 @@ cudaError_t launch_fwd_main(const FwdMainArgs& a, cudaStream_t stream) {
   p.npairs = (a.nb + 1) / 2;
   p.total = a.B * a.H * p.npairs;
   p.sm_scale = a.sm_scale;
+  p.wait_ns = a.wait_ns;
   const int sms = device_sm_count();
   const int grid = p.total < sms ? p.total : sms;
   fwd_main_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tq, tq2, tk, tk2, tv, p);

@@ -61,3 +61,14 @@ extern "C" vsa_status vsa_bwd_no_alloc(const void* dout, const void* q, const vo
   return vsa_bwd(dout, q, k, v, o, lse, k2q_idx, k2q_num, max_q_blocks, vbs, sm_scale, shape, dq,
                  dk, dv, scratch, VSA_BWD_NO_ALLOC_MAX_WORKSPACE_BYTES, stream);
 }
+
+extern "C" vsa_status vsa_bwd_no_alloc_device_error(uint32_t* bits, void* stream) {
+  if (!bits) return VSA_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  vsa_status st = scratch_address(&scratch);
+  if (st != VSA_OK) return st;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return vsa::record_cuda_failure(e);
+  e = cudaMemcpy(bits, scratch, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  return e == cudaSuccess ? VSA_OK : vsa::record_cuda_failure(e);
+}

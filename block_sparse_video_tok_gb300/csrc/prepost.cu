@@ -1,5 +1,7 @@
 // prepost.cu -- the memory-bound kernels around the tensor-core kernels:
-//   absmax_delta  per-head max|X| of the operands; Delta = rowsum(bf16(O) * dO) in fp32, from
+//   absmax_delta  per-head max|X| of the operands (per 64-token kv tile for K and V of the
+//                 backward, with the row-norm bounds the dS scale needs); Delta =
+//                 rowsum(bf16(O) * dO) in fp32, from
 //                 the O the backward receives (FastVideo compare main...vsa_bwd_fix,
 //                 block_sparse_bwd_launch_sm100a.cuh, BlockSparseVsaBwdArgs: the preprocess
 //                 writes Delta); zeroing of the fp32 dQ accumulator, which the main kernel
@@ -41,6 +43,22 @@ __device__ __forceinline__ uint32_t warp_max(uint32_t v) {
   return v;
 }
 
+// Sum of squares of the 8 bf16 values of a 16-byte chunk.
+__device__ __forceinline__ float sumsq8(uint4 x) {
+  float s = bf16lo(x.x) * bf16lo(x.x) + bf16hi(x.x) * bf16hi(x.x);
+  s += bf16lo(x.y) * bf16lo(x.y) + bf16hi(x.y) * bf16hi(x.y);
+  s += bf16lo(x.z) * bf16lo(x.z) + bf16hi(x.z) * bf16hi(x.z);
+  s += bf16lo(x.w) * bf16lo(x.w) + bf16hi(x.w) * bf16hi(x.w);
+  return s;
+}
+
+// Sum over the 16 lanes that hold one 128-element row.
+__device__ __forceinline__ float row_sum16(float s) {
+#pragma unroll
+  for (int d = 8; d > 0; d >>= 1) s += __shfl_xor_sync(0xffffffffu, s, d);
+  return s;
+}
+
 // Grid (S / 64, BH), 256 threads: 16 lanes per 128-element row (8 bf16 = 16 B per lane), two
 // rows per warp per iteration, 64 rows per CTA.
 constexpr int PRE_THREADS = 256;
@@ -69,13 +87,20 @@ __global__ void __launch_bounds__(PRE_THREADS) absmax_delta_kernel(
   const int half = threadIdx.x >> 4;  // which of the 16 rows-in-flight
   const int sub = threadIdx.x & 15;   // 16-byte chunk of the row
   const bool bwd = (dout != nullptr);
-  uint32_t mq = 0, mk = 0, mv = 0, mdo = 0;
+  const bool stats = (x.tstat != nullptr);
+  // Maxima as float bits (non-negative floats order like their bits): |Q|, |K|, |V|, |dO|, then
+  // the squared row norms of dO and V and |Delta|.
+  uint32_t mq = 0, mk = 0, mv = 0, mdo = 0, ndo2 = 0, nv2 = 0, mdl = 0;
   for (int rr = half; rr < BLOCK; rr += PRE_THREADS / 16) {
     const size_t row = static_cast<size_t>(bh) * S + static_cast<size_t>(blockIdx.x) * BLOCK + rr;
     const size_t at = row * 16 + sub;
     if (q) mq = max(mq, absmax_bits8(q[at]));  // a null operand is not scanned (its max stays 0)
     if (k) mk = max(mk, absmax_bits8(k[at]));
-    if (v) mv = max(mv, absmax_bits8(v[at]));
+    if (v) {
+      const uint4 vv = v[at];
+      mv = max(mv, absmax_bits8(vv));
+      if (stats) nv2 = max(nv2, __float_as_uint(row_sum16(sumsq8(vv))));
+    }
     if (bwd) {
       const uint4 a = dout[at], b = o[at];
       mdo = max(mdo, absmax_bits8(a));
@@ -83,32 +108,57 @@ __global__ void __launch_bounds__(PRE_THREADS) absmax_delta_kernel(
       s += bf16lo(a.y) * bf16lo(b.y) + bf16hi(a.y) * bf16hi(b.y);
       s += bf16lo(a.z) * bf16lo(b.z) + bf16hi(a.z) * bf16hi(b.z);
       s += bf16lo(a.w) * bf16lo(b.w) + bf16hi(a.w) * bf16hi(b.w);
-#pragma unroll
-      for (int d = 8; d > 0; d >>= 1) s += __shfl_xor_sync(0xffffffffu, s, d);
+      s = row_sum16(s);
       if (sub == 0) delta[row] = s;
+      if (stats) {
+        mdl = max(mdl, __float_as_uint(fabsf(s)));
+        ndo2 = max(ndo2, __float_as_uint(row_sum16(sumsq8(a))));
+      }
       const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
       float4* dst = dqacc + row * 32 + sub * 2;
       dst[0] = z;
       dst[1] = z;
     }
   }
-  __shared__ uint32_t red[4][PRE_THREADS / 32];
+  constexpr int NRED = 7;
+  __shared__ uint32_t red[NRED][PRE_THREADS / 32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  mq = warp_max(mq);
-  mk = warp_max(mk);
-  mv = warp_max(mv);
-  mdo = warp_max(mdo);
-  if (lane == 0) {
-    red[0][warp] = mq;
-    red[1][warp] = mk;
-    red[2][warp] = mv;
-    red[3][warp] = mdo;
+  const uint32_t mine[NRED] = {mq, mk, mv, mdo, ndo2, nv2, mdl};
+#pragma unroll
+  for (int i = 0; i < NRED; ++i) {
+    const uint32_t m = warp_max(mine[i]);
+    if (lane == 0) red[i][warp] = m;
   }
   __syncthreads();
-  if (threadIdx.x < 4) {
+  if (threadIdx.x < NRED) {
     uint32_t m = 0;
     for (int w = 0; w < PRE_THREADS / 32; ++w) m = max(m, red[threadIdx.x][w]);
-    if (m) atomicMax(absmax + bh * 4 + threadIdx.x, m);
+    uint32_t* hs = absmax + bh * HEAD_STATS;
+    const int i = threadIdx.x;
+    if (i < 4) {
+      if (m) atomicMax(hs + i, m);  // HS_Q, HS_K, HS_V, HS_DO
+    } else if (stats) {
+      // Squared norms become norms here (sqrt is monotonic, so the maximum is kept).
+      const uint32_t val = (i == 6) ? m : __float_as_uint(sqrtf(__uint_as_float(m)));
+      uint32_t* ts = x.tstat + (static_cast<size_t>(bh) * gridDim.x + blockIdx.x) * TILE_STATS;
+      if (i == 4) {
+        if (val) atomicMax(hs + HS_DO_NORM, val);
+      } else if (i == 5) {
+        ts[TS_V_NORM] = val;  // one CTA per tile: a plain store
+      } else {
+        if (val) atomicMax(hs + HS_DELTA, val);
+      }
+    }
+  }
+  if (stats && threadIdx.x == 0) {
+    uint32_t* ts = x.tstat + (static_cast<size_t>(bh) * gridDim.x + blockIdx.x) * TILE_STATS;
+    uint32_t m_k = 0, m_v = 0;
+    for (int w = 0; w < PRE_THREADS / 32; ++w) {
+      m_k = max(m_k, red[1][w]);
+      m_v = max(m_v, red[2][w]);
+    }
+    ts[TS_K] = m_k;
+    ts[TS_V] = m_v;
   }
 }
 
@@ -116,6 +166,7 @@ __global__ void __launch_bounds__(PRE_THREADS) absmax_delta_kernel(
 struct ConvertPack {
   const uint4* src[4];
   uint4* dst[4];
+  const uint32_t* tstat;  // non-null: K (1) and V (2) take their exponent per 64-token tile
 };
 
 __global__ void __launch_bounds__(256) convert_kernel(ConvertPack pk, size_t chunks_per_head,
@@ -125,10 +176,15 @@ __global__ void __launch_bounds__(256) convert_kernel(ConvertPack pk, size_t chu
   const uint4* __restrict__ src = t == 0 ? pk.src[0] : t == 1 ? pk.src[1] : t == 2 ? pk.src[2] : pk.src[3];
   uint4* __restrict__ dst = t == 0 ? pk.dst[0] : t == 1 ? pk.dst[1] : t == 2 ? pk.dst[2] : pk.dst[3];
   if (src == nullptr) return;
+  const bool per_tile = pk.tstat != nullptr && (t == 1 || t == 2);
   for (size_t c = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; c < total_chunks;
        c += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const int bh = static_cast<int>(c / chunks_per_head);
-    const float s = exp2i(-operand_exponent(absmax[bh * 4 + t]));
+    // 16 chunks per row, 64 rows per tile: chunk c lies in tile c / 1024 (heads hold whole
+    // tiles).
+    const uint32_t bits = per_tile ? pk.tstat[(c >> 10) * TILE_STATS + (t == 1 ? TS_K : TS_V)]
+                                   : absmax[bh * HEAD_STATS + t];
+    const float s = exp2i(-operand_exponent(bits));
     const uint4 x = src[c];
     const uint32_t w[4] = {x.x, x.y, x.z, x.w};
     uint32_t out[4];
@@ -157,7 +213,8 @@ __global__ void __launch_bounds__(256) convert_t_kernel(ConvertTPack pk, int S,
   const int t = blockIdx.z, bh = blockIdx.y, tile = blockIdx.x, nt = gridDim.x;
   const uint4* __restrict__ src = t == 0 ? pk.src[0] : pk.src[1];
   __half* __restrict__ dst = t == 0 ? pk.dst[0] : pk.dst[1];
-  const float sc = exp2i(-operand_exponent(absmax[bh * 4 + (t == 0 ? pk.slot[0] : pk.slot[1])]));
+  const float sc =
+      exp2i(-operand_exponent(absmax[bh * HEAD_STATS + (t == 0 ? pk.slot[0] : pk.slot[1])]));
   const size_t row0 = static_cast<size_t>(bh) * S + static_cast<size_t>(tile) * BLOCK;
   // The tile's 1024 16-byte chunks, four per thread, all loads in flight before any is used.
   constexpr int PER = BLOCK * 16 / 256;
@@ -191,23 +248,27 @@ __global__ void __launch_bounds__(256) convert_t_kernel(ConvertTPack pk, int S,
 }
 
 // Grid (BH, ceil(nb / 256)): item x of head bh goes to position
-// #{y : c_y > c_x} + #{y < x : c_y == c_x}, i.e. a stable sort by descending count.
+// #{y : c_y > c_x} + #{y < x : c_y == c_x}, i.e. a stable sort by descending count, with the
+// counts clamped to [0, max_q].  kShared: the head's counts are staged in shared memory first
+// (nb * 4 bytes); otherwise (rows too long for shared memory) each thread reads them from global
+// memory.
+template <bool kShared>
 __global__ void __launch_bounds__(256) order_kernel(const int32_t* __restrict__ k2q_num, int nb,
                                                     int max_q, int32_t* __restrict__ order) {
   extern __shared__ int32_t cnt[];
   const int bh = blockIdx.x;
   const int32_t* num = k2q_num + static_cast<size_t>(bh) * nb;
-  for (int y = threadIdx.x; y < nb; y += blockDim.x) {
-    const int c = num[y];
-    cnt[y] = c < 0 ? 0 : (c > max_q ? max_q : c);
+  auto clamped = [max_q](int c) { return c < 0 ? 0 : (c > max_q ? max_q : c); };
+  if (kShared) {
+    for (int y = threadIdx.x; y < nb; y += blockDim.x) cnt[y] = clamped(num[y]);
+    __syncthreads();
   }
-  __syncthreads();
   const int x = blockIdx.y * blockDim.x + threadIdx.x;
   if (x >= nb) return;
-  const int cx = cnt[x];
+  const int cx = kShared ? cnt[x] : clamped(num[x]);
   int pos = 0;
   for (int y = 0; y < nb; ++y) {
-    const int cy = cnt[y];
+    const int cy = kShared ? cnt[y] : clamped(__ldg(num + y));
     pos += (cy > cx) || (cy == cx && y < x);
   }
   order[static_cast<size_t>(bh) * nb + pos] = bh * nb + x;
@@ -221,9 +282,9 @@ __global__ void __launch_bounds__(256) postprocess_kernel(
   for (size_t c = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; c < total_chunks;
        c += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const int bh = static_cast<int>(c / chunks_per_head);
-    const uint32_t* am = absmax + bh * 4;
-    const int e = operand_exponent(am[1]) + operand_exponent(am[2]) + operand_exponent(am[3]) - KP;
-    const float s = sm_scale * exp2i(e);
+    // The main kernel leaves dQ / (sm_scale 2^e) in the accumulator, e the exponent of the
+    // head's max |dO| (every other scale is undone per item before the reduction).
+    const float s = sm_scale * exp2i(operand_exponent(absmax[bh * HEAD_STATS + HS_DO]));
     const float4 a = dqacc[2 * c], b = dqacc[2 * c + 1];
     const __nv_bfloat162 r0 = __floats2bfloat162_rn(a.x * s, a.y * s);
     const __nv_bfloat162 r1 = __floats2bfloat162_rn(a.z * s, a.w * s);
@@ -321,8 +382,10 @@ cudaError_t launch_absmax_delta(const __nv_bfloat16* q, const __nv_bfloat16* k,
 }
 
 cudaError_t launch_convert(const __nv_bfloat16* const* src, __half* const* dst, int count, int BH,
-                           int S, const uint32_t* absmax, cudaStream_t stream) {
+                           int S, const uint32_t* absmax, const uint32_t* tstat,
+                           cudaStream_t stream) {
   ConvertPack pk{};
+  pk.tstat = tstat;
   for (int t = 0; t < 4; ++t) {
     pk.src[t] = (t < count && src[t]) ? reinterpret_cast<const uint4*>(src[t]) : nullptr;
     pk.dst[t] = (t < count && src[t]) ? reinterpret_cast<uint4*>(dst[t]) : nullptr;
@@ -351,14 +414,20 @@ cudaError_t launch_convert_t(const __nv_bfloat16* q, const __nv_bfloat16* dout, 
 
 cudaError_t launch_order(const int32_t* k2q_num, int BH, int nb, int max_q, int32_t* order,
                          cudaStream_t stream) {
+  constexpr size_t DEFAULT_SMEM = 48 * 1024, MAX_SMEM = 232448;  // sm_103 opt-in limit per CTA
+  static std::atomic<uint64_t> smem_set{0};
   const size_t smem = static_cast<size_t>(nb) * sizeof(int32_t);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+  dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>((nb + 255) / 256));
+  if (smem > MAX_SMEM) {
+    order_kernel<false><<<grid, 256, 0, stream>>>(k2q_num, nb, max_q, order);
+    return cudaGetLastError();
+  }
+  if (smem > DEFAULT_SMEM) {
+    const cudaError_t e = ensure_smem_limit(order_kernel<true>, static_cast<int>(MAX_SMEM),
+                                            smem_set);
     if (e != cudaSuccess) return e;
   }
-  dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>((nb + 255) / 256));
-  order_kernel<<<grid, 256, smem, stream>>>(k2q_num, nb, max_q, order);
+  order_kernel<true><<<grid, 256, smem, stream>>>(k2q_num, nb, max_q, order);
   return cudaGetLastError();
 }
 

@@ -17,12 +17,12 @@ constexpr int ITEM_SLOTS = 4;
 
 // Producer: claim this CTA's k-th item into *w and publish it.  `full0` / `empty0` are the
 // shared addresses of FULL(0) / EMPTY(0); the slots' barriers follow at 8-byte steps.  False on
-// abort or timeout.
+// abort or when a wait runs past `limit_ns`.
 __device__ __forceinline__ bool publish_item(uint32_t full0, uint32_t empty0, volatile int* queue,
                                              uint32_t k, int32_t* counter, volatile int* abort,
-                                             int* w) {
+                                             uint64_t limit_ns, int* w) {
   const uint32_t slot = k % ITEM_SLOTS;
-  if (!mbar_wait_bounded(empty0 + 8u * slot, ((k / ITEM_SLOTS) & 1u) ^ 1u, abort, WAIT_LIMIT_NS))
+  if (!mbar_wait_bounded(empty0 + 8u * slot, ((k / ITEM_SLOTS) & 1u) ^ 1u, abort, limit_ns))
     return false;
   const int v = atomicAdd(counter, 1);
   queue[slot] = v;
@@ -33,9 +33,10 @@ __device__ __forceinline__ bool publish_item(uint32_t full0, uint32_t empty0, vo
 
 // Consumer (one thread): this CTA's k-th item; the slot is handed back at once.
 __device__ __forceinline__ bool take_item(uint32_t full0, uint32_t empty0, volatile int* queue,
-                                          uint32_t k, volatile int* abort, int* w) {
+                                          uint32_t k, volatile int* abort, uint64_t limit_ns,
+                                          int* w) {
   const uint32_t slot = k % ITEM_SLOTS;
-  if (!mbar_wait_bounded(full0 + 8u * slot, (k / ITEM_SLOTS) & 1u, abort, WAIT_LIMIT_NS))
+  if (!mbar_wait_bounded(full0 + 8u * slot, (k / ITEM_SLOTS) & 1u, abort, limit_ns))
     return false;
   *w = queue[slot];
   mbar_arrive(empty0 + 8u * slot);
@@ -45,9 +46,10 @@ __device__ __forceinline__ bool take_item(uint32_t full0, uint32_t empty0, volat
 // Consumer (a whole warp): lane 0 takes the item and broadcasts it; one arrival per warp.
 __device__ __forceinline__ bool warp_take_item(uint32_t full0, uint32_t empty0,
                                                volatile int* queue, uint32_t k,
-                                               volatile int* abort, int lane, int* w) {
+                                               volatile int* abort, uint64_t limit_ns, int lane,
+                                               int* w) {
   int ok = 1, v = 0;
-  if (lane == 0) ok = take_item(full0, empty0, queue, k, abort, &v) ? 1 : 0;
+  if (lane == 0) ok = take_item(full0, empty0, queue, k, abort, limit_ns, &v) ? 1 : 0;
   *w = __shfl_sync(0xffffffffu, v, 0);
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }

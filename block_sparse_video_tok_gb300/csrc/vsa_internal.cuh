@@ -3,6 +3,7 @@
 // host-side launch functions of every kernel.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
@@ -19,18 +20,41 @@ constexpr int HEAD_DIM = 128;  // the only supported head dimension
 constexpr int KP = 5;          // P is carried as P * 2^KP in fp16 (see operand_exponent)
 constexpr float LOG2E_F = 1.4426950408889634f;
 constexpr int ORDER_MIN_KV_BLOCKS = 1024;  // sort work items by list length from here on
-constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;   // pipeline waits: 4 s
-constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;   // in-flight copies after an abort: 0.2 s
+constexpr uint64_t DEFAULT_WAIT_LIMIT_NS = 4000000000ull;  // pipeline waits: 4 s
+constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;          // in-flight copies after an abort: 0.2 s
+
+// The limit of every pipeline wait in kernels launched from now on (vsa_set_wait_limit_ns; the
+// default unless a caller changed it).  The drains after an abort keep DRAIN_LIMIT_NS.
+uint64_t wait_limit_ns();
+// Sets it (0: back to DEFAULT_WAIT_LIMIT_NS); returns the previous limit.
+uint64_t set_wait_limit_ns(uint64_t ns);
 
 // ---------------------------------------------------------------------------- workspaces
 //
 // Every workspace starts with a 256-byte header (the device error word at offset 0) followed
-// by the per-(b, h) absolute maxima of the operands (4 x uint32 float bits per head: Q, K, V,
-// dO), then 1024-byte aligned arrays.
+// by per-(b, h) statistics of the operands (HEAD_STATS uint32 float bits per head, see HeadStat),
+// then 1024-byte aligned arrays.  The backward also keeps statistics per 64-token kv tile
+// (TILE_STATS words per tile of each head, see TileStat).
+
+constexpr int HEAD_STATS = 8;
+enum HeadStat : int {
+  HS_Q = 0,        // max |Q| of the head
+  HS_K = 1,        // max |K|
+  HS_V = 2,        // max |V|
+  HS_DO = 3,       // max |dO|
+  HS_DO_NORM = 4,  // max over rows of the row's L2 norm of dO (backward)
+  HS_DELTA = 5     // max over rows of |Delta| (backward)
+};
+constexpr int TILE_STATS = 4;
+enum TileStat : int {
+  TS_K = 0,      // max |K| over the tile's 64 rows
+  TS_V = 1,      // max |V|
+  TS_V_NORM = 2  // max over the tile's rows of the row's L2 norm of V
+};
 
 struct BwdLayout {
-  size_t err, sched, absmax, split_row, split_acc, delta, order, vbs64, dqacc, q16, k16, v16, do16,
-      total;
+  size_t err, sched, absmax, tstat, split_row, split_acc, delta, order, vbs64, dqacc, q16, k16,
+      v16, do16, total;
 };
 
 // The backward's main kernel hands out its last items as SPLIT_PARTS claims each (shares of the
@@ -64,7 +88,9 @@ inline BwdLayout bwd_layout(long B, long H, long S) {
   L.sched = 128;  // work counter of the main kernel's dynamic scheduler (inside the header)
   off += 256;
   L.absmax = off;
-  off = align_up(off + bh * 4 * sizeof(uint32_t), 1024);
+  off = align_up(off + bh * HEAD_STATS * sizeof(uint32_t), 1024);
+  L.tstat = off;
+  off = align_up(off + bh * nb * TILE_STATS * sizeof(uint32_t), 1024);
   // Split items: the first output row, and [parts][dV, dK][64][128] fp32 rows each.
   const size_t nsplit = static_cast<size_t>(split_capacity(static_cast<long>(bh * nb)));
   L.split_row = off;
@@ -100,7 +126,7 @@ inline FwdLayout fwd_layout(long B, long H, long S) {
   L.sched = 128;  // work counter of the main kernel's dynamic scheduler (inside the header)
   off += 256;
   L.absmax = off;
-  off = align_up(off + bh * 4 * sizeof(uint32_t), 1024);
+  off = align_up(off + bh * HEAD_STATS * sizeof(uint32_t), 1024);
   L.bitmap = off;
   off = align_up(off + bh * nb * words * sizeof(uint32_t), 1024);
   L.vbs64 = off;
@@ -113,12 +139,16 @@ inline FwdLayout fwd_layout(long B, long H, long S) {
 
 // ---------------------------------------------------------------------------- operand scales
 //
-// The tensor-core operands are fp16 copies X' = X * 2^-e of the bf16 inputs, with e the
-// binary exponent of max|X| over one (b, h) head, so |X'| < 2.  bf16 -> fp16 of such values is
-// exact except below 2^-17 (absolute error <= 2^-25).  P and dS are rounded to fp16 as well;
-// with |Q'|,|K'|,|V'|,|dO'| < 2 and head_dim 128, |dO'.V'| and |Delta'| stay below 512, so
-// dS' = P * 2^KP * (dP' - Delta') stays below 2^5 * 1026 < 65504.  The exponents are clamped to
-// [-40, 40]; NaN or Inf maxima give 0 (non-finite inputs then propagate).
+// The tensor-core operands are fp16 copies X' = X * 2^-e of the bf16 inputs, with e the binary
+// exponent of max|X| over a group of values, so |X'| < 2: Q and dO per (b, h) head, K and V of
+// the backward per 64-token kv tile (so that an outlier only moves the scale of its own tile), V
+// of the forward per head.  A value converts exactly unless it lies 17 or more binades below its
+// group's maximum (fp16 subnormals: absolute error <= 2^(e-25)).  P is carried as P * 2^KP
+// (P <= 1).  dS of kv tile j is carried as 2^kappa_j P (dP' - Delta'), with kappa_j from a bound
+// of |dP' - Delta'| (ds_exponent): a fixed scale would have to allow for the worst case, and an
+// outlier in dO or V would then push the dS values of every other row into fp16's subnormal
+// range.  The exponents are clamped to [-40, 40]; NaN or Inf maxima give 0 (non-finite inputs
+// then propagate).
 
 __host__ __device__ inline int operand_exponent(uint32_t absmax_bits) {
   const uint32_t bits = absmax_bits & 0x7FFFFFFFu;
@@ -138,6 +168,39 @@ __host__ __device__ inline float exp2i(int n) {
   return x.f;
 }
 
+__host__ __device__ inline float bits_float(uint32_t u) {
+  union {
+    uint32_t u;
+    float f;
+  } x;
+  x.u = u;
+  return x.f;
+}
+
+__host__ __device__ inline int clamp_exponent(int n, int lim) {
+  return n < -lim ? -lim : (n > lim ? lim : n);
+}
+
+// kappa_j, the exponent of the dS operand of kv tile j: dS' = fp16(2^kappa P (dP' - Delta')) with
+// dP' = dO'.V' = 2^-(eo + ev) dO.V (dO' scaled per head by 2^-eo, V' per tile by 2^-ev) and Delta'
+// = 2^-(eo + ev) Delta.  By Cauchy-Schwarz |dO_r . V_t| <= |dO_r| |V_t| (row L2 norms), so with
+// P <= 1, |dS'| <= 2^kappa 2^-(eo + ev) (max_r |dO_r| max_t|V_t| + max_r |Delta_r|) = 2^kappa b.
+// kappa = 13 - floor(log2 b) keeps |dS'| below 2^14, a factor of 4 under the fp16 maximum for the
+// rounding of the operands and of the fp32 sums.  Clamped to [-60, 60]; 0 if b is 0 or not finite.
+__host__ __device__ inline int ds_exponent(float do_norm, float v_norm, float delta_max, int eo,
+                                           int ev) {
+  const float a = exp2i(-eo), c = exp2i(-ev);
+  const float b = (do_norm * a) * (v_norm * c) + (delta_max * a) * c;
+  if (!(b > 0.f && b <= 3.4028235e38f)) return 0;
+  union {
+    float f;
+    uint32_t u;
+  } x;
+  x.f = b;
+  const int f = static_cast<int>((x.u >> 23) & 0xFFu) - 127;  // floor(log2 b); -127 if subnormal
+  return clamp_exponent(13 - f, 60);
+}
+
 // ---------------------------------------------------------------------------- launches
 // Each returns cudaSuccess or the launch error.  `stream` is the caller's stream.
 
@@ -150,11 +213,14 @@ cudaError_t launch_invert(const int32_t* q2k_idx, const int32_t* q2k_num, int to
 // A job too small for a launch of its own, done by the absmax_delta grid: the valid size of
 // every 64-token kv tile, vbs64[t] = clamp(vbs[t / tiles] - 64 (t % tiles), 0, 64) (an entry
 // outside [0, 64 tiles] raises VSA_DEVERR_VBS in *err).
+// With `tstat` non-null (the backward), the grid also writes the statistics of every 64-token kv
+// tile of K and V (TILE_STATS words each), and the per-head dO row-norm and |Delta| maxima.
 struct PreExtras {
   const int32_t* vbs;
   int nb, tiles;
   int32_t* vbs64;
   uint32_t* err;
+  uint32_t* tstat;
 };
 cudaError_t launch_absmax_delta(const __nv_bfloat16* q, const __nv_bfloat16* k,
                                 const __nv_bfloat16* v, const __nv_bfloat16* dout,
@@ -162,9 +228,12 @@ cudaError_t launch_absmax_delta(const __nv_bfloat16* q, const __nv_bfloat16* k,
                                 float* delta, float* dqacc, const PreExtras& x,
                                 cudaStream_t stream);
 
-// fp16 copies X' = X * 2^-e(head) of up to four [BH, S, 128] bf16 tensors (null entries skipped).
+// fp16 copies X' = X * 2^-e of up to four [BH, S, 128] bf16 tensors (null entries skipped), slot
+// t of the per-head statistics giving e; with `tstat` non-null, tensors 1 (K) and 2 (V) take e
+// per 64-token tile from the tile statistics instead.
 cudaError_t launch_convert(const __nv_bfloat16* const* src, __half* const* dst, int count, int BH,
-                           int S, const uint32_t* absmax, cudaStream_t stream);
+                           int S, const uint32_t* absmax, const uint32_t* tstat,
+                           cudaStream_t stream);
 // Q and dO of the backward as tile-transposed fp16: tile i of head bh is stored at
 // ((bh * S/64 + i) * 128 + d) * 64 + r for row r of the tile and head dim d, scaled like
 // launch_convert (operand slots 0 and 3 of the per-head maxima).
@@ -191,6 +260,7 @@ struct BwdMainArgs {
   const float* lse;
   const float* delta;
   const uint32_t* absmax;
+  const uint32_t* tstat;
   float* dqacc;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -204,6 +274,7 @@ struct BwdMainArgs {
   int tiles;  // 64-token tiles per sparse block: 1, or 2 for 128-token blocks
   int max_q;
   float sm_scale;
+  uint64_t wait_ns;  // limit of each pipeline wait
 };
 cudaError_t launch_bwd_main(const BwdMainArgs& a, cudaStream_t stream);
 // Items the main kernel splits in two for `items` work items on this device.
@@ -228,6 +299,7 @@ struct FwdMainArgs {
   int32_t* sched;  // zeroed work counter
   int B, H, S, nb;
   float sm_scale;
+  uint64_t wait_ns;  // limit of each pipeline wait
 };
 cudaError_t launch_fwd_main(const FwdMainArgs& a, cudaStream_t stream);
 
@@ -249,6 +321,22 @@ cudaError_t make_tmap_rows128_f16_halves(CUtensorMap* map, const void* base, lon
                                          int box_rows, bool bf16 = false);
 
 int device_sm_count();
+
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current device, once per
+// device: the attribute belongs to each device's context, so a process that drives several GPUs
+// sets it on each.  `done` keeps one bit per device id below 64 (ids from 64 on set it on every
+// call); concurrent first calls may both set it, which is harmless.
+template <typename Kernel>
+cudaError_t ensure_smem_limit(Kernel* kernel, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 // Records `e` as this thread's last CUDA error (vsa_last_cuda_error) and returns VSA_ERR_CUDA.
 vsa_status record_cuda_failure(cudaError_t e);

@@ -50,16 +50,19 @@ _lib = None
 SIGNATURES = {
     "vsa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "vsa_last_cuda_error": (ctypes.c_int, []),
+    "vsa_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
     "vsa_invert_indices": (ctypes.c_int, [_P, _P, _I32, VsaShape, _P, _P, _P, _P]),
     "vsa_fwd_workspace_bytes": (_SZ, [VsaShape]),
     "vsa_fwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _P, _F, VsaShape, _P, _P, _P, _SZ, _P]),
     "vsa_bwd_workspace_bytes": (_SZ, [VsaShape]),
+    "vsa_work_order": (ctypes.c_int, [_P, _I32, VsaShape, _P, _P]),
     "vsa_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _P, _F, VsaShape, _P, _P,
                                _P, _P, _SZ, _P]),
     "vsa_bwd_timed": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _P, _F, VsaShape, _P,
                                      _P, _P, _P, _SZ, ctypes.POINTER(VsaBwdEvents), _P]),
     "vsa_bwd_no_alloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _P, _F, VsaShape,
                                         _P, _P, _P, _P]),
+    "vsa_bwd_no_alloc_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), _P]),
     "vsa_read_device_error": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
 }
 
@@ -262,6 +265,37 @@ def vsa_bwd_no_alloc(dout, q, k, v, o, lse, k2q_idx, k2q_num, vbs, sm_scale, dq=
                                   make_shape(B, H, S, D, blk), _ptr(dq), _ptr(dk), _ptr(dv),
                                   _stream(stream)), "vsa_bwd_no_alloc")
     return dq, dk, dv
+
+
+def vsa_set_wait_limit_ns(limit_ns):
+    """Time limit of every pipeline wait in kernels launched from now on (0: the default, 4 s).
+    Returns the previous limit."""
+    return int(lib().vsa_set_wait_limit_ns(int(limit_ns)))
+
+
+def vsa_work_order(k2q_num, max_q_blocks, block=BLOCK, order=None, stream=None):
+    """The backward's work-item order (items sorted by descending clamped k2q count, stable, per
+    (b, h) segment): int32 [B * H * nb] of flat item ids."""
+    _need(k2q_num, "k2q_num", torch.int32, 3)
+    B, H, nb = k2q_num.shape
+    if order is None:
+        order = torch.empty(B * H * nb, dtype=torch.int32, device=k2q_num.device)
+    _need(order, "order", torch.int32, 1)
+    if order.numel() != B * H * nb:
+        raise ValueError("order must hold B * H * nb entries")
+    _check(lib().vsa_work_order(_ptr(k2q_num), int(max_q_blocks),
+                                make_shape(B, H, nb * block, HEAD_DIM, block), _ptr(order),
+                                _stream(stream)), "vsa_work_order")
+    return order
+
+
+def vsa_bwd_no_alloc_device_error(stream=None):
+    """Synchronise the stream and return the device error bits of the last vsa_bwd_no_alloc call
+    on the current device."""
+    bits = ctypes.c_uint32(0)
+    _check(lib().vsa_bwd_no_alloc_device_error(ctypes.byref(bits), _stream(stream)),
+           "vsa_bwd_no_alloc_device_error")
+    return int(bits.value)
 
 
 def vsa_read_device_error(workspace, stream=None):

@@ -30,8 +30,9 @@
  *     `block` tokens.
  *   - Pointers: every buffer is device memory owned and allocated by the caller; activation
  *     and workspace pointers must be 16-byte (activations) / 256-byte (workspace) aligned.
- *     The library never allocates, keeps no per-call state between calls and never
- *     synchronises the stream except in vsa_read_device_error.  `stream` is a cudaStream_t
+ *     The library never allocates, keeps no per-call state between calls (the wait limit of
+ *     vsa_set_wait_limit_ns is a process-wide setting) and never synchronises the stream except
+ *     in vsa_read_device_error and vsa_bwd_no_alloc_device_error.  `stream` is a cudaStream_t
  *     (NULL = legacy default stream).  Work is enqueued on it in order; the call returns
  *     before the GPU finishes.
  *   - Errors: problems visible on the host (null pointer, bad size, misalignment, too small a
@@ -66,7 +67,7 @@ typedef enum vsa_status {
 /* Bits of the device error word. */
 #define VSA_DEVERR_Q2K_ID 0x01u    /* a q2k block id outside [0, nb) was skipped */
 #define VSA_DEVERR_Q2K_COUNT 0x02u /* a q2k count outside [0, topk] was clamped */
-#define VSA_DEVERR_K2Q_ID 0x04u    /* a k2q block id outside [0, nb) was replaced by 0 */
+#define VSA_DEVERR_K2Q_ID 0x04u    /* a k2q block id outside [0, nb) was skipped */
 #define VSA_DEVERR_K2Q_COUNT 0x08u /* a k2q count outside [0, max_q_blocks] was clamped */
 #define VSA_DEVERR_VBS 0x10u       /* a variable_block_sizes entry outside [0, block] was clamped */
 #define VSA_DEVERR_TIMEOUT 0x20u   /* a pipeline wait ran past its limit; outputs are invalid */
@@ -84,6 +85,19 @@ const char* vsa_status_string(vsa_status status);
 
 /* The last CUDA error code seen by this thread's calls (0 if none); for VSA_ERR_CUDA. */
 int vsa_last_cuda_error(void);
+
+/*
+ * vsa_set_wait_limit_ns -- the time limit of every pipeline wait inside the kernels that this
+ * process launches from now on, on any device (the default is 4 s; 0 restores it).  Returns the
+ * previous limit.  The pages have no counterpart: it is the watchdog of the bounded waits that
+ * the error contract above describes.  A wait that runs past the limit sets VSA_DEVERR_TIMEOUT,
+ * the kernel lets the copies it has in flight land, frees its tensor memory and exits, and the
+ * outputs of that call are invalid; the device stays usable and later calls are unaffected.  A
+ * limit far below a kernel's normal waits (microseconds) makes every call time out, which is how
+ * a caller can check its handling of that error.  Thread-safe; launches already enqueued keep
+ * the limit they were given.
+ */
+uint64_t vsa_set_wait_limit_ns(uint64_t limit_ns);
 
 /*
  * vsa_invert_indices -- k2q from q2k.
@@ -147,7 +161,9 @@ size_t vsa_bwd_workspace_bytes(vsa_shape shape);
  *   lse          [B, H, S] fp32, M form, as written by vsa_fwd (read).
  *   k2q_idx      [B, H, nb, max_q_blocks] int32: per kv block the selecting q blocks (any
  *                order; entries past the count unread), e.g. from vsa_invert_indices with
- *                max_q_blocks = nb.
+ *                max_q_blocks = nb.  An id outside [0, nb) is skipped (VSA_DEVERR_K2Q_ID).  A
+ *                row must not repeat an id (vsa_invert_indices never does): a repeated id is
+ *                counted as often as it appears.
  *   k2q_num      [B, H, nb] int32 (clamped to [0, max_q_blocks]).
  *   max_q_blocks row stride of k2q_idx, >= 1.
  *   vbs, sm_scale: as for vsa_fwd.
@@ -162,6 +178,22 @@ vsa_status vsa_bwd(const void* dout, const void* q, const void* k, const void* v
                    int32_t max_q_blocks, const int32_t* vbs, float sm_scale, vsa_shape shape,
                    void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                    void* stream);
+
+/*
+ * vsa_work_order -- the order in which vsa_bwd's main kernel takes its work items when the
+ * sequence has at least 1024 kv tiles of 64 tokens (below that it takes them in item order).
+ * Defined by [FV-bwd] commit message (Semantics: from 1024 kv blocks on, the items are sorted on
+ * the device by the length of their k2q lists) and [FV-diff] ORDER_MIN_KV_BLOCKS: within each
+ * (b, h) segment, in head order, the kv blocks sorted by DESCENDING count, stable (equal counts
+ * keep ascending block order).  Computed here for any nb, so that a caller can inspect it.
+ *   k2q_num       [B, H, nb] int32 (read; each count clamped to [0, max_q_blocks] before
+ *                 sorting).
+ *   max_q_blocks  >= 1.
+ *   order         [B * H * nb] int32 (written): position x of segment bh holds the flat item id
+ *                 bh * nb + j of the kv block that comes x-th.
+ */
+vsa_status vsa_work_order(const int32_t* k2q_num, int32_t max_q_blocks, vsa_shape shape,
+                          int32_t* order, void* stream);
 
 /*
  * vsa_bwd_timed -- vsa_bwd, plus CUDA events recorded on `stream` around its stages, for callers
@@ -213,14 +245,22 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
  * array, which keeps the previous call's contents (each call clears what must start at zero).
  * Calls whose GPU work overlaps -- on different streams, or from host threads that are not
  * ordered -- race on the array; order them (one stream, or events).  The device error word of
- * the last call sits at the start of the array and is not reachable through
- * vsa_read_device_error.
+ * the last call sits at the start of the array: read it with vsa_bwd_no_alloc_device_error (not
+ * vsa_read_device_error, which takes a workspace pointer).
  */
 vsa_status vsa_bwd_no_alloc(const void* dout, const void* q, const void* k, const void* v,
                             const void* o, const float* lse, const int32_t* k2q_idx,
                             const int32_t* k2q_num, int32_t max_q_blocks, const int32_t* vbs,
                             float sm_scale, vsa_shape shape, void* dq, void* dk, void* dv,
                             void* stream);
+
+/*
+ * vsa_bwd_no_alloc_device_error -- synchronise `stream`, then copy to *bits the device error word
+ * that the last vsa_bwd_no_alloc call on the current device left in the static scratch array
+ * (VSA_DEVERR_* bits; 0 if no call has run on this device yet).  Like the entry point it serves,
+ * it allocates nothing.  Another call's GPU work that overlaps the read races with it.
+ */
+vsa_status vsa_bwd_no_alloc_device_error(uint32_t* bits, void* stream);
 
 /*
  * vsa_read_device_error -- synchronise `stream`, then copy the device error word of a

@@ -134,3 +134,21 @@ def bwd(q, k, v, o, do, lse, q2k_idx, q2k_num, vbs, sm_scale, blk=64, qblocks=No
                        _ptr(qb), 0 if qb is None else qb.size, _ptr(kb),
                        0 if kb is None else kb.size, _ptr(dq), _ptr(dk), _ptr(dv))
     return dq, dk, dv
+
+
+def work_order(k2q_num, max_q):
+    """The backward's work order: the FastVideo sm_100a backward's commit message (Semantics)
+    sorts the (batch, head, kv block) items by the length of their k2q lists from 1024 kv blocks
+    on, and its launch header (compare main...vsa_bwd_fix, ORDER_MIN_KV_BLOCKS) keeps the (b, h)
+    segments in head order.  Plain definition: for each (b, h) in order, its kv blocks j by
+    DESCENDING count (clamped to [0, max_q], the bounded active prefix of cudnn-frontend PR #926,
+    Summary), equal counts in ascending j (a stable sort; Python's sort is stable).  Returns
+    int32 [B * H * nb] of flat item ids bh * nb + j."""
+    num = np.asarray(k2q_num).reshape(-1, np.asarray(k2q_num).shape[-1])
+    n_heads, nb = num.shape
+    out = []
+    for bh in range(n_heads):
+        counts = [min(max(int(c), 0), int(max_q)) for c in num[bh]]
+        for j in sorted(range(nb), key=lambda x: -counts[x]):
+            out.append(bh * nb + j)
+    return np.asarray(out, dtype=np.int32)

@@ -32,7 +32,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(vsa):
     names = declared_functions()
-    assert len(names) == 10, names
+    assert len(names) == 13, names
     lib = vsa.lib()
     for name in names:
         assert hasattr(lib, name), name
@@ -89,3 +89,22 @@ def test_host_side_rejections(vsa):
     p = ctypes.c_void_p(0x100000)
     assert lib.vsa_invert_indices(p, p, 0, good, p, p, None, None) == 1
     assert lib.vsa_fwd(p, p, p, p, p, 4, p, 0.1, good, p, p, p, 16, None) == 3
+
+
+def test_host_side_rejections_of_the_helpers(vsa):
+    lib = vsa.lib()
+    p = ctypes.c_void_p(0x100000)
+    good = vsa.make_shape(1, 2, 512)
+    assert lib.vsa_work_order(None, 8, good, p, None) == 1        # null counts
+    assert lib.vsa_work_order(p, 0, good, p, None) == 1           # max_q_blocks < 1
+    assert lib.vsa_work_order(p, 8, vsa.make_shape(1, 2, 500), p, None) == 2
+    assert lib.vsa_bwd_no_alloc_device_error(None, None) == 1     # no place for the bits
+
+
+def test_wait_limit_setting_round_trips(vsa):
+    lib = vsa.lib()
+    default = 4_000_000_000
+    prev = lib.vsa_set_wait_limit_ns(1000)
+    assert prev == default
+    assert lib.vsa_set_wait_limit_ns(0) == 1000                   # 0 restores the default
+    assert lib.vsa_set_wait_limit_ns(0) == default

@@ -7,10 +7,9 @@ inputs.
   max|d| <= 1e-2 max|ref| and mean|d| <= 1e-3 mean|ref| (tests/parity.py), on small cases that
   span several work items, odd pair tails, ragged and empty blocks, unselected kv blocks and
   empty query rows; exact +0.0 for unselected kv blocks and padded kv rows;
-- the full-size workloads, in the launch configuration the benchmark times (GPU forward ->
-  inversion -> backward), on sampled query blocks and kv blocks that the oracle computes one by
-  one;
-- two backward runs agree (dK, dV bitwise; dQ within 5e-3 of max|dQ|).
+- k2q ids outside [0, nb) are skipped and reported;
+- the work order is bit-exact against the oracle's.
+The full-size workloads are in test_gpu_full_size.py.
 """
 import numpy as np
 import pytest
@@ -151,6 +150,43 @@ SMALL_CASES["blk128_batch2_zero_kv"] = lambda: wl.make_case(2, 2, 6, 2, vbs="rag
 SMALL_CASES["split_parts_short_lists"] = lambda: wl.make_case(1, 16, 16, 3, vbs="ragged32", seed=41,
                                                              kv_pool=list(range(14)))
 
+def _outliers(case, which="qkvd", factor=1e3, seed=0):
+    """One element per (b, h) head of each named tensor (q, k, v, d = dO) replaced by
+    +-3 * factor: about `factor` times the largest of the head's other N(0, 1) values.  Such an
+    outlier sets the per-head scale of its tensor, which moves every other value of the head
+    `log2(factor)` binades down the fp16 range of the kernels' operand copies."""
+    rng = np.random.default_rng(seed)
+    names = {"q": "q", "k": "k", "v": "v", "d": "do"}
+    for w in which:
+        t = case[names[w]].float()
+        B, H, S, D = t.shape
+        for b in range(B):
+            for h in range(H):
+                t[b, h, int(rng.integers(S)), int(rng.integers(D))] = \
+                    float(rng.choice([-3.0, 3.0])) * factor
+        case[names[w]] = t.to(torch.bfloat16)
+    return case
+
+
+def _head_scaled(case, factor=1e-3):
+    """Odd heads' Q, K, V and dO multiplied by `factor` (rounded to bf16 again): heads whose
+    values differ by three orders of magnitude in one call."""
+    for n in ("q", "k", "v", "do"):
+        t = case[n].float()
+        t[:, 1::2] *= factor
+        case[n] = t.to(torch.bfloat16)
+    return case
+
+
+# Outliers (fp16 operand scaling): every tensor at once on the tiny and 4k workloads; V and dO
+# (the operands of dP, whose product sets the range of dS) at 8k tokens and full density, where
+# P is as small as at 32k tokens and 25 %.
+SMALL_CASES["outliers_tiny"] = lambda: _outliers(wl.make_config("tiny"), seed=81)
+SMALL_CASES["outliers_4k"] = lambda: _outliers(wl.make_config("4k_25pct"), seed=82)
+SMALL_CASES["outliers_v_do_8k_dense"] = lambda: _outliers(
+    wl.make_case(1, 2, 128, 128, seed=83), which="vd", seed=83)
+SMALL_CASES["head_scales_4k"] = lambda: _head_scaled(wl.make_config("4k_25pct"))
+
 SMALL_CASES["growing_scores"] = lambda: _scaled_kv_blocks(
     wl.make_case(1, 2, 16, 8, vbs="ragged32", seed=15), lambda j: 1.0 + j)
 SMALL_CASES["shrinking_scores"] = lambda: _scaled_kv_blocks(
@@ -244,93 +280,84 @@ def test_device_error_bits_and_clean_results(vsa):
     assert torch.equal(o_d, o_c) and torch.equal(lse_d, lse_c)
 
 
-# ------------------------------------------------------------------------------ full size
+# ------------------------------------------------------------------------------ invalid k2q ids
 
 
-def _head_case(case, b, h):
-    sub = {n: case[n][b:b + 1, h:h + 1].contiguous() for n in ("q", "k", "v", "do")}
-    sub["q2k_idx"] = case["q2k_idx"][b:b + 1, h:h + 1]
-    sub["q2k_num"] = case["q2k_num"][b:b + 1, h:h + 1]
-    sub["vbs"] = case["vbs"]
-    sub["sm_scale"] = case["sm_scale"]
-    sub["blk"] = case.get("blk", 64)
-    return sub
+def _dirty_k2q(k2q_idx, k2q_num, nb, rng, aligned, keep_last=0):
+    """Copy of a k2q list with ids outside [0, nb) added to some rows.  aligned: the bad ids go
+    in as a pair at an even position, so every step keeps its pair of valid q blocks (the dK/dV
+    accumulation order is unchanged); else one bad id at position 1 (the pairing shifts).  The
+    last `keep_last` rows (in item order) stay clean: the backward splits its last items into
+    parts by step count, and a longer list would move the part boundaries."""
+    idx, num = k2q_idx.copy(), k2q_num.copy()
+    B, H, _, width = idx.shape
+    for b in range(B):
+        for h in range(H):
+            for j in range(nb):
+                if (b * H + h) * nb + j >= B * H * nb - keep_last:
+                    continue
+                n = int(num[b, h, j])
+                extra = 2 if aligned else 1
+                if n + extra > width or rng.random() < 0.3:
+                    continue
+                row = idx[b, h, j, :n].tolist()
+                pos = 2 * int(rng.integers(0, n // 2 + 1)) if aligned else min(1, n)
+                bad = [-1 - int(rng.integers(0, 5)), nb + int(rng.integers(0, 5))][:extra]
+                row[pos:pos] = bad
+                idx[b, h, j, :n + extra] = row
+                num[b, h, j] = n + extra
+    return idx, num
 
 
-def _full_size(vsa, name, n_heads=2, n_q=3, n_kv=2, seed=0):
-    case = wl.make_config(name)
+@pytest.mark.parametrize("aligned", [True, False])
+def test_invalid_k2q_ids_are_skipped(vsa, aligned):
+    """A k2q id outside [0, nb) is skipped and reported: the result equals that of the clean
+    list (dK, dV bitwise when the bad ids keep the step pairs), and matches the oracle."""
+    case = wl.make_case(1, 2, 16, 6, vbs="ragged32", seed=51)
     B, H, S, nb = case["B"], case["H"], case["S"], case["nb"]
+    (o64, lse64), (dq64, dk64, dv64), (dq, dk, dv), _ = _run_small(vsa, case)
+    o_b = bf16_round(o64).cuda()
+    lse = torch.from_numpy(lse64.astype(np.float32)).cuda()
     dev = to_device(case)
-    o, lse = vsa.vsa_fwd(dev["q"], dev["k"], dev["v"], dev["q2k_idx"], dev["q2k_num"], dev["vbs"],
-                         case["sm_scale"])
     k2q_idx, k2q_num = vsa.vsa_invert_indices(dev["q2k_idx"], dev["q2k_num"], nb)
+    rng = np.random.default_rng(7)
+    d_idx, d_num = _dirty_k2q(k2q_idx.cpu().numpy(), k2q_num.cpu().numpy(), nb, rng, aligned,
+                              keep_last=8)
+    assert (d_num > k2q_num.cpu().numpy()).any()
     ws = torch.empty(vsa.vsa_bwd_workspace_bytes(B, H, S), dtype=torch.uint8, device="cuda")
-    dq, dk, dv = vsa.vsa_bwd(dev["do"], dev["q"], dev["k"], dev["v"], o, lse, k2q_idx, k2q_num,
-                             dev["vbs"], case["sm_scale"], workspace=ws)
-    assert vsa.vsa_read_device_error(ws) == 0
-    counts = k2q_num.cpu().numpy()
-    rng = np.random.default_rng(seed)
-    heads = [(int(rng.integers(B)), int(rng.integers(H))) for _ in range(n_heads)]
-    results = []
-    for b, h in heads:
-        sub = _head_case(case, b, h)
-        cnt = counts[b, h]
-        q_s = sorted(set(int(x) for x in rng.choice(nb, n_q, replace=False)))
-        # kv blocks with a moderate list length (the oracle recomputes every selecting row),
-        # plus one no q block selects, when there is one.
-        mid = np.flatnonzero((cnt > 0) & (cnt <= max(160, int(np.median(cnt)))))
-        kv_s = sorted(set(int(x) for x in rng.choice(mid, n_kv, replace=False)))
-        zero = np.flatnonzero(cnt == 0)
-        kv_all = kv_s + ([int(zero[0])] if zero.size else [])
-        sel = sub["q2k_idx"][0, 0]
-        need = set(q_s)
-        for j in kv_s:
-            need.update(int(i) for i in range(nb) if j in sel[i, :sub["q2k_num"][0, 0, i]])
-        need = sorted(need)
-        o64, lse64 = oracle_forward(sub, qblocks=need)
-        o_b = bf16_round(np.nan_to_num(o64))
-        lse32 = lse64.astype(np.float32)
-        dq64, dk64, dv64 = oracle_backward(sub, f64(o_b), np.nan_to_num(lse32.astype(np.float64)),
-                                           qblocks=q_s, kvblocks=kv_all)
-        blk = case.get("blk", 64)
-        for i in q_s:
-            r = slice(blk * i, blk * (i + 1))
-            results.append(check_close("%s o[%d,%d,q%d]" % (name, b, h, i), o[b, h, r],
-                                       o64[0, 0, r]))
-            g = lse[b, h, r].cpu().numpy().astype(np.float64)
-            assert np.abs(g - lse64[0, 0, r]).max() <= 1e-4 * max(1.0, np.abs(lse64[0, 0, r]).max())
-            results.append(check_close("%s dq[%d,%d,q%d]" % (name, b, h, i), dq[b, h, r],
-                                       dq64[0, 0, r]))
-        for j in kv_all:
-            r = slice(blk * j, blk * (j + 1))
-            if cnt[j] == 0:
-                assert zero_bits(dk[b, h, r]).all() and zero_bits(dv[b, h, r]).all()
-                continue
-            results.append(check_close("%s dk[%d,%d,kv%d]" % (name, b, h, j), dk[b, h, r],
-                                       dk64[0, 0, r]))
-            results.append(check_close("%s dv[%d,%d,kv%d]" % (name, b, h, j), dv[b, h, r],
-                                       dv64[0, 0, r]))
-    return dev, case, (o, lse, k2q_idx, k2q_num), (dq, dk, dv)
+    outs = [torch.full_like(dev["q"], float("nan")) for _ in range(3)]
+    g = vsa.vsa_bwd(dev["do"], dev["q"], dev["k"], dev["v"], o_b, lse,
+                    torch.from_numpy(d_idx).cuda(), torch.from_numpy(d_num).cuda(), dev["vbs"],
+                    case["sm_scale"], dq=outs[0], dk=outs[1], dv=outs[2], workspace=ws)
+    bits = vsa.vsa_read_device_error(ws)
+    assert bits & vsa.DEVERR_K2Q_ID and not bits & vsa.DEVERR_TIMEOUT
+    check_close("dq", g[0], dq64)
+    check_close("dk", g[1], dk64)
+    check_close("dv", g[2], dv64)
+    if aligned:
+        assert torch.equal(g[1], dk) and torch.equal(g[2], dv)
 
 
-@pytest.mark.parametrize("name", ["32k_25pct", "65k_12pct_zipf", "video_dit_21x30x52",
-                                  "32k_25pct_blk128"])
-def test_full_size_sampled(vsa, name):
-    _full_size(vsa, name)
+# ------------------------------------------------------------------------------ work order
 
 
-def test_long_sequence_sampled(vsa):
-    """524,288 tokens (8192 kv blocks, so the work order is sorted) at low density: sampled
-    parity of O, lse, dQ, dK and dV, and exact zeros for unselected kv blocks."""
-    _full_size(vsa, "524k_sparse")
-
-
-def test_two_runs_agree_at_65k(vsa):
-    dev, case, (o, lse, k2q_idx, k2q_num), (dq, dk, dv) = _full_size(vsa, "65k_12pct_zipf",
-                                                                   n_heads=1, n_q=1, n_kv=1)
-    dq2, dk2, dv2 = vsa.vsa_bwd(dev["do"], dev["q"], dev["k"], dev["v"], o, lse, k2q_idx, k2q_num,
-                                dev["vbs"], case["sm_scale"])
+@pytest.mark.parametrize("name", ["65k_12pct_zipf", "ties", "long_rows"])
+def test_work_order_bit_exact(vsa, name):
+    """The backward's item order (vsa_work_order, the same launch the backward makes from 1024
+    kv tiles on) against the oracle's stable descending sort, bit for bit."""
+    if name == "65k_12pct_zipf":
+        q2k_idx, q2k_num = wl.make_selection(1, 8, 1024, 128, select="zipf", seed=0)
+        _, k_num, _ = orc.invert(q2k_idx, q2k_num, 1024)
+        max_q = 1024
+    elif name == "ties":   # few distinct counts, some out of range: long runs of ties
+        rng = np.random.default_rng(3)
+        k_num = rng.integers(-2, 7, size=(2, 3, 1500)).astype(np.int32)
+        max_q = 4
+    else:                  # a head too long for the shared-memory copy of its counts
+        rng = np.random.default_rng(4)
+        k_num = rng.integers(0, 300, size=(1, 1, 65536)).astype(np.int32)
+        max_q = 256
+    want = orc.work_order(k_num, max_q)
+    got = vsa.vsa_work_order(torch.from_numpy(k_num).cuda(), max_q)
     torch.cuda.synchronize()
-    assert torch.equal(dk, dk2) and torch.equal(dv, dv2)
-    d = (dq.float() - dq2.float()).abs()
-    assert d.max().item() <= 5e-3 * dq.float().abs().max().item()
+    assert np.array_equal(got.cpu().numpy(), want)

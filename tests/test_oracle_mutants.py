@@ -89,3 +89,47 @@ def test_planted_mistake_is_caught(name):
         except AssertionError:
             failures += 1
     assert failures > 0, "no pin caught the planted mistake " + name
+
+
+# The work order is plain Python in oracle.py: its mistakes are planted in a copy of that
+# function's source, executed on its own, and the work-order pins must catch each.
+WORK_ORDER_MUTATIONS = {
+    "order_ascending": ("key=lambda x: -counts[x]", "key=lambda x: counts[x]"),
+    "order_ties_descending": ("key=lambda x: -counts[x]", "key=lambda x: (-counts[x], -x)"),
+    "order_no_clamp": ("min(max(int(c), 0), int(max_q))", "int(c)"),
+    "order_local_ids": ("out.append(bh * nb + j)", "out.append(j)"),
+}
+
+
+class _OrderBound:
+    def __init__(self, fn):
+        self.work_order = fn
+
+
+def _work_order_variant(old, new):
+    import inspect
+    import textwrap
+    src = textwrap.dedent(inspect.getsource(oracle_mod.work_order))
+    assert src.count(old) == 1, "mutation anchor not unique: " + old
+    ns = {"np": oracle_mod.np}
+    exec(compile(src.replace(old, new), "<work_order variant>", "exec"), ns)  # noqa: S102
+    return _OrderBound(ns["work_order"])
+
+
+def test_unmutated_work_order_copy_passes_its_pins():
+    bound = _work_order_variant("key=lambda x: -counts[x]", "key=lambda x: -counts[x]")
+    pins.test_work_order_golden_fixture(bound)
+    pins.test_work_order_properties(bound, 0)
+
+
+@pytest.mark.parametrize("name", sorted(WORK_ORDER_MUTATIONS))
+def test_planted_work_order_mistake_is_caught(name):
+    bound = _work_order_variant(*WORK_ORDER_MUTATIONS[name])
+    failures = 0
+    for t in (lambda o: pins.test_work_order_golden_fixture(o),
+              lambda o: pins.test_work_order_properties(o, 0)):
+        try:
+            t(bound)
+        except AssertionError:
+            failures += 1
+    assert failures > 0, "no pin caught the planted mistake " + name

@@ -264,3 +264,34 @@ def test_backward_subsets_match_full(oracle):
     assert np.array_equal(dq2[0, 1, 64:128], dq[0, 1, 64:128])
     assert np.array_equal(dk2[0, 0, 64:128], dk[0, 0, 64:128])
     assert np.array_equal(dv2[0, 1, 256:320], dv[0, 1, 256:320])
+
+
+# ----------------------------------------------------------------------------- work order
+
+
+def test_work_order_golden_fixture(oracle):
+    with open(os.path.join(HERE, "golden", "work_order_tiny.json")) as f:
+        data = json.load(f)
+    for case in data["cases"]:
+        got = oracle.work_order(np.asarray(case["k2q_num"], np.int32), case["max_q"])
+        assert got.tolist() == case["order"], case["note"]
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_work_order_properties(oracle, seed):
+    """Within every head: a permutation of the head's items, clamped counts non-increasing, and
+    equal counts in ascending block order -- properties that fix a stable descending sort."""
+    rng = np.random.default_rng(seed)
+    B, H, nb, max_q = 2, 3, 257, 40
+    num = rng.integers(-3, max_q + 6, size=(B, H, nb)).astype(np.int32)
+    num[0, 1, :] = 7                       # a head of equal counts keeps block order
+    order = oracle.work_order(num, max_q)
+    flat = np.clip(num.reshape(-1), 0, max_q)
+    for bh in range(B * H):
+        seg = order[bh * nb:(bh + 1) * nb]
+        assert sorted(seg.tolist()) == list(range(bh * nb, (bh + 1) * nb))
+        c = flat[seg]
+        assert np.all(c[:-1] >= c[1:])
+        tie = c[:-1] == c[1:]
+        assert np.all(seg[:-1][tie] < seg[1:][tie])
+    assert order[nb:2 * nb].tolist() == list(range(nb, 2 * nb))

@@ -71,3 +71,27 @@ def test_no_alloc_rejects_shapes_that_do_not_fit(vsa):
     bad_dim = vsa.make_shape(1, 2, 4096, 64)
     args[11] = bad_dim
     assert lib.vsa_bwd_no_alloc(*args) == 2     # VSA_ERR_UNSUPPORTED, as vsa_bwd reports
+
+
+def test_no_alloc_reports_device_errors(vsa):
+    """The error word of a no-allocation call lives in the library's scratch array; the companion
+    entry point reads it back.  A k2q id outside [0, nb) is skipped and reported; a clean call
+    that follows reports nothing (each call clears the word)."""
+    case = wl.make_case(1, 2, 8, 3, vbs="ragged32", seed=32)
+    nb = case["nb"]
+    dev = to_device(case)
+    o, lse = vsa.vsa_fwd(dev["q"], dev["k"], dev["v"], dev["q2k_idx"], dev["q2k_num"], dev["vbs"],
+                         case["sm_scale"])
+    k2q_idx, k2q_num = vsa.vsa_invert_indices(dev["q2k_idx"], dev["q2k_num"], nb)
+    torch.cuda.synchronize()
+    args = (dev["do"], dev["q"], dev["k"], dev["v"], o, lse)
+    dirty_idx, dirty_num = k2q_idx.clone(), k2q_num.clone()
+    j = int(torch.nonzero(k2q_num[0, 0] < nb - 1)[0])
+    n = int(k2q_num[0, 0, j])
+    dirty_idx[0, 0, j, n] = nb + 3          # one more slot, with an id past the last block
+    dirty_num[0, 0, j] = n + 1
+    vsa.vsa_bwd_no_alloc(*args, dirty_idx, dirty_num, dev["vbs"], case["sm_scale"])
+    bits = vsa.vsa_bwd_no_alloc_device_error()
+    assert bits & vsa.DEVERR_K2Q_ID and not bits & vsa.DEVERR_TIMEOUT, hex(bits)
+    vsa.vsa_bwd_no_alloc(*args, k2q_idx, k2q_num, dev["vbs"], case["sm_scale"])
+    assert vsa.vsa_bwd_no_alloc_device_error() == 0
