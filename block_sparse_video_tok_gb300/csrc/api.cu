@@ -180,6 +180,7 @@ vsa_status vsa_fwd(const void* q, const void* k, const void* v, const int32_t* q
   x.vbs64 = vbs64;
   x.err = err;
   x.tstat = nullptr;
+  x.k16 = x.v16 = nullptr;
   if ((e = vsa::launch_absmax_delta(nullptr, nullptr, vb, nullptr, nullptr, BH, S, absmax, nullptr,
                                     nullptr, x, s)) != cudaSuccess)
     return cuda_fail(e);
@@ -271,15 +272,14 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
   x.vbs64 = vbs64;
   x.err = err;
   x.tstat = tstat;
+  // K and V are scaled per 64-token tile, so the statistics pass converts them as it goes
+  // (row-major); Q and dO are scaled per head and converted once the head's maxima are known,
+  // tile-transposed (one 16 KB copy per 64-row tile in the main kernel, whatever the distance
+  // between the two q tiles of a step).
+  x.k16 = k16;
+  x.v16 = v16;
   if ((e = vsa::launch_absmax_delta(qb, kb, vb, dob, ob, BH, S, absmax, delta, dqacc, x, s)) !=
       cudaSuccess)
-    return cuda_fail(e);
-  // K and V row-major, scaled per 64-token tile; Q and dO tile-transposed, scaled per head (one
-  // 16 KB copy per 64-row tile in the main kernel, whatever the distance between the two q tiles
-  // of a step).
-  const __nv_bfloat16* src[4] = {nullptr, kb, vb, nullptr};
-  __half* dst[4] = {nullptr, k16, v16, nullptr};
-  if ((e = vsa::launch_convert(src, dst, 4, BH, S, absmax, tstat, s)) != cudaSuccess)
     return cuda_fail(e);
   if ((e = vsa::launch_convert_t(qb, dob, q16, do16, BH, S, absmax, s)) != cudaSuccess)
     return cuda_fail(e);

@@ -43,6 +43,18 @@ __device__ __forceinline__ uint32_t warp_max(uint32_t v) {
   return v;
 }
 
+// 8 bf16 values times s, rounded to fp16 (round to nearest even).
+__device__ __forceinline__ uint4 to_half8(uint4 x, float s) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  uint32_t out[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 h = __floats2half2_rn(bf16lo(w[i]) * s, bf16hi(w[i]) * s);
+    out[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
 // Sum of squares of the 8 bf16 values of a 16-byte chunk.
 __device__ __forceinline__ float sumsq8(uint4 x) {
   float s = bf16lo(x.x) * bf16lo(x.x) + bf16hi(x.x) * bf16hi(x.x);
@@ -88,18 +100,25 @@ __global__ void __launch_bounds__(PRE_THREADS) absmax_delta_kernel(
   const int sub = threadIdx.x & 15;   // 16-byte chunk of the row
   const bool bwd = (dout != nullptr);
   const bool stats = (x.tstat != nullptr);
+  constexpr int ROWS = BLOCK / (PRE_THREADS / 16);  // rows of the tile per thread
   // Maxima as float bits (non-negative floats order like their bits): |Q|, |K|, |V|, |dO|, then
   // the squared row norms of dO and V and |Delta|.
   uint32_t mq = 0, mk = 0, mv = 0, mdo = 0, ndo2 = 0, nv2 = 0, mdl = 0;
-  for (int rr = half; rr < BLOCK; rr += PRE_THREADS / 16) {
+  uint4 kt[ROWS], vt[ROWS];  // this thread's chunks of the K and V tile, converted at the end
+#pragma unroll
+  for (int u = 0; u < ROWS; ++u) {
+    const int rr = half + u * (PRE_THREADS / 16);
     const size_t row = static_cast<size_t>(bh) * S + static_cast<size_t>(blockIdx.x) * BLOCK + rr;
     const size_t at = row * 16 + sub;
     if (q) mq = max(mq, absmax_bits8(q[at]));  // a null operand is not scanned (its max stays 0)
-    if (k) mk = max(mk, absmax_bits8(k[at]));
+    if (k) {
+      kt[u] = k[at];
+      mk = max(mk, absmax_bits8(kt[u]));
+    }
     if (v) {
-      const uint4 vv = v[at];
-      mv = max(mv, absmax_bits8(vv));
-      if (stats) nv2 = max(nv2, __float_as_uint(row_sum16(sumsq8(vv))));
+      vt[u] = v[at];
+      mv = max(mv, absmax_bits8(vt[u]));
+      if (stats) nv2 = max(nv2, __float_as_uint(row_sum16(sumsq8(vt[u]))));
     }
     if (bwd) {
       const uint4 a = dout[at], b = o[at];
@@ -134,31 +153,44 @@ __global__ void __launch_bounds__(PRE_THREADS) absmax_delta_kernel(
     uint32_t m = 0;
     for (int w = 0; w < PRE_THREADS / 32; ++w) m = max(m, red[threadIdx.x][w]);
     uint32_t* hs = absmax + bh * HEAD_STATS;
+    uint32_t* ts = stats ? x.tstat + (static_cast<size_t>(bh) * gridDim.x + blockIdx.x) * TILE_STATS
+                         : nullptr;
     const int i = threadIdx.x;
     if (i < 4) {
       if (m) atomicMax(hs + i, m);  // HS_Q, HS_K, HS_V, HS_DO
+      if (stats && i == 1) ts[TS_K] = m;  // one CTA per tile: plain stores
+      if (stats && i == 2) ts[TS_V] = m;
     } else if (stats) {
       // Squared norms become norms here (sqrt is monotonic, so the maximum is kept).
       const uint32_t val = (i == 6) ? m : __float_as_uint(sqrtf(__uint_as_float(m)));
-      uint32_t* ts = x.tstat + (static_cast<size_t>(bh) * gridDim.x + blockIdx.x) * TILE_STATS;
       if (i == 4) {
         if (val) atomicMax(hs + HS_DO_NORM, val);
       } else if (i == 5) {
-        ts[TS_V_NORM] = val;  // one CTA per tile: a plain store
+        ts[TS_V_NORM] = val;
       } else {
         if (val) atomicMax(hs + HS_DELTA, val);
       }
     }
   }
-  if (stats && threadIdx.x == 0) {
-    uint32_t* ts = x.tstat + (static_cast<size_t>(bh) * gridDim.x + blockIdx.x) * TILE_STATS;
-    uint32_t m_k = 0, m_v = 0;
+  if (x.k16 != nullptr) {
+    // The tile's K and V maxima are in red[1], red[2]: convert the chunks held in registers.
+    uint32_t tk = 0, tv = 0;
+#pragma unroll
     for (int w = 0; w < PRE_THREADS / 32; ++w) {
-      m_k = max(m_k, red[1][w]);
-      m_v = max(m_v, red[2][w]);
+      tk = max(tk, red[1][w]);
+      tv = max(tv, red[2][w]);
     }
-    ts[TS_K] = m_k;
-    ts[TS_V] = m_v;
+    const float sk = exp2i(-operand_exponent(tk)), sv = exp2i(-operand_exponent(tv));
+    uint4* k16 = reinterpret_cast<uint4*>(x.k16);
+    uint4* v16 = reinterpret_cast<uint4*>(x.v16);
+#pragma unroll
+    for (int u = 0; u < ROWS; ++u) {
+      const int rr = half + u * (PRE_THREADS / 16);
+      const size_t at =
+          (static_cast<size_t>(bh) * S + static_cast<size_t>(blockIdx.x) * BLOCK + rr) * 16 + sub;
+      k16[at] = to_half8(kt[u], sk);
+      v16[at] = to_half8(vt[u], sv);
+    }
   }
 }
 
@@ -184,16 +216,7 @@ __global__ void __launch_bounds__(256) convert_kernel(ConvertPack pk, size_t chu
     // tiles).
     const uint32_t bits = per_tile ? pk.tstat[(c >> 10) * TILE_STATS + (t == 1 ? TS_K : TS_V)]
                                    : absmax[bh * HEAD_STATS + t];
-    const float s = exp2i(-operand_exponent(bits));
-    const uint4 x = src[c];
-    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-    uint32_t out[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const __half2 h = __floats2half2_rn(bf16lo(w[i]) * s, bf16hi(w[i]) * s);
-      out[i] = *reinterpret_cast<const uint32_t*>(&h);
-    }
-    dst[c] = make_uint4(out[0], out[1], out[2], out[3]);
+    dst[c] = to_half8(src[c], exp2i(-operand_exponent(bits)));
   }
 }
 

@@ -214,13 +214,17 @@ cudaError_t launch_invert(const int32_t* q2k_idx, const int32_t* q2k_num, int to
 // every 64-token kv tile, vbs64[t] = clamp(vbs[t / tiles] - 64 (t % tiles), 0, 64) (an entry
 // outside [0, 64 tiles] raises VSA_DEVERR_VBS in *err).
 // With `tstat` non-null (the backward), the grid also writes the statistics of every 64-token kv
-// tile of K and V (TILE_STATS words each), and the per-head dO row-norm and |Delta| maxima.
+// tile of K and V (TILE_STATS words each) and the per-head dO row-norm and |Delta| maxima, and,
+// since each CTA holds one whole tile of K and V, their fp16 copies scaled by the tile's own
+// exponent (k16, v16: row-major [BH * S, 128]).
 struct PreExtras {
   const int32_t* vbs;
   int nb, tiles;
   int32_t* vbs64;
   uint32_t* err;
   uint32_t* tstat;
+  __half* k16;
+  __half* v16;
 };
 cudaError_t launch_absmax_delta(const __nv_bfloat16* q, const __nv_bfloat16* k,
                                 const __nv_bfloat16* v, const __nv_bfloat16* dout,
