@@ -3,8 +3,8 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
 
 One step = one pass of the backward hot path over one batch of synthetic input: the k2q
-inversion and the backward (preprocess, work order when nb >= 1024, main kernel, dQ
-postprocess), all through the C ABI (libvsa.so).  The forward runs once before the timed region
+inversion and the backward (preprocess with the work order, main kernel, dQ postprocess), all
+through the C ABI (libvsa.so).  The forward runs once before the timed region
 to produce O and lse (its own time is reported under "fwd").
 
 value   bwd TFLOPS on selected blocks: pairs x 5 x (2 x 64 x 64 x 128) flop / step time, summed
@@ -356,8 +356,9 @@ def main():
     k2q_num = torch.empty((B, H, nb), dtype=torch.int32, device=device)
     dq, dk, dv = (torch.empty_like(dev["q"]) for _ in range(3))
     ws = torch.empty(vsa.vsa_bwd_workspace_bytes(B, H, S), dtype=torch.uint8, device=device)
-    # invert, absmax/delta, convert (K, V), convert_t (Q, dO), [order], main, postprocess
-    kernels_per_step = 6 + (1 if nb >= 1024 else 0)
+    # invert, statistics (Delta, dQ zeroing, K/V to fp16, work order), convert_t (Q, dO), main,
+    # postprocess
+    kernels_per_step = 5
 
     def step(events=None, inv=None):
         if inv is not None:
@@ -519,7 +520,7 @@ def main():
         "config": {"workload": args.config, "B": B, "H": H, "S": S, "D": 128, "nb": nb,
                    "topk": cfg["topk"], "selection": cfg["select"], "vbs": cfg["vbs"],
                    "pairs_per_gpu": pairs, "l2": "inputs larger than L2 (no flush)",
-                   "step": "invert + backward (preprocess, order if nb>=1024, main, postprocess)",
+                   "step": "invert + backward (preprocess with the work order, main, postprocess)",
                    "parallelism": "replicas over (b,h) problems, one per GPU"},
         "pct_of_peak": 100.0 * value / peak / world,
         "breakdown_ms": {"invert": float(np.mean(inv_ms)), "preprocess": float(np.mean(pre_ms)),

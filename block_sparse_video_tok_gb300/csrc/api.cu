@@ -2,7 +2,8 @@
 // carving and the stream-ordered launch sequence of each operation.  Follows the host surface of
 // FastVideo's backward (compare main...vsa_bwd_fix, block_sparse_bwd_launch_sm100a.cuh:
 // block_sparse_bwd_supported returns an error for bad configurations; the launch chains
-// preprocess -> order -> main -> postprocess on one stream without a host sync) and the caller-
+// preprocess -> order -> main -> postprocess on one stream without a host sync; here the order
+// is computed inside the preprocess) and the caller-
 // workspace contract of cudnn-frontend PR #926's follow-up (no allocation on the hot path).
 #include <climits>
 #include <cmath>
@@ -32,6 +33,11 @@ int device_sm_count() {
   return sms;
 }
 
+bool use_work_order(int BH, int S) {
+  const long tiles = S / BLOCK;
+  return tiles >= ORDER_MIN_KV_TILES || BH * tiles < 8L * device_sm_count();
+}
+
 }  // namespace vsa
 
 namespace {
@@ -57,6 +63,8 @@ vsa_status check_shape(const vsa_shape& s, int* nb, int* blk = nullptr) {
   if (s.seqlen % b != 0) return VSA_ERR_UNSUPPORTED;
   const long long rows = static_cast<long long>(s.batch) * s.heads * s.seqlen;
   if (rows > INT_MAX / 2) return VSA_ERR_UNSUPPORTED;
+  // Some grids put B * H on their second dimension (at most 65535 blocks).
+  if (static_cast<long long>(s.batch) * s.heads > 65535) return VSA_ERR_UNSUPPORTED;
   *nb = s.seqlen / b;
   if (blk) *blk = b;
   return VSA_OK;
@@ -181,6 +189,8 @@ vsa_status vsa_fwd(const void* q, const void* k, const void* v, const int32_t* q
   x.err = err;
   x.tstat = nullptr;
   x.k16 = x.v16 = nullptr;
+  x.k2q_num = nullptr;
+  x.order = nullptr;
   if ((e = vsa::launch_absmax_delta(nullptr, nullptr, vb, nullptr, nullptr, BH, S, absmax, nullptr,
                                     nullptr, x, s)) != cudaSuccess)
     return cuda_fail(e);
@@ -278,17 +288,20 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
   // between the two q tiles of a step).
   x.k16 = k16;
   x.v16 = v16;
+  // The work order (items by descending list length, stable, per head), a side job of the same
+  // grid, is used from 1024 kv tiles on (the pages' rule) and when there are fewer than 8 items
+  // per SM (the longest items first then even out the CTAs' few items: 3 % off the main kernel
+  // at 4k tokens); in between, the item order is as fast and the side job would cost a few µs.
+  const bool sorted = vsa::use_work_order(BH, S);
+  x.k2q_num = k2q_num;
+  x.order = sorted ? order : nullptr;
+  x.nsel = nb;
+  x.max_q = max_q_blocks;
   if ((e = vsa::launch_absmax_delta(qb, kb, vb, dob, ob, BH, S, absmax, delta, dqacc, x, s)) !=
       cudaSuccess)
     return cuda_fail(e);
   if ((e = vsa::launch_convert_t(qb, dob, q16, do16, BH, S, absmax, s)) != cudaSuccess)
     return cuda_fail(e);
-  const int32_t* work_order = nullptr;
-  if (S / vsa::BLOCK >= vsa::ORDER_MIN_KV_BLOCKS) {
-    if ((e = vsa::launch_order(k2q_num, BH, nb, max_q_blocks, order, s)) != cudaSuccess)
-      return cuda_fail(e);
-    work_order = order;
-  }
   vsa::BwdMainArgs a{};
   a.q16 = q16;
   a.k16 = k16;
@@ -296,7 +309,7 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
   a.do16 = do16;
   a.k2q_idx = k2q_idx;
   a.k2q_num = k2q_num;
-  a.order = work_order;
+  a.order = sorted ? order : nullptr;
   a.vbs = vbs64;
   a.lse = lse;
   a.delta = delta;

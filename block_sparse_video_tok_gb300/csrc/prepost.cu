@@ -12,7 +12,7 @@
 //                 ([128 head dims][64 rows]), so one 16 KB copy brings a whole tile.
 //   order         work order: (b, h) segments, items sorted by descending k2q list length,
 //                 stable (the commit message: sorted on the device, from 1024 kv blocks per
-//                 sequence on).
+//                 sequence on; here at every size, computed by the statistics pass).
 //   postprocess   dQ = bf16(dqacc * sm_scale * 2^scale) (the commit message's postprocess step
 //                 applies sm_scale to dQ); the dV, dK rows of the main kernel's split items.
 //   fwd_bitmap    per-q-block selection bitmaps for the forward.
@@ -71,11 +71,35 @@ __device__ __forceinline__ float row_sum16(float s) {
   return s;
 }
 
+// Position of k2q row x of one head in the work order: the rows whose count (clamped to
+// [0, max_q]) is larger, plus the rows with an equal count and a smaller index -- a stable sort
+// by descending count.  Executed by a whole CTA of 256 threads, which all get the result;
+// `scratch` is 8 shared ints, free again on return.
+__device__ __forceinline__ int order_position(const int32_t* __restrict__ counts, int n,
+                                              int max_q, int x, int* scratch) {
+  auto clamped = [max_q](int c) { return c < 0 ? 0 : (c > max_q ? max_q : c); };
+  const int cx = clamped(counts[x]);
+  int pos = 0;
+  for (int y = threadIdx.x; y < n; y += blockDim.x) {
+    const int cy = clamped(__ldg(counts + y));
+    pos += (cy > cx) || (cy == cx && y < x);
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) pos += __shfl_xor_sync(0xffffffffu, pos, d);
+  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = pos;
+  __syncthreads();
+  int total = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) total += scratch[w];
+  __syncthreads();
+  return total;
+}
+
 // Grid (S / 64, BH), 256 threads: 16 lanes per 128-element row (8 bf16 = 16 B per lane), two
 // rows per warp per iteration, 64 rows per CTA.
 constexpr int PRE_THREADS = 256;
 
-__global__ void __launch_bounds__(PRE_THREADS) absmax_delta_kernel(
+__global__ void __launch_bounds__(PRE_THREADS, 4) absmax_delta_kernel(
     const uint4* __restrict__ q, const uint4* __restrict__ k, const uint4* __restrict__ v,
     const uint4* __restrict__ dout, const uint4* __restrict__ o, int S, uint32_t* absmax,
     float* __restrict__ delta, float4* __restrict__ dqacc, PreExtras x) {
@@ -141,6 +165,15 @@ __global__ void __launch_bounds__(PRE_THREADS) absmax_delta_kernel(
   }
   constexpr int NRED = 7;
   __shared__ uint32_t red[NRED][PRE_THREADS / 32];
+  __shared__ int scratch[PRE_THREADS / 32];
+  // A side job of the backward's grid: CTA (tile, head) places k2q row `tile` of its head in the
+  // work order (one CTA per row; the rows are blocks of x.tiles 64-token tiles).
+  if (x.order != nullptr && static_cast<int>(blockIdx.x) < x.nsel) {
+    const int r = blockIdx.x;
+    const size_t seg = static_cast<size_t>(bh) * x.nsel;
+    const int pos = order_position(x.k2q_num + seg, x.nsel, x.max_q, r, scratch);
+    if (threadIdx.x == 0) x.order[seg + pos] = static_cast<int32_t>(seg) + r;
+  }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t mine[NRED] = {mq, mk, mv, mdo, ndo2, nv2, mdl};
 #pragma unroll
@@ -270,31 +303,19 @@ __global__ void __launch_bounds__(256) convert_t_kernel(ConvertTPack pk, int S,
   }
 }
 
-// Grid (BH, ceil(nb / 256)): item x of head bh goes to position
-// #{y : c_y > c_x} + #{y < x : c_y == c_x}, i.e. a stable sort by descending count, with the
-// counts clamped to [0, max_q].  kShared: the head's counts are staged in shared memory first
-// (nb * 4 bytes); otherwise (rows too long for shared memory) each thread reads them from global
-// memory.
-template <bool kShared>
-__global__ void __launch_bounds__(256) order_kernel(const int32_t* __restrict__ k2q_num, int nb,
-                                                    int max_q, int32_t* __restrict__ order) {
-  extern __shared__ int32_t cnt[];
-  const int bh = blockIdx.x;
-  const int32_t* num = k2q_num + static_cast<size_t>(bh) * nb;
-  auto clamped = [max_q](int c) { return c < 0 ? 0 : (c > max_q ? max_q : c); };
-  if (kShared) {
-    for (int y = threadIdx.x; y < nb; y += blockDim.x) cnt[y] = clamped(num[y]);
-    __syncthreads();
+// One CTA per item (grid-stride over the B * H * n items): item x of head bh goes to position
+// order_position(x) of its head's segment.  The same function places the items in the backward's
+// statistics pass, so this launch (vsa_work_order) shows the order the backward uses.
+__global__ void __launch_bounds__(256) order_kernel(const int32_t* __restrict__ k2q_num, int n,
+                                                    long items, int max_q,
+                                                    int32_t* __restrict__ order) {
+  __shared__ int scratch[8];
+  for (long i = blockIdx.x; i < items; i += gridDim.x) {
+    const long bh = i / n;
+    const int x = static_cast<int>(i - bh * n);
+    const int pos = order_position(k2q_num + bh * n, n, max_q, x, scratch);
+    if (threadIdx.x == 0) order[bh * n + pos] = static_cast<int32_t>(bh * n + x);
   }
-  const int x = blockIdx.y * blockDim.x + threadIdx.x;
-  if (x >= nb) return;
-  const int cx = kShared ? cnt[x] : clamped(num[x]);
-  int pos = 0;
-  for (int y = 0; y < nb; ++y) {
-    const int cy = kShared ? cnt[y] : clamped(__ldg(num + y));
-    pos += (cy > cx) || (cy == cx && y < x);
-  }
-  order[static_cast<size_t>(bh) * nb + pos] = bh * nb + x;
 }
 
 __global__ void __launch_bounds__(256) postprocess_kernel(
@@ -437,20 +458,9 @@ cudaError_t launch_convert_t(const __nv_bfloat16* q, const __nv_bfloat16* dout, 
 
 cudaError_t launch_order(const int32_t* k2q_num, int BH, int nb, int max_q, int32_t* order,
                          cudaStream_t stream) {
-  constexpr size_t DEFAULT_SMEM = 48 * 1024, MAX_SMEM = 232448;  // sm_103 opt-in limit per CTA
-  static std::atomic<uint64_t> smem_set{0};
-  const size_t smem = static_cast<size_t>(nb) * sizeof(int32_t);
-  dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>((nb + 255) / 256));
-  if (smem > MAX_SMEM) {
-    order_kernel<false><<<grid, 256, 0, stream>>>(k2q_num, nb, max_q, order);
-    return cudaGetLastError();
-  }
-  if (smem > DEFAULT_SMEM) {
-    const cudaError_t e = ensure_smem_limit(order_kernel<true>, static_cast<int>(MAX_SMEM),
-                                            smem_set);
-    if (e != cudaSuccess) return e;
-  }
-  order_kernel<true><<<grid, 256, smem, stream>>>(k2q_num, nb, max_q, order);
+  const long items = static_cast<long>(BH) * nb;
+  order_kernel<<<grid_for(static_cast<size_t>(items) * 256, 256, 8), 256, 0, stream>>>(
+      k2q_num, nb, items, max_q, order);
   return cudaGetLastError();
 }
 

@@ -19,7 +19,7 @@ constexpr int BLOCK = 64;      // tokens per sparse block
 constexpr int HEAD_DIM = 128;  // the only supported head dimension
 constexpr int KP = 5;          // P is carried as P * 2^KP in fp16 (see operand_exponent)
 constexpr float LOG2E_F = 1.4426950408889634f;
-constexpr int ORDER_MIN_KV_BLOCKS = 1024;  // sort work items by list length from here on
+constexpr int ORDER_MIN_KV_TILES = 1024;  // the backward sorts its items from here on
 constexpr uint64_t DEFAULT_WAIT_LIMIT_NS = 4000000000ull;  // pipeline waits: 4 s
 constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;          // in-flight copies after an abort: 0.2 s
 
@@ -216,7 +216,9 @@ cudaError_t launch_invert(const int32_t* q2k_idx, const int32_t* q2k_num, int to
 // With `tstat` non-null (the backward), the grid also writes the statistics of every 64-token kv
 // tile of K and V (TILE_STATS words each) and the per-head dO row-norm and |Delta| maxima, and,
 // since each CTA holds one whole tile of K and V, their fp16 copies scaled by the tile's own
-// exponent (k16, v16: row-major [BH * S, 128]).
+// exponent (k16, v16: row-major [BH * S, 128]).  With `order` non-null it also writes the work
+// order of the nsel k2q rows of every head (launch_order's permutation; counts k2q_num clamped
+// to [0, max_q]).
 struct PreExtras {
   const int32_t* vbs;
   int nb, tiles;
@@ -225,6 +227,9 @@ struct PreExtras {
   uint32_t* tstat;
   __half* k16;
   __half* v16;
+  const int32_t* k2q_num;
+  int32_t* order;
+  int nsel, max_q;
 };
 cudaError_t launch_absmax_delta(const __nv_bfloat16* q, const __nv_bfloat16* k,
                                 const __nv_bfloat16* v, const __nv_bfloat16* dout,
@@ -259,7 +264,7 @@ struct BwdMainArgs {
   const __half *q16, *k16, *v16, *do16;
   const int32_t* k2q_idx;
   const int32_t* k2q_num;
-  const int32_t* order;  // null: identity order
+  const int32_t* order;  // the work order (vsa_work_order's permutation), or null: item order
   const int32_t* vbs;
   const float* lse;
   const float* delta;
@@ -325,6 +330,10 @@ cudaError_t make_tmap_rows128_f16_halves(CUtensorMap* map, const void* base, lon
                                          int box_rows, bool bf16 = false);
 
 int device_sm_count();
+
+// Whether vsa_bwd takes its work items in the sorted order (vsa_work_order) on this device:
+// from ORDER_MIN_KV_TILES 64-token kv tiles per sequence on, or with fewer than 8 items per SM.
+bool use_work_order(int BH, int S);
 
 // Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current device, once per
 // device: the attribute belongs to each device's context, so a process that drives several GPUs

@@ -58,8 +58,8 @@ extern "C" {
 typedef enum vsa_status {
   VSA_OK = 0,
   VSA_ERR_INVALID_ARG = 1, /* null pointer, bad size or stride, misalignment, bad sm_scale */
-  VSA_ERR_UNSUPPORTED = 2, /* head_dim != 128, block not 64/128, S not a multiple of block, or
-                              not an sm_103 device */
+  VSA_ERR_UNSUPPORTED = 2, /* head_dim != 128, block not 64/128, S not a multiple of block,
+                              B * H above 65535, or not an sm_103 device */
   VSA_ERR_WORKSPACE = 3,   /* workspace NULL, misaligned or smaller than required */
   VSA_ERR_CUDA = 4         /* a CUDA runtime or driver call failed (see vsa_last_cuda_error) */
 } vsa_status;
@@ -180,12 +180,14 @@ vsa_status vsa_bwd(const void* dout, const void* q, const void* k, const void* v
                    void* stream);
 
 /*
- * vsa_work_order -- the order in which vsa_bwd's main kernel takes its work items when the
- * sequence has at least 1024 kv tiles of 64 tokens (below that it takes them in item order).
- * Defined by [FV-bwd] commit message (Semantics: from 1024 kv blocks on, the items are sorted on
- * the device by the length of their k2q lists) and [FV-diff] ORDER_MIN_KV_BLOCKS: within each
- * (b, h) segment, in head order, the kv blocks sorted by DESCENDING count, stable (equal counts
- * keep ascending block order).  Computed here for any nb, so that a caller can inspect it.
+ * vsa_work_order -- the order in which vsa_bwd's main kernel takes its work items.  Defined by
+ * [FV-bwd] commit message (Semantics: from 1024 kv blocks on, the items are sorted on the device
+ * by the length of their k2q lists) and [FV-diff] ORDER_MIN_KV_BLOCKS: within each (b, h)
+ * segment, in head order, the kv blocks sorted by DESCENDING count, stable (equal counts keep
+ * ascending block order).  vsa_bwd computes this order inside its preprocess, with the same
+ * device code as this call, and takes its items in it from 1024 kv tiles of 64 tokens on (as the
+ * pages do) and when there are fewer than 8 items (kv tiles of all heads) per SM, where the
+ * longest items first even out the CTAs' few items; otherwise it takes them in item order.
  *   k2q_num       [B, H, nb] int32 (read; each count clamped to [0, max_q_blocks] before
  *                 sorting).
  *   max_q_blocks  >= 1.

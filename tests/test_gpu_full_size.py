@@ -13,7 +13,7 @@ through the C ABI), with every output element accounted for.
   dQ, dK, dV).  It is the last head in claim order, which holds every item the backward splits
   into parts (the grid's last claims).  The kv block with the longest k2q list of the whole
   workload (the first item the sorted order hands out) is compared too.
-- The work order the backward uses (from 1024 kv tiles on) bit for bit against the oracle's.
+- The work order the backward uses bit for bit against the oracle's.
 The backward gets the GPU forward's O and lse; the oracle's backward is given the same O and lse,
 and the GPU forward itself is checked against the oracle's forward on the whole head.
 """
@@ -124,10 +124,8 @@ def check_blocks(case, fwd, grads, b, h, qblocks, kvblocks, label):
 
 
 def check_work_order(vsa, case, k2q_num):
-    """From 1024 kv tiles on the backward takes its items in the order vsa_work_order computes
-    (the same launch); check it bit for bit against the oracle."""
-    if case["S"] // 64 < 1024:
-        return
+    """The backward takes its items in the order vsa_work_order computes (the same device code
+    places them in the backward's preprocess); check it bit for bit against the oracle."""
     got = vsa.vsa_work_order(k2q_num, case["nb"], block=case.get("blk", 64))
     torch.cuda.synchronize()
     assert np.array_equal(got.cpu().numpy(), orc.work_order(k2q_num.cpu().numpy(), case["nb"]))

@@ -283,29 +283,27 @@ def test_device_error_bits_and_clean_results(vsa):
 # ------------------------------------------------------------------------------ invalid k2q ids
 
 
-def _dirty_k2q(k2q_idx, k2q_num, nb, rng, aligned, keep_last=0):
-    """Copy of a k2q list with ids outside [0, nb) added to some rows.  aligned: the bad ids go
-    in as a pair at an even position, so every step keeps its pair of valid q blocks (the dK/dV
-    accumulation order is unchanged); else one bad id at position 1 (the pairing shifts).  The
-    last `keep_last` rows (in item order) stay clean: the backward splits its last items into
-    parts by step count, and a longer list would move the part boundaries."""
+def _dirty_k2q(k2q_idx, k2q_num, nb, rng, aligned, heads=(0,)):
+    """Copy of a k2q list with ids outside [0, nb) added to every row of the given (flat) heads.
+    aligned: the bad ids go in as a pair at an even position, so every step keeps its pair of
+    valid q blocks (the dK/dV accumulation order is unchanged); else one bad id at position 1
+    (the pairing shifts).  Every row of a head gets the same number of extra slots, so the
+    head's work order (by count) is unchanged, and the other heads -- among them the last one,
+    whose last items the backward splits into parts -- are left alone."""
     idx, num = k2q_idx.copy(), k2q_num.copy()
     B, H, _, width = idx.shape
-    for b in range(B):
-        for h in range(H):
-            for j in range(nb):
-                if (b * H + h) * nb + j >= B * H * nb - keep_last:
-                    continue
-                n = int(num[b, h, j])
-                extra = 2 if aligned else 1
-                if n + extra > width or rng.random() < 0.3:
-                    continue
-                row = idx[b, h, j, :n].tolist()
-                pos = 2 * int(rng.integers(0, n // 2 + 1)) if aligned else min(1, n)
-                bad = [-1 - int(rng.integers(0, 5)), nb + int(rng.integers(0, 5))][:extra]
-                row[pos:pos] = bad
-                idx[b, h, j, :n + extra] = row
-                num[b, h, j] = n + extra
+    extra = 2 if aligned else 1
+    for flat in heads:
+        b, h = divmod(flat, H)
+        for j in range(nb):
+            n = int(num[b, h, j])
+            assert n + extra <= width
+            row = idx[b, h, j, :n].tolist()
+            pos = 2 * int(rng.integers(0, n // 2 + 1)) if aligned else min(1, n)
+            bad = [-1 - int(rng.integers(0, 5)), nb + int(rng.integers(0, 5))][:extra]
+            row[pos:pos] = bad
+            idx[b, h, j, :n + extra] = row
+            num[b, h, j] = n + extra
     return idx, num
 
 
@@ -321,8 +319,7 @@ def test_invalid_k2q_ids_are_skipped(vsa, aligned):
     dev = to_device(case)
     k2q_idx, k2q_num = vsa.vsa_invert_indices(dev["q2k_idx"], dev["q2k_num"], nb)
     rng = np.random.default_rng(7)
-    d_idx, d_num = _dirty_k2q(k2q_idx.cpu().numpy(), k2q_num.cpu().numpy(), nb, rng, aligned,
-                              keep_last=8)
+    d_idx, d_num = _dirty_k2q(k2q_idx.cpu().numpy(), k2q_num.cpu().numpy(), nb, rng, aligned)
     assert (d_num > k2q_num.cpu().numpy()).any()
     ws = torch.empty(vsa.vsa_bwd_workspace_bytes(B, H, S), dtype=torch.uint8, device="cuda")
     outs = [torch.full_like(dev["q"], float("nan")) for _ in range(3)]
@@ -343,8 +340,8 @@ def test_invalid_k2q_ids_are_skipped(vsa, aligned):
 
 @pytest.mark.parametrize("name", ["65k_12pct_zipf", "ties", "long_rows"])
 def test_work_order_bit_exact(vsa, name):
-    """The backward's item order (vsa_work_order, the same launch the backward makes from 1024
-    kv tiles on) against the oracle's stable descending sort, bit for bit."""
+    """The backward's item order (vsa_work_order; the backward's preprocess places its items with
+    the same device code) against the oracle's stable descending sort, bit for bit."""
     if name == "65k_12pct_zipf":
         q2k_idx, q2k_num = wl.make_selection(1, 8, 1024, 128, select="zipf", seed=0)
         _, k_num, _ = orc.invert(q2k_idx, q2k_num, 1024)
