@@ -152,12 +152,14 @@ def test_full_size_whole_head(vsa, name):
         check_blocks(case, fwd, grads, lb, lh, [], [lj], name + " longest")
 
 
-@pytest.mark.parametrize("name", ["262k_25pct", "524k_sparse", "wan480p_h12"])
+@pytest.mark.parametrize("name", ["131k_25pct", "262k_25pct", "524k_25pct", "524k_sparse",
+                                  "wan480p_h12"])
 def test_long_sequence_sampled(vsa, name):
-    """Sequences of 262,144 tokens at 25 % density (4096 kv blocks), 524,288 tokens at low
-    density (8192) and a Wan 480P-like layer (12 heads, 149,760 tokens in 2340 clipped 4x4x4
-    cubes, 12.5 %): every head as above; sampled q and kv blocks of the last head (including its
-    shortest lists, the split items) and the longest list, against the oracle."""
+    """Sequences of 131,072, 262,144 and 524,288 tokens at 25 % density (2048, 4096 and 8192 kv
+    blocks), 524,288 tokens at low density and a Wan 480P-like layer (12 heads, 149,760 tokens in
+    2340 clipped 4x4x4 cubes, 12.5 %): every head as above; sampled q and kv blocks of the last
+    head (including its shortest lists, the split items) and the longest list, against the
+    oracle."""
     case = wl.make_config(name)
     B, H, nb = case["B"], case["H"], case["nb"]
     dev, fwd, grads = run_chain(vsa, case)
