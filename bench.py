@@ -12,7 +12,8 @@ value   bwd TFLOPS on selected blocks: pairs x 5 x (2 x 64 x 64 x 128) flop / st
         L2, so no separate flush), timed with CUDA events on the launching stream.
 e2e     the same metric with host buffers: every step copies the inputs from pinned host memory
         to the device and the gradients back, inside the timed region.
-roofline  the main kernel against the measured dense 16-bit tensor peak (MEASURED_PEAKS.json).
+roofline  the main kernel against the measured dense 16-bit tensor peak (MEASURED_PEAKS.json), with
+          its fraction of the nominal 2.25 PFLOP/s and its ncu tensor-pipe activity beside it.
 cpu_baseline  the CPU oracle timed on a bounded sample of the same workload (rank 0, N = 1).
 
 With --impl reference the CPU oracle is the timed implementation (rank 0 only).
@@ -68,22 +69,34 @@ def kernel_code_hash(text):
     return hashlib.sha256(t.encode()).hexdigest()
 
 
-def main_kernel_traffic(config):
-    """DRAM bytes per main-kernel launch from the committed ncu summary of this workload, or None
-    when there is none or the kernel's code changed since it was captured."""
+def main_kernel_profile(config):
+    """(DRAM bytes per main-kernel launch, tensor-pipe active fraction) from the committed ncu
+    summary of this workload, or (None, None) when there is none or the kernel's code changed
+    since it was captured."""
     import re
     prof = os.path.join(ROOT, "profiles", "bwd_main_%s.md" % config.split("_")[0])
     src = os.path.join(ROOT, "block_sparse_video_tok_gb300", "csrc", "bwd_main.cu")
     if not os.path.exists(prof):
-        return None
+        return None, None
     text = open(prof).read()
     m_code = re.search(r"code sha256 at capture: `([0-9a-f]{64})`", text)
     m_tr = re.search(r"traffic_bytes_per_launch \| (\d+)", text)
+    m_tp = re.search(r"sm__pipe_tensor_cycles_active \| ([0-9.]+) %", text)
     if not (m_code and m_tr):
-        return None
+        return None, None
     if kernel_code_hash(open(src).read()) != m_code.group(1):
-        return None
-    return int(m_tr.group(1))
+        return None, None
+    return int(m_tr.group(1)), (float(m_tp.group(1)) / 100.0 if m_tp else None)
+
+
+def main_kernel_traffic(config):
+    """DRAM bytes per main-kernel launch from the committed ncu summary (see main_kernel_profile)."""
+    return main_kernel_profile(config)[0]
+
+
+# Nominal dense 16-bit tensor rate of a GB300 (PFLOP/s at its maximum clock); context only, the
+# roofline's peak is the measured one.
+NOMINAL_BF16_TFLOPS = 2250.0
 
 
 def peaks():
@@ -526,7 +539,9 @@ def main():
         "breakdown_ms": {"invert": float(np.mean(inv_ms)), "preprocess": float(np.mean(pre_ms)),
                          "main": main_avg, "postprocess": float(np.mean(post_ms))},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": main_kernel_traffic(args.config),
+                     "frac": achieved / peak, "traffic": main_kernel_profile(args.config)[0],
+                     "frac_of_nominal": achieved / NOMINAL_BF16_TFLOPS,
+                     "tensor_pipe_active_ncu": main_kernel_profile(args.config)[1],
                      "peak_source": "%s bf16_tflops (burst); fp16 dense rate = bf16" % peak_src,
                      "frac_of_sustained": achieved / peak_sus},
         "fwd": {"ms": fwd_ms, "note": "operand producer, timed alone; not in the step"},
