@@ -187,6 +187,19 @@ SMALL_CASES["outliers_v_do_8k_dense"] = lambda: _outliers(
     wl.make_case(1, 2, 128, 128, seed=83), which="vd", seed=83)
 SMALL_CASES["head_scales_4k"] = lambda: _head_scaled(wl.make_config("4k_25pct"))
 
+def _zero_tiles(case):
+    """Tiles of zeros: V of kv tile 1 and K of kv tile 3 in head 0, and all of dO in head 1 --
+    the per-tile and per-head scale exponents of zero groups, and a dS bound of zero."""
+    for n, sl in (("v", (0, 0, slice(64, 128))), ("k", (0, 0, slice(192, 256))),
+                  ("do", (0, 1, slice(None)))):
+        t = case[n].clone()
+        t[sl] = 0
+        case[n] = t
+    return case
+
+
+SMALL_CASES["zero_tiles"] = lambda: _zero_tiles(wl.make_case(1, 2, 8, 4, vbs="ragged32", seed=91))
+
 SMALL_CASES["growing_scores"] = lambda: _scaled_kv_blocks(
     wl.make_case(1, 2, 16, 8, vbs="ragged32", seed=15), lambda j: 1.0 + j)
 SMALL_CASES["shrinking_scores"] = lambda: _scaled_kv_blocks(
@@ -358,3 +371,28 @@ def test_work_order_bit_exact(vsa, name):
     got = vsa.vsa_work_order(torch.from_numpy(k_num).cuda(), max_q)
     torch.cuda.synchronize()
     assert np.array_equal(got.cpu().numpy(), want)
+
+
+def test_nan_stays_in_its_head(vsa):
+    """A NaN in one head's Q shows up in that head's gradients (nothing masks it), and the other
+    head -- with its own operand scales and work items -- gives the results of the clean run."""
+    case = wl.make_case(1, 2, 8, 4, vbs="ragged32", seed=92)
+    B, H, S, nb = case["B"], case["H"], case["S"], case["nb"]
+    o64, lse64 = oracle_forward(case)
+    o_b = bf16_round(o64).cuda()
+    lse = torch.from_numpy(lse64.astype(np.float32)).cuda()
+    dev = to_device(case)
+    k2q_idx, k2q_num = vsa.vsa_invert_indices(dev["q2k_idx"], dev["q2k_num"], nb)
+    args = (dev["do"], dev["q"], dev["k"], dev["v"], o_b, lse, k2q_idx, k2q_num, dev["vbs"],
+            case["sm_scale"])
+    clean = vsa.vsa_bwd(*args)
+    q_nan = dev["q"].clone()
+    q_nan[0, 0, 5, 3] = float("nan")
+    dirty = vsa.vsa_bwd(args[0], q_nan, *args[2:])
+    torch.cuda.synchronize()
+    for name, c, d in zip(("dq", "dk", "dv"), clean, dirty):
+        assert torch.isnan(d[0, 0].float()).any(), name
+        assert torch.isfinite(d[0, 1].float()).all(), name
+    assert torch.equal(clean[1][0, 1], dirty[1][0, 1]) and torch.equal(clean[2][0, 1], dirty[2][0, 1])
+    dq_c, dq_d = clean[0][0, 1].float(), dirty[0][0, 1].float()
+    assert (dq_c - dq_d).abs().max() <= 5e-3 * dq_c.abs().max()
