@@ -5,7 +5,8 @@
 // which produces dK, dV and the dQ partials).  The item's k2q list of q blocks is walked two q
 // blocks at a time, so every UMMA has M = 128 (the q pair, or the 128 head-dim rows) and the
 // fp32 accumulator maps row m to TMEM lane m.  Per q pair (p = the pair's 128 query rows, all
-// operands fp16 with per-head power-of-two scales, fp32 accumulation):
+// operands fp16 with power-of-two scales -- per head for Q and dO, per kv tile for K, V and dS,
+// see ItemScales -- and fp32 accumulation):
 //   S   [128 q  x  64 kv] = Q_p  K_j^T      A = Q_p    (MN-major), B = K_j (K-major)
 //   dP  [128 q  x  64 kv] = dO_p V_j^T      A = dO_p   (MN-major), B = V_j (K-major)
 //   P   = exp2(S * c - lse), masked (kv row >= vbs[j], missing second q block, or a k2q id

@@ -1,5 +1,5 @@
 // vsa_internal.cuh -- definitions shared by the CUDA translation units of libvsa.so: constants,
-// the workspace layouts, the per-head scale exponents of the fp16 operand copies, and the
+// the workspace layouts, the scale exponents of the fp16 operand copies, and the
 // host-side launch functions of every kernel.
 #pragma once
 
