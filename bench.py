@@ -421,6 +421,34 @@ def main():
     fpp = flop_per_pair(case.get("blk", 64))
     value = all_pairs * fpp / (total_ms / K / 1e3) / 1e12
 
+    # The same step captured once in a CUDA graph and replayed: one launch from the host per
+    # step instead of one per kernel (the backward enqueues only kernels and one memset on the
+    # caller's stream).
+    side = torch.cuda.Stream(device)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist, device)
+    torch.cuda.synchronize()
+    g0.record(stream)
+    for _ in range(K):
+        graph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist, device)
+    graph_ms = reduce_max(dist, g0.elapsed_time(g1), device) / K
+    assert vsa.vsa_read_device_error(ws) == 0
+    del graph
+
     # End to end through the public API with host buffers.  Every step uploads its inputs from
     # pinned host memory and downloads its three gradients; inputs and outputs are
     # double-buffered on the device and the copies run on their own streams, so the upload of
@@ -544,6 +572,9 @@ def main():
                      "tensor_pipe_active_ncu": main_kernel_profile(args.config)[1],
                      "peak_source": "%s bf16_tflops (burst); fp16 dense rate = bf16" % peak_src,
                      "frac_of_sustained": achieved / peak_sus},
+        "graph_step": {"ms": graph_ms, "tflops": all_pairs * fpp / (graph_ms / 1e3) / 1e12,
+                       "note": "the same step (inversion + backward) captured in one CUDA graph "
+                               "and replayed; not the headline value"},
         "fwd": {"ms": fwd_ms, "note": "operand producer, timed alone; not in the step"},
         "train_step": {"ms": train_ms, "tflops": train_tflops, "steps": K_train,
                        "note": "forward + inversion + backward through the autograd binding; "
