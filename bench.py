@@ -369,9 +369,9 @@ def main():
     k2q_num = torch.empty((B, H, nb), dtype=torch.int32, device=device)
     dq, dk, dv = (torch.empty_like(dev["q"]) for _ in range(3))
     ws = torch.empty(vsa.vsa_bwd_workspace_bytes(B, H, S), dtype=torch.uint8, device=device)
-    # invert, statistics (Delta, dQ zeroing, K/V to fp16, work order), convert_t (Q, dO), main,
-    # postprocess
-    kernels_per_step = 5
+    # invert (bitmap, compact), statistics (Delta, dQ zeroing, K/V to fp16, work order),
+    # convert_t (Q, dO to fp16), main, postprocess
+    kernels_per_step = 6
 
     def step(events=None, inv=None):
         if inv is not None:
