@@ -334,9 +334,10 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
   if ((e = record(events ? events->before_main : nullptr, s)) != cudaSuccess) return cuda_fail(e);
   if ((e = vsa::launch_bwd_main(a, s)) != cudaSuccess) return cuda_fail(e);
   if ((e = record(events ? events->after_main : nullptr, s)) != cudaSuccess) return cuda_fail(e);
+  const vsa::SplitPlan sp = vsa::bwd_split_plan(BH * a.nb);  // as launch_bwd_main splits
   if ((e = vsa::launch_postprocess(dqacc, absmax, BH, S, sm_scale,
                                    static_cast<__nv_bfloat16*>(dq), a.split_acc, a.split_row,
-                                   vsa::bwd_split_items(BH * a.nb), a.dk, a.dv, s)) != cudaSuccess)
+                                   sp.nsplit, sp.parts, a.dk, a.dv, s)) != cudaSuccess)
     return cuda_fail(e);
   if ((e = record(events ? events->end : nullptr, s)) != cudaSuccess) return cuda_fail(e);
   return VSA_OK;

@@ -24,8 +24,9 @@
 // Work items are claimed dynamically (queue.cuh).  With 128-token blocks an item is one of the
 // two 64-token kv tiles of a block, and each k2q entry supplies a whole q tile pair.  The last
 // items of the claim order (one per two CTAs) are handed out as four claims each, one per
-// quarter of their step lists, so the grid ends on short claims; a part stores its fp32 dK, dV
-// rows in a workspace slot of its own, and the postprocess adds the parts and writes bf16.
+// quarter of their step lists (halves when there are fewer than 8 items per SM: the kernel's
+// PARTS), so the grid ends on short claims; a part stores its fp32 dK, dV rows in a workspace
+// slot of its own, and the postprocess adds the parts and writes bf16.
 //
 // Roles (448 threads):
 //   warps 0-7  softmax: warps w and w+4 share TMEM lane quarter w (query rows 32w..32w+31 of the
@@ -132,15 +133,16 @@ struct Params {
   int nsel;   // sparse blocks per sequence (k2q rows per head)
   int tiles;  // 64-token tiles per sparse block: 1, or 2 for 128-token blocks
   int max_q;
-  // The last `nsplit` items (claim positions split0 ..) are each taken as SPLIT_PARTS claims,
-  // one per consecutive share of their step list, so that the grid's last claims are short.
-  // Part x stores its dK, dV rows (fp32, scaled; zeros for masked rows and for a part without
-  // steps) in split_acc[slot][x] ([dV, dK][64 kv rows][128]) and the item's first output row in
-  // split_row[slot]; the postprocess adds the parts in a fixed order and writes the bf16 rows.
+  // The last `nsplit` items (claim positions split0 ..) are each taken as PARTS claims, one
+  // per consecutive share of the item's step list, so that the grid's last claims are short.
+  // Part x of split item s stores its dK, dV rows (fp32, scaled; zeros for masked rows and for a
+  // part without steps) in slot s * PARTS + x of split_acc ([dV, dK][64 kv rows][128]), and the
+  // item's first output row in split_row[s]; the postprocess adds the parts in a fixed order and
+  // writes the bf16 rows.
   int split0, nsplit;
   float* split_acc;
   int32_t* split_row;
-  int total;  // claim positions: split0 + SPLIT_PARTS * nsplit
+  int total;  // claim positions: split0 + PARTS * nsplit
   float sm_scale;
   uint64_t wait_ns;  // limit of each pipeline wait
 };
@@ -151,15 +153,17 @@ struct Params {
 struct Item {
   int bh, j, sel, n;
   int first, np;  // this claim's steps: first .. first + np - 1 of the item's list
-  int slot, part;  // split slot and part, or -1 for a whole item
+  int slot, part;  // split item and part, or -1 for a whole item
   const int32_t* list;
 };
 
+// PARTS: claims per split item (the kernel's template argument, bwd_split_plan).
+template <int PARTS>
 __device__ __forceinline__ Item decode_item(const Params& p, int u) {
   int w = u, part = -1, slot = -1;
   if (u >= p.split0) {  // one part of a split item
-    slot = (u - p.split0) / SPLIT_PARTS;
-    part = (u - p.split0) % SPLIT_PARTS;
+    slot = (u - p.split0) / PARTS;
+    part = (u - p.split0) % PARTS;
     w = p.split0 + slot;
   }
   int half = 0, ws = w;
@@ -175,10 +179,10 @@ __device__ __forceinline__ Item decode_item(const Params& p, int u) {
   const int n = p.k2q_num[sel];
   it.n = n < 0 ? 0 : (n > p.max_q ? p.max_q : n);
   const int np = p.tiles == 2 ? it.n : (it.n + 1) >> 1;
-  // Part x takes steps [np x / P, np (x + 1) / P): shares differ by at most one, and a part
+  // Part x of P takes steps [np x / P, np (x + 1) / P): shares differ by at most one, and a part
   // may have none when the list is short.
-  it.first = part < 0 ? 0 : np * part / SPLIT_PARTS;
-  it.np = part < 0 ? np : np * (part + 1) / SPLIT_PARTS - it.first;
+  it.first = part < 0 ? 0 : np * part / PARTS;
+  it.np = part < 0 ? np : np * (part + 1) / PARTS - it.first;
   it.slot = slot;
   it.part = part;
   it.list = p.k2q_idx + static_cast<size_t>(sel) * p.max_q;
@@ -269,6 +273,7 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+template <int PARTS>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_q2,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -354,7 +359,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         break;
       }
       if (w >= p.total) break;  // the end marker
-      const Item it = decode_item(p, w);
+      const Item it = decode_item<PARTS>(p, w);
       uint32_t bad = 0;
       if (lane == 0 && p.k2q_num[it.sel] != it.n) bad |= VSA_DEVERR_K2Q_COUNT;
       for (int x = lane; x < it.n; x += 32) {
@@ -511,7 +516,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         break;
       }
       if (w >= p.total) break;
-      const Item it = decode_item(p, w);
+      const Item it = decode_item<PARTS>(p, w);
       if (it.np == 0) continue;  // nothing to compute (an unselected block, or an empty part)
       const int np = it.np;
       if (!mbar_wait_warp(bar(KV_FULL), itc & 1u, abort, p.wait_ns)) {
@@ -602,7 +607,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         break;
       }
       if (w >= p.total) break;
-      const Item it = decode_item(p, w);
+      const Item it = decode_item<PARTS>(p, w);
       if (it.np == 0) continue;  // nothing to compute (an unselected block, or an empty part)
       const int vb = clamp_vbs(p.vbs[it.j]);
       const ItemScales es = item_scales(p, it);
@@ -711,7 +716,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         break;
       }
       if (w >= p.total) break;
-      const Item it = decode_item(p, w);
+      const Item it = decode_item<PARTS>(p, w);
       const size_t row_kv = static_cast<size_t>(it.bh) * S + static_cast<size_t>(it.j) * BLOCK;
       __nv_bfloat16* dk_out = p.dk + row_kv * HEAD_DIM + d;
       __nv_bfloat16* dv_out = p.dv + row_kv * HEAD_DIM + d;
@@ -737,7 +742,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       float* acc = nullptr;
       if (it.slot >= 0)
         acc = p.split_acc +
-              static_cast<size_t>(it.slot * SPLIT_PARTS + it.part) * (2 * BLOCK * HEAD_DIM) + d;
+              static_cast<size_t>(it.slot * PARTS + it.part) * (2 * BLOCK * HEAD_DIM) + d;
       // The item's dV^T and dK^T, complete once its last dK^T is (before its last dQ^T): read
       // out before the last step's dQ^T is drained, so that the next item's dV^T can start.
       auto read_acc = [&]() -> bool {
@@ -858,15 +863,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 }  // namespace
 
-int bwd_split_items(int items) {
+SplitPlan bwd_split_plan(int items) {
   // SPLIT_CLAIMS split claims per CTA on average: enough short claims at the end of the grid
-  // for the CTAs that finish their whole items early to even out the finishing times.
+  // for the CTAs that finish their whole items early to even out the finishing times, as far as
+  // the workspace's slots go.  With fewer than 8 items per SM (about 8 steps each at 4k tokens,
+  // 25 %) a quarter of an item costs about as much in its item boundary as it computes, and
+  // halves measured faster (71.7 against 75.8 µs at 4k; at 32k halves were 0.5 % slower).
   const int sms = device_sm_count();
   const int grid = items < sms ? items : sms;
-  const int want =
-      SPLIT_CLAIMS * grid / SPLIT_PARTS > 0 ? SPLIT_CLAIMS * grid / SPLIT_PARTS : 1;
-  const int cap = split_capacity(items);
-  return want < cap ? want : cap;
+  SplitPlan sp;
+  sp.parts = static_cast<long>(items) < 8L * sms ? 2 : SPLIT_PARTS;
+  const int want = SPLIT_CLAIMS * grid / sp.parts > 0 ? SPLIT_CLAIMS * grid / sp.parts : 1;
+  const int cap = static_cast<int>(split_slots(items) / sp.parts);
+  sp.nsplit = want < cap ? want : cap;
+  return sp;
 }
 
 cudaError_t launch_bwd_main(const BwdMainArgs& a, cudaStream_t stream) {
@@ -882,9 +892,12 @@ cudaError_t launch_bwd_main(const BwdMainArgs& a, cudaStream_t stream) {
   if ((e = make_tmap_tiles_t(&tdo2, a.do16, rows, 2)) != cudaSuccess) return e;
   if ((e = make_tmap_rows128_f16_halves(&tk, a.k16, rows, 64)) != cudaSuccess) return e;
   if ((e = make_tmap_rows128_f16_halves(&tv, a.v16, rows, 64)) != cudaSuccess) return e;
-  static std::atomic<uint64_t> smem_set{0};
-  if ((e = ensure_smem_limit(bwd_main_kernel, static_cast<int>(SMEM_BYTES), smem_set)) !=
-      cudaSuccess)
+  const int items = a.B * a.H * a.nb;
+  const SplitPlan sp = bwd_split_plan(items);
+  auto kernel = sp.parts == 2 ? bwd_main_kernel<2> : bwd_main_kernel<SPLIT_PARTS>;
+  static std::atomic<uint64_t> smem_set2{0}, smem_set4{0};
+  if ((e = ensure_smem_limit(kernel, static_cast<int>(SMEM_BYTES),
+                             sp.parts == 2 ? smem_set2 : smem_set4)) != cudaSuccess)
     return e;
   Params p{};
   p.k2q_idx = a.k2q_idx;
@@ -907,15 +920,14 @@ cudaError_t launch_bwd_main(const BwdMainArgs& a, cudaStream_t stream) {
   p.max_q = a.max_q;
   p.sm_scale = a.sm_scale;
   p.wait_ns = a.wait_ns;
-  const int items = a.B * a.H * a.nb;
   const int sms = device_sm_count();
   const int grid = items < sms ? items : sms;
-  p.nsplit = bwd_split_items(items);
+  p.nsplit = sp.nsplit;
   p.split0 = items - p.nsplit;
-  p.total = items + (SPLIT_PARTS - 1) * p.nsplit;
+  p.total = items + (sp.parts - 1) * p.nsplit;
   p.split_acc = a.split_acc;
   p.split_row = a.split_row;
-  bwd_main_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tq, tq2, tk, tv, tdo, tdo2, tdq, p);
+  kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tq, tq2, tk, tv, tdo, tdo2, tdq, p);
   return cudaGetLastError();
 }
 

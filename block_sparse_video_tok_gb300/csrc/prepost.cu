@@ -318,6 +318,7 @@ __global__ void __launch_bounds__(256) order_kernel(const int32_t* __restrict__ 
   }
 }
 
+template <int PARTS>
 __global__ void __launch_bounds__(256) postprocess_kernel(
     const float4* __restrict__ dqacc, const uint32_t* __restrict__ absmax, size_t chunks_per_head,
     size_t total_chunks, float sm_scale, uint4* __restrict__ dq,
@@ -339,19 +340,20 @@ __global__ void __launch_bounds__(256) postprocess_kernel(
                        *reinterpret_cast<const uint32_t*>(&r2),
                        *reinterpret_cast<const uint32_t*>(&r3));
   }
-  // Split items of the main kernel: part x of slot s holds [dV, dK][64 kv rows][128] fp32,
-  // already scaled (rows past the block's valid size hold zeros); 16 chunks of 8 per row.  The
-  // parts are added in order, so the sums do not depend on which part finished first.
+  // Split items of the main kernel: part x of split item s holds [dV, dK][64 kv rows][128] fp32
+  // in slot s * PARTS + x, already scaled (rows past the block's valid size hold zeros); 16
+  // chunks of 8 per row.  The parts are added in order, so the sums do not depend on which part
+  // finished first.
   for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < split_chunks;
        c += gridDim.x * blockDim.x) {
     const int slot = c / (2 * BLOCK * 16), rem = c % (2 * BLOCK * 16);
     const bool is_dk = rem >= BLOCK * 16;
     const int t = (rem / 16) % BLOCK, d8 = rem % 16;
     const float4* part =
-        split_acc + (static_cast<size_t>(slot) * SPLIT_PARTS * 2 * BLOCK * 16 + rem) * 2;
+        split_acc + (static_cast<size_t>(slot) * PARTS * 2 * BLOCK * 16 + rem) * 2;
     float4 a = part[0], b = part[1];
 #pragma unroll
-    for (int x = 1; x < SPLIT_PARTS; ++x) {
+    for (int x = 1; x < PARTS; ++x) {
       const float4 a2 = part[x * 2 * BLOCK * 16 * 2], b2 = part[x * 2 * BLOCK * 16 * 2 + 1];
       a = make_float4(a.x + a2.x, a.y + a2.y, a.z + a2.z, a.w + a2.w);
       b = make_float4(b.x + b2.x, b.y + b2.y, b.z + b2.z, b.w + b2.w);
@@ -466,12 +468,14 @@ cudaError_t launch_order(const int32_t* k2q_num, int BH, int nb, int max_q, int3
 
 cudaError_t launch_postprocess(const float* dqacc, const uint32_t* absmax, int BH, int S,
                                float sm_scale, __nv_bfloat16* dq, const float* split_acc,
-                               const int32_t* split_row, int nsplit, __nv_bfloat16* dk,
+                               const int32_t* split_row, int nsplit, int parts, __nv_bfloat16* dk,
                                __nv_bfloat16* dv, cudaStream_t stream) {
   const size_t per_head = static_cast<size_t>(S) * HEAD_DIM / 8;
   const size_t total = per_head * BH;
   const int split_chunks = nsplit * 2 * BLOCK * (HEAD_DIM / 8);
-  postprocess_kernel<<<grid_for(total, 256, 8), 256, 0, stream>>>(
+  if (parts != 2 && parts != SPLIT_PARTS) return cudaErrorInvalidValue;
+  auto kernel = parts == 2 ? postprocess_kernel<2> : postprocess_kernel<SPLIT_PARTS>;
+  kernel<<<grid_for(total, 256, 8), 256, 0, stream>>>(
       reinterpret_cast<const float4*>(dqacc), absmax, per_head, total, sm_scale,
       reinterpret_cast<uint4*>(dq), reinterpret_cast<const float4*>(split_acc), split_row,
       split_chunks, reinterpret_cast<uint4*>(dk), reinterpret_cast<uint4*>(dv));

@@ -57,23 +57,16 @@ struct BwdLayout {
       v16, do16, total;
 };
 
-// The backward's main kernel hands out its last items as SPLIT_PARTS claims each (shares of the
-// item's step list), so that the grid ends on short claims.  split_capacity(W): how many of the
-// W = B * H * S / 64 items the workspace has room to split, SPLIT_PARTS slots of 64 KB each,
-// at most a quarter of W slots in all (about 256 bytes per token row) and SPLIT_MAX_SLOTS.
-#ifndef VSA_SPLIT_PARTS
-#define VSA_SPLIT_PARTS 4
-#endif
-constexpr int SPLIT_PARTS = VSA_SPLIT_PARTS;
-#ifndef VSA_SPLIT_CLAIMS
-#define VSA_SPLIT_CLAIMS 2
-#endif
-constexpr int SPLIT_CLAIMS = VSA_SPLIT_CLAIMS;  // split claims per CTA, on average
+// The backward's main kernel hands out its last items as `parts` claims each (consecutive
+// shares of the item's step list), so that the grid ends on short claims: quarters
+// (SPLIT_PARTS), or halves when there are fewer than 8 items per SM (bwd_split_plan).  Each part
+// fills a slot of 64 KB ([dV, dK][64][128] fp32); split_slots(W): the workspace's slots for W =
+// B * H * S / 64 items, a quarter of W (about 256 bytes per token row) and at most
+// SPLIT_MAX_SLOTS.
+constexpr int SPLIT_PARTS = 4;
+constexpr int SPLIT_CLAIMS = 2;  // split claims per CTA, on average
 constexpr int SPLIT_MAX_SLOTS = 512;
-inline int split_capacity(long W) {
-  const long slots = W / 4 < SPLIT_MAX_SLOTS ? W / 4 : SPLIT_MAX_SLOTS;
-  return static_cast<int>(slots / SPLIT_PARTS);
-}
+inline long split_slots(long W) { return W / 4 < SPLIT_MAX_SLOTS ? W / 4 : SPLIT_MAX_SLOTS; }
 struct FwdLayout {
   size_t err, sched, absmax, bitmap, vbs64, v16, total;
 };
@@ -91,12 +84,13 @@ inline BwdLayout bwd_layout(long B, long H, long S) {
   off = align_up(off + bh * HEAD_STATS * sizeof(uint32_t), 1024);
   L.tstat = off;
   off = align_up(off + bh * nb * TILE_STATS * sizeof(uint32_t), 1024);
-  // Split items: the first output row, and [parts][dV, dK][64][128] fp32 rows each.
-  const size_t nsplit = static_cast<size_t>(split_capacity(static_cast<long>(bh * nb)));
+  // Split items: the first output row of each (at most one item per slot), and the parts'
+  // [dV, dK][64][128] fp32 rows, one slot each.
+  const size_t slots = static_cast<size_t>(split_slots(static_cast<long>(bh * nb)));
   L.split_row = off;
-  off = align_up(off + nsplit * sizeof(int32_t), 1024);
+  off = align_up(off + slots * sizeof(int32_t), 1024);
   L.split_acc = off;
-  off = align_up(off + nsplit * SPLIT_PARTS * 2 * BLOCK * HEAD_DIM * sizeof(float), 1024);
+  off = align_up(off + slots * 2 * BLOCK * HEAD_DIM * sizeof(float), 1024);
   L.delta = off;
   off = align_up(off + rows * sizeof(float), 1024);
   L.order = off;
@@ -253,11 +247,11 @@ cudaError_t launch_convert_t(const __nv_bfloat16* q, const __nv_bfloat16* dout, 
 cudaError_t launch_order(const int32_t* k2q_num, int BH, int nb, int max_q, int32_t* order,
                          cudaStream_t stream);
 
-// dQ = bf16(dqacc * scale); then the bf16 dV, dK rows of the main kernel's `nsplit` split items:
-// the sum of their SPLIT_PARTS fp32 parts, added in part order.
+// dQ = bf16(dqacc * scale); then the bf16 dV, dK rows of the main kernel's split items
+// (bwd_split_plan): the sum of the `parts` fp32 parts of each, added in part order.
 cudaError_t launch_postprocess(const float* dqacc, const uint32_t* absmax, int BH, int S,
                                float sm_scale, __nv_bfloat16* dq, const float* split_acc,
-                               const int32_t* split_row, int nsplit, __nv_bfloat16* dk,
+                               const int32_t* split_row, int nsplit, int parts, __nv_bfloat16* dk,
                                __nv_bfloat16* dv, cudaStream_t stream);
 
 struct BwdMainArgs {
@@ -275,8 +269,8 @@ struct BwdMainArgs {
   __nv_bfloat16* dv;
   uint32_t* err;
   int32_t* sched;  // zeroed work counter
-  float* split_acc;    // split_capacity(B * H * nb) x SPLIT_PARTS slots of [2][64][128]
-  int32_t* split_row;  // [split_capacity]
+  float* split_acc;    // split_slots(B * H * nb) slots of [2][64][128]
+  int32_t* split_row;  // [split_slots]: the first output row of each split item
   int B, H, S;
   int nb;     // 64-token tiles per sequence (kv items per head = nb)
   int nsel;   // sparse blocks per sequence (rows of k2q per head); nb = nsel * tiles
@@ -286,8 +280,12 @@ struct BwdMainArgs {
   uint64_t wait_ns;  // limit of each pipeline wait
 };
 cudaError_t launch_bwd_main(const BwdMainArgs& a, cudaStream_t stream);
-// Items the main kernel splits in two for `items` work items on this device.
-int bwd_split_items(int items);
+// How the main kernel splits its last items for `items` work items on this device: `nsplit`
+// items, `parts` claims each.
+struct SplitPlan {
+  int parts, nsplit;
+};
+SplitPlan bwd_split_plan(int items);
 
 // Selection bitmap of the forward at 64-token granularity: [BH, nb * tiles, ceil(nb * tiles / 32)]
 // bits from q2k rows that count blocks of `tiles` 64-token tiles (1 or 2).

@@ -143,12 +143,16 @@ SMALL_CASES["blk128_odd_nb_topk3"] = lambda: wl.make_case(1, 2, 5, 3, vbs="ragge
 SMALL_CASES["blk128_batch2_zero_kv"] = lambda: wl.make_case(2, 2, 6, 2, vbs="ragged65", seed=33,
                                                            kv_pool=[0, 2, 3, 5], blk=128)
 
-# The backward hands out the last items of its grid in parts (shares of an item's step list).
-# With 16 heads of 16 kv blocks the last 16 items are split; with 3 q blocks per row most items
-# have two steps, so some parts have none, and kv blocks 14 and 15 (selected by no q block) give
-# split items without any step.
+# The backward hands out the last items of its grid in parts (shares of an item's step list:
+# halves with fewer than 8 items per SM, as in these cases, quarters otherwise).  With 16 heads
+# of 16 kv blocks the last 32 items are split; with 3 q blocks per row most items have two
+# steps, so some parts have one and some none, and kv blocks 14 and 15 (selected by no q block)
+# give split items without any step.
 SMALL_CASES["split_parts_short_lists"] = lambda: wl.make_case(1, 16, 16, 3, vbs="ragged32", seed=41,
                                                              kv_pool=list(range(14)))
+# 4 heads of 64 kv blocks, 40 selected per q block: the 32 split items (the shortest lists of the
+# last head, last in the sorted order) have 14 to 20 steps, 7 to 10 per part.
+SMALL_CASES["split_parts_long_lists"] = lambda: wl.make_case(1, 4, 64, 40, vbs="ragged33", seed=42)
 
 def _outliers(case, which="qkvd", factor=1e3, seed=0):
     """One element per (b, h) head of each named tensor (q, k, v, d = dO) replaced by
