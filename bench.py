@@ -496,7 +496,9 @@ def main():
     for k_ in range(3):
         e2e_step(k_)
     torch.cuda.synchronize()
-    K_e2e = max(3, min(K, 50))
+    # As many steps as the timed loop (at least 50), within about 3 s: the first upload and the
+    # last download are not overlapped, and the steps spread them as in the device-timed loop.
+    K_e2e = max(3, min(max(K, 50), int(3000.0 / max(total_ms / K, 1e-3))))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist, device)
     torch.cuda.synchronize()
