@@ -329,6 +329,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tm_do2);
     tma_prefetch_desc(&tm_dq);
   }
+  grid_dependency_wait();  // the preprocess's outputs (programmatic dependent launch)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -927,8 +928,8 @@ cudaError_t launch_bwd_main(const BwdMainArgs& a, cudaStream_t stream) {
   p.total = items + (sp.parts - 1) * p.nsplit;
   p.split_acc = a.split_acc;
   p.split_row = a.split_row;
-  kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tq, tq2, tk, tv, tdo, tdo2, tdq, p);
-  return cudaGetLastError();
+  return launch_dependent(kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, stream, tq, tq2, tk,
+                          tv, tdo, tdo2, tdq, p);
 }
 
 }  // namespace vsa

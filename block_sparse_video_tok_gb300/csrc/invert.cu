@@ -157,6 +157,7 @@ __global__ void __launch_bounds__(BM_THREADS) invert_bitmap_kernel(
 __global__ void __launch_bounds__(CP_WARPS * 32) invert_compact_kernel(int nb, long rows,
                                                                        int32_t* __restrict__ k2q_idx,
                                                                        int32_t* __restrict__ k2q_num) {
+  grid_dependency_wait();
   extern __shared__ uint32_t tails[];  // [CP_WARPS][words]
   const int nq = nb, words = (nq + 31) >> 5;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -218,9 +219,8 @@ cudaError_t launch_invert(const int32_t* q2k_idx, const int32_t* q2k_num, int to
     const long rows = static_cast<long>(BH) * nb;
     const long want = (rows + CP_WARPS - 1) / CP_WARPS;
     const long cap = 16L * device_sm_count();
-    invert_compact_kernel<<<static_cast<unsigned>(want < cap ? want : cap), CP_WARPS * 32,
-                            cp_smem, stream>>>(nb, rows, k2q_idx, k2q_num);
-    return cudaGetLastError();
+    return launch_dependent(invert_compact_kernel, dim3(static_cast<unsigned>(want < cap ? want : cap)),
+                            dim3(CP_WARPS * 32), cp_smem, stream, nb, rows, k2q_idx, k2q_num);
   }
   const size_t col_bytes = static_cast<size_t>((nb + 31) / 32) * sizeof(uint32_t);
   // Widest slice shared memory holds, but no wider than two waves of CTAs need.

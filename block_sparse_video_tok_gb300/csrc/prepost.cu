@@ -264,6 +264,7 @@ struct ConvertTPack {
 
 __global__ void __launch_bounds__(256) convert_t_kernel(ConvertTPack pk, int S,
                                                         const uint32_t* __restrict__ absmax) {
+  grid_dependency_wait();
   constexpr int LD = 130;
   __shared__ __half tl[BLOCK * LD];
   const int t = blockIdx.z, bh = blockIdx.y, tile = blockIdx.x, nt = gridDim.x;
@@ -324,6 +325,7 @@ __global__ void __launch_bounds__(256) postprocess_kernel(
     size_t total_chunks, float sm_scale, uint4* __restrict__ dq,
     const float4* __restrict__ split_acc, const int32_t* __restrict__ split_row, int split_chunks,
     uint4* __restrict__ dk, uint4* __restrict__ dv) {
+  grid_dependency_wait();
   for (size_t c = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; c < total_chunks;
        c += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const int bh = static_cast<int>(c / chunks_per_head);
@@ -454,8 +456,7 @@ cudaError_t launch_convert_t(const __nv_bfloat16* q, const __nv_bfloat16* dout, 
   pk.slot[0] = 0;
   pk.slot[1] = 3;
   dim3 grid(static_cast<unsigned>(S / BLOCK), static_cast<unsigned>(BH), 2u);
-  convert_t_kernel<<<grid, 256, 0, stream>>>(pk, S, absmax);
-  return cudaGetLastError();
+  return launch_dependent(convert_t_kernel, grid, dim3(256), 0, stream, pk, S, absmax);
 }
 
 cudaError_t launch_order(const int32_t* k2q_num, int BH, int nb, int max_q, int32_t* order,
@@ -475,11 +476,10 @@ cudaError_t launch_postprocess(const float* dqacc, const uint32_t* absmax, int B
   const int split_chunks = nsplit * 2 * BLOCK * (HEAD_DIM / 8);
   if (parts != 2 && parts != SPLIT_PARTS) return cudaErrorInvalidValue;
   auto kernel = parts == 2 ? postprocess_kernel<2> : postprocess_kernel<SPLIT_PARTS>;
-  kernel<<<grid_for(total, 256, 8), 256, 0, stream>>>(
+  return launch_dependent(kernel, dim3(grid_for(total, 256, 8)), dim3(256), 0, stream,
       reinterpret_cast<const float4*>(dqacc), absmax, per_head, total, sm_scale,
       reinterpret_cast<uint4*>(dq), reinterpret_cast<const float4*>(split_acc), split_row,
       split_chunks, reinterpret_cast<uint4*>(dk), reinterpret_cast<uint4*>(dv));
-  return cudaGetLastError();
 }
 
 cudaError_t launch_fwd_bitmap(const int32_t* q2k_idx, const int32_t* q2k_num, int topk, int BH,

@@ -195,7 +195,32 @@ __host__ __device__ inline int ds_exponent(float do_norm, float v_norm, float de
   return clamp_exponent(13 - f, 60);
 }
 
+// Programmatic dependent launch: wait until the previous grid on the stream has completed and its
+// memory operations are visible (a no-op when the kernel was launched without the attribute).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------- launches
+// `kernel` launched so that it may start before the previous kernel on `stream` has finished
+// (programmatic dependent launch); it calls grid_dependency_wait() before it touches global
+// memory that the previous kernels write or read.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Each returns cudaSuccess or the launch error.  `stream` is the caller's stream.
 
 cudaError_t launch_invert(const int32_t* q2k_idx, const int32_t* q2k_num, int topk, int BH,
