@@ -283,6 +283,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tm_k2);
     tma_prefetch_desc(&tm_v);
   }
+  grid_dependency_wait();  // the V copy and the bitmap (programmatic dependent launch)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -798,8 +799,8 @@ cudaError_t launch_fwd_main(const FwdMainArgs& a, cudaStream_t stream) {
   p.wait_ns = a.wait_ns;
   const int sms = device_sm_count();
   const int grid = p.total < sms ? p.total : sms;
-  fwd_main_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tq, tq2, tk, tk2, tv, p);
-  return cudaGetLastError();
+  return launch_dependent(fwd_main_kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, stream, tq,
+                          tq2, tk, tk2, tv, p);
 }
 
 }  // namespace vsa

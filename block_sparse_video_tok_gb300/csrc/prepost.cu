@@ -237,6 +237,7 @@ struct ConvertPack {
 __global__ void __launch_bounds__(256) convert_kernel(ConvertPack pk, size_t chunks_per_head,
                                                       size_t total_chunks,
                                                       const uint32_t* __restrict__ absmax) {
+  grid_dependency_wait();
   const int t = blockIdx.y;
   const uint4* __restrict__ src = t == 0 ? pk.src[0] : t == 1 ? pk.src[1] : t == 2 ? pk.src[2] : pk.src[3];
   uint4* __restrict__ dst = t == 0 ? pk.dst[0] : t == 1 ? pk.dst[1] : t == 2 ? pk.dst[2] : pk.dst[3];
@@ -381,6 +382,7 @@ __global__ void __launch_bounds__(256) fwd_bitmap_kernel(const int32_t* __restri
                                                          size_t entries,
                                                          uint32_t* __restrict__ bitmap,
                                                          uint32_t* err) {
+  grid_dependency_wait();
   const int nt = nb * tiles;
   const int words = (nt + 31) >> 5;
   uint32_t bad = 0;
@@ -441,8 +443,7 @@ cudaError_t launch_convert(const __nv_bfloat16* const* src, __half* const* dst, 
   const size_t per_head = static_cast<size_t>(S) * HEAD_DIM / 8;
   const size_t total = per_head * BH;
   dim3 grid(static_cast<unsigned>(grid_for(total, 256, 8)), static_cast<unsigned>(count));
-  convert_kernel<<<grid, 256, 0, stream>>>(pk, per_head, total, absmax);
-  return cudaGetLastError();
+  return launch_dependent(convert_kernel, grid, dim3(256), 0, stream, pk, per_head, total, absmax);
 }
 
 cudaError_t launch_convert_t(const __nv_bfloat16* q, const __nv_bfloat16* dout, __half* q16t,
@@ -486,9 +487,8 @@ cudaError_t launch_fwd_bitmap(const int32_t* q2k_idx, const int32_t* q2k_num, in
                               int nb, int tiles, uint32_t* bitmap, uint32_t* err,
                               cudaStream_t stream) {
   const size_t entries = static_cast<size_t>(BH) * nb * topk;
-  fwd_bitmap_kernel<<<grid_for(entries, 256, 4), 256, 0, stream>>>(q2k_idx, q2k_num, topk, nb,
-                                                                    tiles, entries, bitmap, err);
-  return cudaGetLastError();
+  return launch_dependent(fwd_bitmap_kernel, dim3(grid_for(entries, 256, 4)), dim3(256), 0, stream,
+                          q2k_idx, q2k_num, topk, nb, tiles, entries, bitmap, err);
 }
 
 }  // namespace vsa
