@@ -369,9 +369,9 @@ def main():
     k2q_num = torch.empty((B, H, nb), dtype=torch.int32, device=device)
     dq, dk, dv = (torch.empty_like(dev["q"]) for _ in range(3))
     ws = torch.empty(vsa.vsa_bwd_workspace_bytes(B, H, S), dtype=torch.uint8, device=device)
-    # invert (bitmap, compact), statistics (Delta, dQ zeroing, K/V to fp16, work order),
-    # convert_t (Q, dO to fp16), main, postprocess
-    kernels_per_step = 6
+    # invert (bitmap, compact), zeroing of the workspace header, statistics (Delta, dQ zeroing,
+    # K/V to fp16, work order), convert_t (Q, dO to fp16), main, postprocess
+    kernels_per_step = 7
 
     def step(events=None, inv=None):
         if inv is not None:
@@ -422,7 +422,7 @@ def main():
     value = all_pairs * fpp / (total_ms / K / 1e3) / 1e12
 
     # The same step captured once in a CUDA graph and replayed: one launch from the host per
-    # step instead of one per kernel (the backward enqueues only kernels and one memset on the
+    # step instead of one per kernel (the inversion and the backward enqueue only kernels on the
     # caller's stream).
     side = torch.cuda.Stream(device)
     side.wait_stream(stream)

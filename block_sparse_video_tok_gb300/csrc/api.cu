@@ -177,7 +177,7 @@ vsa_status vsa_fwd(const void* q, const void* k, const void* v, const int32_t* q
   const auto* kb = static_cast<const __nv_bfloat16*>(k);
   const auto* vb = static_cast<const __nv_bfloat16*>(v);
 
-  cudaError_t e = cudaMemsetAsync(workspace, 0, L.v16, s);  // header, maxima, bitmap
+  cudaError_t e = vsa::launch_zero(workspace, L.v16, s);  // header, maxima, bitmap
   if (e != cudaSuccess) return cuda_fail(e);
   // S = Q K^T takes the bf16 Q and K as given; only V needs the scaled fp16 copy that P.V (fp16
   // P) takes, so only V's maximum is scanned.
@@ -274,7 +274,7 @@ vsa_status vsa_bwd_timed(const void* dout, const void* q, const void* k, const v
   cudaError_t e = record(events ? events->start : nullptr, s);
   if (e != cudaSuccess) return cuda_fail(e);
   // Header, work counter, head and tile statistics and the split items' rows.
-  if ((e = cudaMemsetAsync(workspace, 0, L.split_acc, s)) != cudaSuccess) return cuda_fail(e);
+  if ((e = vsa::launch_zero(workspace, L.split_acc, s)) != cudaSuccess) return cuda_fail(e);
   vsa::PreExtras x{};
   x.vbs = vbs;
   x.nb = nb;

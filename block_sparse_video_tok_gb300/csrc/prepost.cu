@@ -99,10 +99,22 @@ __device__ __forceinline__ int order_position(const int32_t* __restrict__ counts
 // rows per warp per iteration, 64 rows per CTA.
 constexpr int PRE_THREADS = 256;
 
+// Zeroes n 16-byte words from p on (the workspace's header, statistics and split rows, which the
+// next kernels accumulate into), as a kernel so that a step's launches chain as programmatic
+// dependent launches; the previous call's postprocess may still be reading them, hence the wait.
+__global__ void __launch_bounds__(256) zero_kernel(uint4* __restrict__ p, size_t n) {
+  grid_dependency_wait();
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x)
+    p[i] = z;
+}
+
 __global__ void __launch_bounds__(PRE_THREADS, 4) absmax_delta_kernel(
     const uint4* __restrict__ q, const uint4* __restrict__ k, const uint4* __restrict__ v,
     const uint4* __restrict__ dout, const uint4* __restrict__ o, int S, uint32_t* absmax,
     float* __restrict__ delta, float4* __restrict__ dqacc, PreExtras x) {
+  grid_dependency_wait();
   // A small job spread over the whole grid: the clamped valid size of every 64-token kv tile
   // (64-token tile t of block t / tiles).
   {
@@ -424,11 +436,18 @@ cudaError_t launch_absmax_delta(const __nv_bfloat16* q, const __nv_bfloat16* k,
                                 float* delta, float* dqacc, const PreExtras& x,
                                 cudaStream_t stream) {
   dim3 grid(static_cast<unsigned>(S / BLOCK), static_cast<unsigned>(BH));
-  absmax_delta_kernel<<<grid, PRE_THREADS, 0, stream>>>(
-      reinterpret_cast<const uint4*>(q), reinterpret_cast<const uint4*>(k),
-      reinterpret_cast<const uint4*>(v), reinterpret_cast<const uint4*>(dout),
-      reinterpret_cast<const uint4*>(o), S, absmax, delta, reinterpret_cast<float4*>(dqacc), x);
-  return cudaGetLastError();
+  return launch_dependent(
+      absmax_delta_kernel, grid, dim3(PRE_THREADS), 0, stream, reinterpret_cast<const uint4*>(q),
+      reinterpret_cast<const uint4*>(k), reinterpret_cast<const uint4*>(v),
+      reinterpret_cast<const uint4*>(dout), reinterpret_cast<const uint4*>(o), S, absmax, delta,
+      reinterpret_cast<float4*>(dqacc), x);
+}
+
+cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t stream) {
+  const size_t n = bytes / 16;
+  if (n == 0) return cudaSuccess;
+  return launch_dependent(zero_kernel, dim3(grid_for(n, 256, 4)), dim3(256), 0, stream,
+                          static_cast<uint4*>(p), n);
 }
 
 cudaError_t launch_convert(const __nv_bfloat16* const* src, __half* const* dst, int count, int BH,

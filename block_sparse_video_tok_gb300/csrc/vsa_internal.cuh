@@ -223,6 +223,9 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
 
 // Each returns cudaSuccess or the launch error.  `stream` is the caller's stream.
 
+// Zeroes `bytes` (a multiple of 16) from `p` (16-byte aligned) on.
+cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t stream);
+
 cudaError_t launch_invert(const int32_t* q2k_idx, const int32_t* q2k_num, int topk, int BH,
                           int nb, int32_t* k2q_idx, int32_t* k2q_num, uint32_t* err,
                           cudaStream_t stream);

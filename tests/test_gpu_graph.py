@@ -1,8 +1,8 @@
 """The inversion and the backward captured in one CUDA graph (torch.cuda.graph) and replayed.
 
 A caller that runs many small layers launches the whole backward as one graph instead of a
-handful of kernel launches (and one memset) from the host.  Capture needs every launch on the
-caller's stream and no host synchronisation inside; replay must re-read the inputs, so the graph
+handful of kernel launches from the host.  Capture needs every launch on the caller's stream and
+no host synchronisation inside; replay must re-read the inputs, so the graph
 is checked on the inputs it was captured with and again after new inputs (another selection,
 other activations) have been copied into the same buffers.  dK and dV involve no atomics and
 must equal the eager result bit for bit; dQ's fp32 partial sums are added in a varying order
