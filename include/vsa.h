@@ -33,10 +33,10 @@
  *     The library never allocates, keeps no per-call state between calls (the wait limit of
  *     vsa_set_wait_limit_ns is a process-wide setting) and never synchronises the stream except
  *     in vsa_read_device_error and vsa_bwd_no_alloc_device_error.  `stream` is a cudaStream_t
- *     (NULL = legacy default stream).  Work is enqueued on it in order (kernels only; every
- *     kernel after a call's first is a programmatic dependent launch that waits, before it
- *     touches memory, until the previous work on the stream has completed, so the caller's own
- *     work before and after keeps its order); the call returns before the GPU finishes and
+ *     (NULL = legacy default stream).  Work is enqueued on it in order (kernels only; all but
+ *     the inversion's first are programmatic dependent launches, each of which waits, before
+ *     it touches memory, until the previous work on the stream has completed, so the caller's
+ *     own work before and after keeps its order); the call returns before the GPU finishes and
  *     may be captured in a CUDA graph.
  *   - Errors: problems visible on the host (null pointer, bad size, misalignment, too small a
  *     workspace, non-finite sm_scale, wrong device) return a status before anything is
