@@ -34,7 +34,8 @@
  *     vsa_set_wait_limit_ns is a process-wide setting) and never synchronises the stream except
  *     in vsa_read_device_error and vsa_bwd_no_alloc_device_error.  `stream` is a cudaStream_t
  *     (NULL = legacy default stream).  Work is enqueued on it in order (kernels only; all but
- *     the inversion's first are programmatic dependent launches, each of which waits, before
+ *     the first of vsa_invert_indices and the one of vsa_work_order are programmatic dependent
+ *     launches, each of which waits, before
  *     it touches memory, until the previous work on the stream has completed, so the caller's
  *     own work before and after keeps its order); the call returns before the GPU finishes and
  *     may be captured in a CUDA graph.
