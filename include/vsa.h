@@ -35,10 +35,9 @@
  *     in vsa_read_device_error and vsa_bwd_no_alloc_device_error.  `stream` is a cudaStream_t
  *     (NULL = legacy default stream).  Work is enqueued on it in order (kernels only; all but
  *     the first of vsa_invert_indices and the one of vsa_work_order are programmatic dependent
- *     launches, each of which waits, before
- *     it touches memory, until the previous work on the stream has completed, so the caller's
- *     own work before and after keeps its order); the call returns before the GPU finishes and
- *     may be captured in a CUDA graph.
+ *     launches, each of which waits, before it touches memory, until the previous work on the
+ *     stream has completed, so the caller's own work before and after keeps its order); the
+ *     call returns before the GPU finishes and may be captured in a CUDA graph.
  *   - Errors: problems visible on the host (null pointer, bad size, misalignment, too small a
  *     workspace, non-finite sm_scale, wrong device) return a status before anything is
  *     enqueued (an unsupported configuration is an error, never a silently wrong result:
